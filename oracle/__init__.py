@@ -1,0 +1,10 @@
+"""fp64 CPU oracle of the fused normalization block (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. It shares no code with the CUDA
+library and imports nothing from ``normalization_fwd_gb300``.
+"""
+
+from .norm import LAYERNORM, RMSNORM, norm_bwd, norm_fwd, round_to_format
+
+__all__ = ["LAYERNORM", "RMSNORM", "norm_fwd", "norm_bwd", "round_to_format"]
