@@ -1,0 +1,459 @@
+"""Benchmark of the fused normalization block (forward + backward step).
+
+One step is the whole hot path on one batch: ln_fwd (bias + residual add,
+LayerNorm, amax) followed by ln_bwd (dx, dgamma, dbeta) on the 576000 x 384
+bf16 workload. Inputs (442 MB per [rows, hidden] tensor) are larger than L2,
+so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline] [--no-clocks]
+
+Rank 0 prints one JSON line. Under torchrun (N > 1) every rank runs its own
+replica of the workload on its own GPU (the block has no cross-row exchange),
+timing is bracketed by barriers and the max over ranks is reported.
+``--impl reference`` times the fp64 CPU oracle instead, on host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "fwd+bwd rows/s and achieved HBM GB/s vs ~8 TB/s peak at (576000×384) bf16"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+BENCH_WORKLOADS = {w.name: w for w in (W.BENCH_LN_BF16_576000x384, W.BENCH_RMS_BF16_16384x8192)}
+
+
+# ---------------------------------------------------------------- bytes model
+def elem_bytes(w) -> int:
+    return 4 if w.dtype == "f32" else 2
+
+
+def fwd_bytes(w) -> int:
+    """Minimal HBM bytes of one ln_fwd: each input read once, each output
+    written once (x, residual, bias, gamma, beta in; sum, y, stats, amax out)."""
+    R, H, e = w.rows, w.hidden, elem_bytes(w)
+    has_res = w.residual_std is not None
+    store_sum = has_res or w.bias_std is not None
+    nstats = 2 if w.mode == W.LAYERNORM else 1
+    nparams = 1 + (w.mode == W.LAYERNORM and w.beta_std is not None) + (w.bias_std is not None)
+    return (R * H * e * (1 + has_res) + R * H * e * (1 + store_sum) + R * 4 * nstats
+            + H * e * nparams + (4 if w.amax else 0))
+
+
+def bwd_bytes(w) -> int:
+    """Minimal HBM bytes of one ln_bwd: dy, x_sum, stats, gamma in; dx,
+    dgamma (and dbeta) out. The workspace partials are not counted."""
+    R, H, e = w.rows, w.hidden, elem_bytes(w)
+    nstats = 2 if w.mode == W.LAYERNORM else 1
+    ngrads = 2 if w.mode == W.LAYERNORM else 1
+    return 3 * R * H * e + R * 4 * nstats + H * e + H * 4 * ngrads
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """Polls nvidia-smi in the background; keeps timestamped samples."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, period_ms: int = 100):
+        self.samples = []
+        self.proc = None
+        ids = []
+        try:
+            props = torch.cuda.get_device_properties(device_index)
+            uuid = getattr(props, "uuid", None)
+            if uuid:
+                ids.append("GPU-" + str(uuid))
+        except Exception:
+            pass
+        ids.append(None)
+        for gid in ids:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", str(period_ms)]
+            if gid:
+                cmd += ["-i", gid]
+            try:
+                p = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                     text=True)
+            except OSError:
+                return
+            time.sleep(0.3)
+            if p.poll() is None:
+                self.proc = p
+                break
+        if self.proc is not None:
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        win = [p for t, p in self.samples if t0 <= t <= t1]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        smax = [num(p[2]) for p in win if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in win for n, v in zip(names, p[5:9]) if v.lower() == "active"})
+        power = [num(p[3]) for p in win if num(p[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(win), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- helpers
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    d = os.path.join(ROOT, "normalization_fwd_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != source_hash():
+        return None
+    return d.get("workloads", {}).get(workload, {}).get(kernel)
+
+
+class Step:
+    """Device buffers and the two C-ABI calls of one fused fwd + bwd step."""
+
+    def __init__(self, nf, w, inp, device):
+        self.nf, self.w = nf, w
+        g = {k: (v.to(device) if v is not None else None) for k, v in inp.items()}
+        self.inp = g
+        R, H = w.rows, w.hidden
+        dt = W.TORCH_DTYPES[w.dtype]
+        self.rms = w.mode == W.RMSNORM
+        f32 = dict(dtype=torch.float32, device=device)
+        self.sum = torch.empty(R, H, dtype=dt, device=device)
+        self.y = torch.empty(R, H, dtype=dt, device=device)
+        self.mean = None if self.rms else torch.empty(R, **f32)
+        self.rstd = torch.empty(R, **f32)
+        self.amax = torch.empty(1, **f32) if w.amax else None
+        self.dx = torch.empty(R, H, dtype=dt, device=device)
+        self.dgamma = torch.empty(H, **f32)
+        self.dbeta = None if self.rms else torch.empty(H, **f32)
+        need = nf.ln_bwd_workspace_bytes(R, H, dt, w.mode)
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+
+    def fwd(self, stream):
+        g, w = self.inp, self.w
+        self.nf.ln_fwd(g["x"], g["bias"], g["residual"], g["gamma"], g["beta"], w.eps, w.mode,
+                       w.zero_centered_gamma, self.sum, self.y, self.mean, self.rstd, self.amax,
+                       stream)
+
+    def bwd(self, stream):
+        g, w = self.inp, self.w
+        self.nf.ln_bwd(g["dy"], self.sum, g["gamma"], self.mean, self.rstd, self.dx, self.dgamma,
+                       self.dbeta, stream, mode=w.mode, zero_centered_gamma=w.zero_centered_gamma,
+                       workspace=self.ws)
+
+    def h2d_tensors(self):
+        return [(k, self.inp[k]) for k in ("x", "residual", "bias", "gamma", "beta", "dy")
+                if self.inp[k] is not None]
+
+    def d2h_tensors(self):
+        out = [("sum", self.sum), ("y", self.y), ("mean", self.mean), ("rstd", self.rstd),
+               ("amax", self.amax), ("dx", self.dx), ("dgamma", self.dgamma),
+               ("dbeta", self.dbeta)]
+        return [(k, t) for k, t in out if t is not None]
+
+
+def nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+# ---------------------------------------------------------------- oracle timing
+def oracle_step(w, inp, rows):
+    """One fwd + bwd of the fp64 oracle over the first `rows` rows."""
+    from oracle import norm_bwd, norm_fwd
+    sl = slice(0, rows)
+    f = W.as_f64
+    res = inp["residual"]
+    ref = norm_fwd(f(inp["x"][sl]), f(inp["bias"]), None if res is None else f(res[sl]),
+                   f(inp["gamma"]), f(inp["beta"]), w.eps, w.mode, w.zero_centered_gamma,
+                   w.dtype)
+    norm_bwd(f(inp["dy"][sl]), ref["sum"], f(inp["gamma"]), ref["mean"], ref["rstd"], w.mode,
+             w.zero_centered_gamma, w.dtype)
+
+
+def time_oracle(w, inp, budget_s: float):
+    """rows/s of the oracle on a sample sized to about `budget_s` of CPU work."""
+    probe = min(2048, w.rows)
+    t0 = time.perf_counter()
+    oracle_step(w, inp, probe)
+    t_probe = time.perf_counter() - t0
+    rows = int(min(w.rows, max(probe, probe * budget_s / max(t_probe, 1e-6))))
+    rows = min(rows, 131072)
+    t0 = time.perf_counter()
+    oracle_step(w, inp, rows)
+    dt = time.perf_counter() - t0
+    return rows / dt, rows, dt
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, w, rank):
+    """The oracle on host cores, as the reference arm."""
+    if rank != 0:
+        return
+    inp = W.make_inputs(w, seed=0)
+    budget = 150.0
+    probe = min(1024, w.rows)
+    t0 = time.perf_counter()
+    oracle_step(w, inp, probe)
+    per_row = (time.perf_counter() - t0) / probe
+    steps = args.steps + args.warmup
+    rows = max(16, min(w.rows, int(budget / max(steps, 1) / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        oracle_step(w, inp, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, inp, rows)
+    el = time.perf_counter() - t0
+    value = rows * args.steps / el
+    sample = f"first {rows} of {w.rows} rows per step, fp64 numpy oracle fwd+bwd, 1 thread"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * el / args.steps * (w.rows / rows), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, n):
+    return {"workload": w.name, "rows": w.rows, "hidden": w.hidden, "mode": w.mode,
+            "io_dtype": w.dtype, "stats_dtype": "f32", "bias": w.bias_std is not None,
+            "residual": w.residual_std is not None, "amax": w.amax, "eps": w.eps,
+            "l2": "no flush: every [rows, hidden] input is larger than the 129 MB L2",
+            "parallelism": "replicas" if n > 1 else "single-gpu"}
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import normalization_fwd_gb300 as nf
+    nf.load_library()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    inp_host = W.make_inputs(w, seed=0)
+    step = Step(nf, w, inp_host, device)
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step.fwd(stream)
+        step.bwd(stream)
+    torch.cuda.synchronize(device)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank) if (rank == 0 and not args.no_clocks) else None
+    if sampler is not None:
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(device)
+    t_host0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step.fwd(stream)
+        ev[i][1].record(stream)
+        step.bwd(stream)
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    t_host1 = time.time()
+    barrier()
+    elapsed = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([elapsed], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(t.item())
+    clocks = None
+    if sampler is not None:
+        time.sleep(0.25)
+        sampler.stop()
+        clocks = sampler.summary(t_host0, t_host1)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+
+    # end to end through the same calls, inputs from pinned host memory and
+    # every output read back, each step
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(step, stream, device, min(args.e2e_steps, max(K, 1)))
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    fb, bb = fwd_bytes(w), bwd_bytes(w)
+    kernels = {}
+    for name, ms, by in (("ln_fwd", fwd_ms, fb), ("ln_bwd", bwd_ms, bb)):
+        gbs = by / (ms * 1e-3) / 1e9
+        kernels[name] = {"us": ms * 1e3, "algorithmic_bytes": by, "GBps": gbs,
+                         f"frac_of_{peak_kind}": gbs / peak, "frac_of_8TBps": gbs / NOMINAL_HBM_GBS,
+                         "traffic": ncu_traffic(w.name, name)}
+    dom = max(kernels, key=lambda k: kernels[k]["us"])
+    d = kernels[dom]
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": d["GBps"], "peak": peak,
+                "unit": "GB/s", "frac": d["GBps"] / peak, "peak_kind": peak_kind,
+                "traffic": d["traffic"]}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        v, rows, secs = time_oracle(w, inp_host, budget_s=12.0)
+        cpu = {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {rows} of {w.rows} rows, fp64 numpy oracle fwd+bwd, "
+                         f"{secs:.1f} s on 1 host thread"}
+    ms_step = elapsed / K
+    line = {
+        "metric": METRIC, "value": world * w.rows / (ms_step * 1e-3), "unit": "rows/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": config_of(w, world), "roofline": roofline,
+        "kernels": kernels, "step_GBps": (fb + bb) / (ms_step * 1e-3) / 1e9,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clocks,
+        "impl": "ours",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(step, stream, device, steps):
+    h2d = step.h2d_tensors()
+    d2h = step.d2h_tensors()
+    host_in = {k: t.detach().to("cpu").pin_memory() for k, t in h2d}
+    host_out = {k: torch.empty(t.shape, dtype=t.dtype).pin_memory() for k, t in d2h}
+
+    def one():
+        for k, t in h2d:
+            t.copy_(host_in[k], non_blocking=True)
+        step.fwd(stream)
+        step.bwd(stream)
+        for k, t in d2h:
+            host_out[k].copy_(t, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize(device)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / steps
+    return {"value": step.w.rows / (ms * 1e-3), "unit": "rows/s", "ms_per_step": ms,
+            "steps": steps, "h2d_bytes_per_step": sum(nbytes(t) for _, t in h2d),
+            "d2h_bytes_per_step": sum(nbytes(t) for _, t in d2h)}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS),
+                    default=W.BENCH_LN_BF16_576000x384.name)
+    ap.add_argument("--rows", type=int, default=None,
+                    help="override the workload's row count (smaller profiling captures)")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = BENCH_WORKLOADS[args.workload]
+    if args.rows is not None:
+        w = w.with_(rows=args.rows, name=f"{w.name}@rows={args.rows}")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus != world:
+        if world == 1 and args.gpus > 1:
+            ap.error("--gpus N > 1 runs under torchrun (one process per GPU)")
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * normfuse: the fused normalization block on one GPU (sm_103a).
+ *
+ * Forward: bias + residual add, then LayerNorm or RMSNorm over the hidden
+ * dimension, with an optional amax of |y| for FP8 scaling, in one pass over
+ * HBM. Backward: the per-row dx reduction over the hidden dimension and the
+ * dgamma/dbeta reductions over the rows in one persistent kernel, followed by
+ * a small deterministic finalize.
+ *
+ * Conventions shared by every entry point:
+ *  - Matrices are row-major and contiguous, [rows, hidden]. gamma, beta and
+ *    bias are [hidden] in the I/O dtype. mean and rstd are fp32 [rows].
+ *    dgamma and dbeta are fp32 [hidden]. amax is one fp32 scalar.
+ *  - Every tensor pointer is a DEVICE pointer on the current device, owned by
+ *    the caller; the library never allocates, frees or keeps one. Pointers
+ *    must be aligned to their element size. When every matrix/vector pointer
+ *    is 16-byte aligned and hidden * sizeof(dtype) is a multiple of 16, the
+ *    128-bit vectorised kernels run; otherwise a scalar kernel handles the
+ *    call with the same results.
+ *  - Outputs must not overlap inputs or each other.
+ *  - Work is enqueued on `stream` (0 = the legacy default stream) and the call
+ *    returns without waiting for it. The library calls no allocating CUDA API
+ *    and no synchronising one.
+ *  - Failure: arguments are validated on the host first; a validation failure
+ *    returns its status before anything is enqueued and leaves every output
+ *    untouched. A CUDA error from an enqueue returns LN_ERR_CUDA; the CUDA
+ *    error code is then available from ln_last_cuda_error() on the calling
+ *    thread. No entry point aborts, throws or prints.
+ *  - Limits: 1 <= hidden <= LN_MAX_HIDDEN_VEC on the vectorised path,
+ *    1 <= hidden <= LN_MAX_HIDDEN_SCALAR on the scalar path; rows >= 0.
+ *
+ * Citations are to the four pages the method comes from: NVIDIA/cutlass
+ * discussion 874 (GEMM -> residual add -> LayerNorm), iree-org/iree issue
+ * 9139 (LayerNorm as mean, variance and normalize over one read of the input),
+ * NVIDIA/Fuser issue 1660 (bias + residual -> LayerNorm -> FP8 amax, with the
+ * amax split into a fused partial and a final reduction) and pytorch/pytorch
+ * PR 165370 (mixed-order fusion of the norm-backward reductions).
+ */
+#ifndef NORMFUSE_H
+#define NORMFUSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LN_MAX_HIDDEN_VEC 32768
+#define LN_MAX_HIDDEN_SCALAR 8192
+
+typedef enum { LN_F32 = 0, LN_BF16 = 1, LN_F16 = 2 } ln_dtype;
+typedef enum { LN_LAYERNORM = 0, LN_RMSNORM = 1 } ln_mode;
+typedef enum {
+  LN_OK = 0,
+  LN_ERR_NULL = 1,        /* a required pointer is NULL */
+  LN_ERR_ALIGN = 2,       /* a pointer is not aligned to its element size */
+  LN_ERR_SHAPE = 3,       /* rows < 0, hidden out of range */
+  LN_ERR_UNSUPPORTED = 4, /* unknown dtype or mode */
+  LN_ERR_CUDA = 5,        /* a CUDA call failed; see ln_last_cuda_error() */
+  LN_ERR_WORKSPACE = 6,   /* backward workspace missing, misaligned or too small */
+  LN_ERR_INVALID = 7      /* eps negative or not finite; outputs overlap inputs */
+} ln_status;
+
+/*
+ * ln_fwd: out_sum = (x + bias) + residual; y = norm(out_sum) * w + beta;
+ * amax = max |y|.
+ *
+ * Defined by the forward snippet of NVIDIA/Fuser issue 1660 (bias and
+ * residual add, w = gamma or 1 + gamma, layer_norm, amax of |y| written into
+ * a preallocated scalar) and by iree-org/iree issue 9139 (mean, variance and
+ * normalize over a single read of the input; bias and skip operands optional).
+ * RMSNorm, named on pytorch/pytorch PR 165370, is y = s * rstd * w with
+ * rstd = 1/sqrt(mean(s^2) + eps).
+ *
+ * Per row, in fp32 arithmetic:
+ *   s      = (x + bias) + residual, stored to out_sum rounded to dtype;
+ *   the statistics are taken from the stored (rounded) sum:
+ *   LayerNorm: mean = sum(s)/H, var = sum((s - mean)^2)/H (biased),
+ *              rstd = 1/sqrt(var + eps), y = (s - mean) * rstd * w + beta;
+ *   RMSNorm:   rstd = 1/sqrt(sum(s^2)/H + eps), y = s * rstd * w;
+ *   w = gamma, or 1 + gamma (formed in fp32) when zero_centered_gamma != 0;
+ *   y is rounded to dtype; amax = max over all stored y of |y| (exact).
+ *
+ * x         [rows, hidden] dtype, required.
+ * bias      [hidden] dtype, NULL = no bias.
+ * residual  [rows, hidden] dtype, NULL = no residual.
+ * gamma     [hidden] dtype, required.
+ * beta      [hidden] dtype, NULL = 0; ignored for RMSNorm.
+ * eps       >= 0 and finite.
+ * out_sum   [rows, hidden] dtype, NULL = not stored (the backward needs it
+ *           whenever bias or residual is given).
+ * y         [rows, hidden] dtype, required.
+ * mean      [rows] fp32, NULL = not stored; ignored for RMSNorm.
+ * rstd      [rows] fp32, NULL = not stored.
+ * amax      one fp32, NULL = not computed. When given it is overwritten
+ *           (set to 0 on `stream`, then maxed into), not accumulated.
+ */
+ln_status ln_fwd(const void* x, const void* bias, const void* residual,
+                 const void* gamma, const void* beta, float eps, ln_mode mode,
+                 int zero_centered_gamma, void* out_sum, void* y, float* mean,
+                 float* rstd, float* amax, cudaStream_t stream, int64_t rows,
+                 int64_t hidden, ln_dtype dtype);
+
+/*
+ * ln_bwd: dx, dgamma, dbeta of the normalization given dy and the forward's
+ * saved sum and statistics.
+ *
+ * Defined by pytorch/pytorch PR 165370: the dx reduction runs over the hidden
+ * dimension, the dgamma/dbeta reductions over the rows, and both share dy,
+ * x_sum and the statistics, so one persistent kernel loads each input once,
+ * keeps per-CTA partial sums of the row reduction (the PR's partial
+ * accumulation) and a finalize adds the partials. Per row, in fp32:
+ *   xhat = (x_sum - mean) * rstd   (RMSNorm: x_sum * rstd);  g = dy * w;
+ *   c1 = sum(g)/H (LayerNorm only); c2 = sum(g * xhat)/H;
+ *   dx = rstd * (g - c1 - xhat * c2)   (RMSNorm: no c1), rounded to dtype;
+ *   dgamma = sum over rows of dy * xhat; dbeta = sum over rows of dy.
+ * dx is also the gradient of the residual and of x through the identity add.
+ * dgamma and dbeta are bitwise reproducible from run to run on the same GPU
+ * model: the row-to-CTA assignment depends only on the SM count and the
+ * finalize adds the partials in a fixed order (in fp64).
+ *
+ * dy, x_sum [rows, hidden] dtype, required (x_sum is the forward's out_sum,
+ *           or x itself when the forward had neither bias nor residual).
+ * gamma     [hidden] dtype, required; w = gamma or 1 + gamma as in ln_fwd.
+ * mean      [rows] fp32, required for LayerNorm, ignored for RMSNorm.
+ * rstd      [rows] fp32, required.
+ * dx        [rows, hidden] dtype, required.
+ * dgamma    [hidden] fp32, required, overwritten.
+ * dbeta     [hidden] fp32, NULL = not computed; ignored for RMSNorm.
+ * workspace device scratch of at least ln_bwd_workspace_bytes() bytes,
+ *           16-byte aligned, owned by the caller; may be NULL only when
+ *           rows == 0. Its contents need no initialisation and are not
+ *           meaningful after the call. Calls that share one workspace must
+ *           not run concurrently.
+ */
+ln_status ln_bwd(const void* dy, const void* x_sum, const void* gamma,
+                 const float* mean, const float* rstd, void* dx, float* dgamma,
+                 float* dbeta, cudaStream_t stream, int64_t rows,
+                 int64_t hidden, ln_dtype dtype, ln_mode mode,
+                 int zero_centered_gamma, void* workspace,
+                 size_t workspace_bytes);
+
+/*
+ * Bytes of workspace ln_bwd needs for this shape on the current device (the
+ * maximum over the vectorised and the scalar kernel, so it holds whatever
+ * the pointers' alignment). Queries device attributes; returns LN_ERR_CUDA
+ * when no device is usable.
+ */
+ln_status ln_bwd_workspace_bytes(int64_t rows, int64_t hidden, ln_dtype dtype,
+                                 ln_mode mode, size_t* bytes);
+
+/* Static, human-readable name of a status code. */
+const char* ln_status_string(ln_status status);
+
+/* The cudaError_t behind the last LN_ERR_CUDA on the calling thread. */
+int ln_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NORMFUSE_H */

@@ -1,0 +1,306 @@
+// C entry points of the fused normalization library: argument validation,
+// per-device caches, dispatch to the per-dtype launchers.
+#include <math.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/normfuse.h"
+#include "launch.h"
+
+namespace nf {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+ln_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return LN_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+std::mutex g_mu;
+
+struct OccEntry {
+  const void* fn;
+  int block;
+  size_t smem;
+  int device;
+  int blocks;
+};
+std::vector<OccEntry>& occ_cache() {
+  static std::vector<OccEntry> v;
+  return v;
+}
+
+size_t elem_size(ln_dtype dt) { return dt == LN_F32 ? 4 : 2; }
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Byte ranges for the overlap check.
+struct Range {
+  const void* p;
+  size_t bytes;
+};
+bool overlap(const Range& a, const Range& b) {
+  if (a.p == nullptr || b.p == nullptr || a.bytes == 0 || b.bytes == 0) return false;
+  const uintptr_t a0 = (uintptr_t)a.p, a1 = a0 + a.bytes;
+  const uintptr_t b0 = (uintptr_t)b.p, b1 = b0 + b.bytes;
+  return a0 < b1 && b0 < a1;
+}
+bool any_overlap(const Range* outs, int n_out, const Range* ins, int n_in) {
+  for (int i = 0; i < n_out; ++i) {
+    for (int j = 0; j < n_in; ++j)
+      if (overlap(outs[i], ins[j])) return true;
+    for (int j = i + 1; j < n_out; ++j)
+      if (overlap(outs[i], outs[j])) return true;
+  }
+  return false;
+}
+
+int max_hidden(ln_dtype dt, bool vec) {
+  return vec ? kMaxVecSlots * (int)(16 / elem_size(dt)) : kMaxHiddenScalar;
+}
+
+template <typename F>
+cudaError_t by_dtype(ln_dtype dt, F&& f) {
+  switch (dt) {
+    case LN_F32: return f(float{});
+    case LN_BF16: return f(bf16{});
+    default: return f(f16{});
+  }
+}
+
+}  // namespace
+
+int device_sm_count(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  if (dev >= 0 && dev < kMaxDevices) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sm_count[dev] == 0) {
+      int n = 0;
+      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return (int)e;
+      g_sm_count[dev] = n;
+    }
+    *sms = g_sm_count[dev];
+    return (int)cudaSuccess;
+  }
+  return (int)cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+}
+
+int resident_blocks(const void* fn, int block, size_t smem, int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const OccEntry& o : occ_cache()) {
+    if (o.fn == fn && o.block == block && o.smem == smem && o.device == dev) {
+      *out = o.blocks;
+      return (int)cudaSuccess;
+    }
+  }
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, block, smem);
+  if (e != cudaSuccess) return (int)e;
+  occ_cache().push_back({fn, block, smem, dev, n});
+  *out = n;
+  return (int)cudaSuccess;
+}
+
+}  // namespace nf
+
+using namespace nf;
+
+extern "C" {
+
+const char* ln_status_string(ln_status s) {
+  switch (s) {
+    case LN_OK: return "LN_OK";
+    case LN_ERR_NULL: return "LN_ERR_NULL: a required pointer is NULL";
+    case LN_ERR_ALIGN: return "LN_ERR_ALIGN: a pointer is not aligned to its element size";
+    case LN_ERR_SHAPE: return "LN_ERR_SHAPE: rows < 0 or hidden out of range";
+    case LN_ERR_UNSUPPORTED: return "LN_ERR_UNSUPPORTED: unknown dtype or mode";
+    case LN_ERR_CUDA: return "LN_ERR_CUDA: a CUDA call failed (see ln_last_cuda_error)";
+    case LN_ERR_WORKSPACE: return "LN_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case LN_ERR_INVALID: return "LN_ERR_INVALID: bad eps, or outputs overlap inputs";
+  }
+  return "unknown ln_status";
+}
+
+int ln_last_cuda_error(void) { return g_last_cuda_error; }
+
+ln_status ln_fwd(const void* x, const void* bias, const void* residual, const void* gamma,
+                 const void* beta, float eps, ln_mode mode, int zero_centered_gamma,
+                 void* out_sum, void* y, float* mean, float* rstd, float* amax,
+                 cudaStream_t stream, int64_t rows, int64_t hidden, ln_dtype dtype) {
+  if (dtype != LN_F32 && dtype != LN_BF16 && dtype != LN_F16) return LN_ERR_UNSUPPORTED;
+  if (mode != LN_LAYERNORM && mode != LN_RMSNORM) return LN_ERR_UNSUPPORTED;
+  if (rows < 0 || hidden < 1) return LN_ERR_SHAPE;
+  if (!(eps >= 0.0f) || !isfinite(eps)) return LN_ERR_INVALID;
+  const bool rms = mode == LN_RMSNORM;
+  if (rms) {
+    beta = nullptr;
+    mean = nullptr;
+  }
+  if (gamma == nullptr) return LN_ERR_NULL;
+  if (rows > 0 && (x == nullptr || y == nullptr)) return LN_ERR_NULL;
+  const size_t es = elem_size(dtype);
+  const void* tensors[] = {x, bias, residual, gamma, beta, out_sum, y};
+  for (const void* p : tensors)
+    if (!aligned(p, es)) return LN_ERR_ALIGN;
+  if (!aligned(mean, 4) || !aligned(rstd, 4) || !aligned(amax, 4)) return LN_ERR_ALIGN;
+  bool vec = (hidden * (int64_t)es) % 16 == 0;
+  for (const void* p : tensors)
+    if (!aligned(p, 16)) vec = false;
+  if (hidden > max_hidden(dtype, vec)) {
+    if (!vec || hidden > max_hidden(dtype, false)) return LN_ERR_SHAPE;
+    vec = false;
+  }
+  const size_t mat = (size_t)rows * (size_t)hidden * es, vecb = (size_t)hidden * es;
+  const Range outs[] = {{out_sum, mat}, {y, mat}, {mean, (size_t)rows * 4},
+                        {rstd, (size_t)rows * 4}, {amax, amax ? 4u : 0u}};
+  const Range ins[] = {{x, mat}, {residual, mat}, {bias, vecb}, {gamma, vecb}, {beta, vecb}};
+  if (any_overlap(outs, 5, ins, 5)) return LN_ERR_INVALID;
+
+  if (amax) {
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (rows == 0) return LN_OK;
+
+  FwdArgs a;
+  a.x = x;
+  a.bias = bias;
+  a.residual = residual;
+  a.gamma = gamma;
+  a.beta = beta;
+  a.out_sum = out_sum;
+  a.y = y;
+  a.mean = mean;
+  a.rstd = rstd;
+  a.amax = reinterpret_cast<unsigned*>(amax);
+  a.rows = rows;
+  a.hidden = (int)hidden;
+  a.eps = eps;
+  a.inv_hidden = 1.0f / (float)hidden;
+  a.rms = rms ? 1 : 0;
+  a.zero_centered = zero_centered_gamma ? 1 : 0;
+  cudaError_t e = by_dtype(dtype, [&](auto t) {
+    using T = decltype(t);
+    Plan p;
+    cudaError_t r = fwd_plan<T>(rows, (int)hidden, vec, &p);
+    if (r != cudaSuccess) return r;
+    return fwd_launch<T>(a, p, stream);
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  return LN_OK;
+}
+
+static cudaError_t bwd_plan_any(ln_dtype dtype, int64_t rows, int hidden, bool rms, bool vec,
+                                Plan* p) {
+  return by_dtype(dtype, [&](auto t) {
+    using T = decltype(t);
+    return bwd_plan<T>(rows, hidden, rms, vec, p);
+  });
+}
+
+ln_status ln_bwd_workspace_bytes(int64_t rows, int64_t hidden, ln_dtype dtype, ln_mode mode,
+                                 size_t* bytes) {
+  if (bytes == nullptr) return LN_ERR_NULL;
+  if (dtype != LN_F32 && dtype != LN_BF16 && dtype != LN_F16) return LN_ERR_UNSUPPORTED;
+  if (mode != LN_LAYERNORM && mode != LN_RMSNORM) return LN_ERR_UNSUPPORTED;
+  if (rows < 0 || hidden < 1) return LN_ERR_SHAPE;
+  *bytes = 0;
+  if (rows == 0) return LN_OK;
+  const bool rms = mode == LN_RMSNORM;
+  const bool vec_possible = (hidden * (int64_t)elem_size(dtype)) % 16 == 0 &&
+                            hidden <= max_hidden(dtype, true);
+  if (!vec_possible && hidden > max_hidden(dtype, false)) return LN_ERR_SHAPE;
+  size_t need = 0;
+  for (int v = 0; v < 2; ++v) {
+    const bool vec = v == 1;
+    if (vec && !vec_possible) continue;
+    if (!vec && hidden > max_hidden(dtype, false)) continue;
+    Plan p;
+    cudaError_t e = bwd_plan_any(dtype, rows, (int)hidden, rms, vec, &p);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const size_t b = (size_t)p.grid * (size_t)p.ws_cols * sizeof(float);
+    if (b > need) need = b;
+  }
+  *bytes = need;
+  return LN_OK;
+}
+
+ln_status ln_bwd(const void* dy, const void* x_sum, const void* gamma, const float* mean,
+                 const float* rstd, void* dx, float* dgamma, float* dbeta, cudaStream_t stream,
+                 int64_t rows, int64_t hidden, ln_dtype dtype, ln_mode mode,
+                 int zero_centered_gamma, void* workspace, size_t workspace_bytes) {
+  if (dtype != LN_F32 && dtype != LN_BF16 && dtype != LN_F16) return LN_ERR_UNSUPPORTED;
+  if (mode != LN_LAYERNORM && mode != LN_RMSNORM) return LN_ERR_UNSUPPORTED;
+  if (rows < 0 || hidden < 1) return LN_ERR_SHAPE;
+  const bool rms = mode == LN_RMSNORM;
+  if (rms) {
+    mean = nullptr;
+    dbeta = nullptr;
+  }
+  if (gamma == nullptr || dgamma == nullptr) return LN_ERR_NULL;
+  if (rows > 0 && (dy == nullptr || x_sum == nullptr || rstd == nullptr || dx == nullptr ||
+                   (!rms && mean == nullptr)))
+    return LN_ERR_NULL;
+  const size_t es = elem_size(dtype);
+  const void* tensors[] = {dy, x_sum, gamma, dx};
+  for (const void* p : tensors)
+    if (!aligned(p, es)) return LN_ERR_ALIGN;
+  if (!aligned(mean, 4) || !aligned(rstd, 4) || !aligned(dgamma, 4) || !aligned(dbeta, 4))
+    return LN_ERR_ALIGN;
+  bool vec = (hidden * (int64_t)es) % 16 == 0;
+  for (const void* p : tensors)
+    if (!aligned(p, 16)) vec = false;
+  if (hidden > max_hidden(dtype, vec)) {
+    if (!vec || hidden > max_hidden(dtype, false)) return LN_ERR_SHAPE;
+    vec = false;
+  }
+  const size_t mat = (size_t)rows * (size_t)hidden * es;
+  const size_t hb = (size_t)hidden * es, h4 = (size_t)hidden * 4, r4 = (size_t)rows * 4;
+  const Range outs[] = {{dx, mat}, {dgamma, h4}, {dbeta, h4}, {workspace, workspace_bytes}};
+  const Range ins[] = {{dy, mat}, {x_sum, mat}, {gamma, hb}, {mean, r4}, {rstd, r4}};
+  if (any_overlap(outs, 4, ins, 5)) return LN_ERR_INVALID;
+
+  if (rows == 0) {
+    cudaError_t e = cudaMemsetAsync(dgamma, 0, h4, stream);
+    if (e == cudaSuccess && dbeta) e = cudaMemsetAsync(dbeta, 0, h4, stream);
+    return e == cudaSuccess ? LN_OK : cuda_fail(e);
+  }
+  Plan p;
+  cudaError_t e = bwd_plan_any(dtype, rows, (int)hidden, rms, vec, &p);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const size_t need = (size_t)p.grid * (size_t)p.ws_cols * sizeof(float);
+  if (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < need)
+    return LN_ERR_WORKSPACE;
+
+  BwdArgs a;
+  a.dy = dy;
+  a.x_sum = x_sum;
+  a.gamma = gamma;
+  a.mean = mean;
+  a.rstd = rstd;
+  a.dx = dx;
+  a.ws = static_cast<float*>(workspace);
+  a.rows = rows;
+  a.hidden = (int)hidden;
+  a.inv_hidden = 1.0f / (float)hidden;
+  a.rms = rms ? 1 : 0;
+  a.zero_centered = zero_centered_gamma ? 1 : 0;
+  e = by_dtype(dtype, [&](auto t) {
+    using T = decltype(t);
+    return bwd_launch<T>(a, p, dgamma, dbeta, stream);
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  return LN_OK;
+}
+
+}  // extern "C"

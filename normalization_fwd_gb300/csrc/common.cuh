@@ -1,0 +1,199 @@
+// Shared device helpers for the normalization kernels: 128-bit vector
+// load/store, dtype <-> fp32 conversion, warp and CTA reductions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace nf {
+
+using bf16 = __nv_bfloat16;
+using f16 = __half;
+
+// Elements per 16-byte vector.
+template <typename T> struct Vec;
+template <> struct Vec<float> { static constexpr int N = 4; };
+template <> struct Vec<bf16> { static constexpr int N = 8; };
+template <> struct Vec<f16> { static constexpr int N = 8; };
+
+// Arguments of the forward kernels (validated on the host).
+struct FwdArgs {
+  const void* x;
+  const void* bias;      // nullable
+  const void* residual;  // nullable
+  const void* gamma;
+  const void* beta;      // nullable (always null for RMSNorm)
+  void* out_sum;         // nullable
+  void* y;
+  float* mean;           // nullable (always null for RMSNorm)
+  float* rstd;           // nullable
+  unsigned* amax;        // nullable; fp32 bit pattern, zeroed before launch
+  int64_t rows;
+  int hidden;
+  float eps;
+  float inv_hidden;
+  int rms;
+  int zero_centered;
+};
+
+// Arguments of the backward kernels.
+struct BwdArgs {
+  const void* dy;
+  const void* x_sum;
+  const void* gamma;
+  const float* mean;     // null for RMSNorm
+  const float* rstd;
+  void* dx;
+  float* ws;             // [gridDim.x][cols] partials, cols = hidden or 2*hidden
+  int64_t rows;
+  int hidden;
+  float inv_hidden;
+  int rms;
+  int zero_centered;
+};
+
+// ---- scalar conversions --------------------------------------------------
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(bf16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f(f16 v) { return __half2float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
+template <> __device__ __forceinline__ f16 from_f<f16>(float v) { return __float2half_rn(v); }
+
+// Round an fp32 value to T and back: the value the stored tensor holds.
+template <typename T> __device__ __forceinline__ float round_trip(float v) {
+  return to_f(from_f<T>(v));
+}
+
+// ---- 16-byte vectors -----------------------------------------------------
+// Read-only streaming load of 16 bytes (non-coherent path; inputs are never
+// written by the same kernel).
+__device__ __forceinline__ uint4 ld_vec(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+// L1-cached load for the small per-column vectors (gamma, beta, bias).
+__device__ __forceinline__ uint4 ld_vec_param(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void st_vec(void* p, uint4 v) {
+  *reinterpret_cast<uint4*>(p) = v;
+}
+
+// Unpack a 16-byte vector of T into fp32.
+template <typename T> __device__ __forceinline__ void unpack(const uint4& u, float* f);
+template <> __device__ __forceinline__ void unpack<float>(const uint4& u, float* f) {
+  f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+// bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 bits.
+__device__ __forceinline__ void unpack_bf16x2(unsigned w, float* f) {
+  f[0] = __uint_as_float(w << 16);
+  f[1] = __uint_as_float(w & 0xffff0000u);
+}
+template <> __device__ __forceinline__ void unpack<bf16>(const uint4& u, float* f) {
+  unpack_bf16x2(u.x, f); unpack_bf16x2(u.y, f + 2);
+  unpack_bf16x2(u.z, f + 4); unpack_bf16x2(u.w, f + 6);
+}
+__device__ __forceinline__ void unpack_f16x2(unsigned w, float* f) {
+  __half2 h = *reinterpret_cast<__half2*>(&w);
+  float2 v = __half22float2(h);
+  f[0] = v.x; f[1] = v.y;
+}
+template <> __device__ __forceinline__ void unpack<f16>(const uint4& u, float* f) {
+  unpack_f16x2(u.x, f); unpack_f16x2(u.y, f + 2);
+  unpack_f16x2(u.z, f + 4); unpack_f16x2(u.w, f + 6);
+}
+
+// Pack fp32 values into a 16-byte vector of T, rounding to nearest even.
+template <typename T> __device__ __forceinline__ uint4 pack(const float* f);
+template <> __device__ __forceinline__ uint4 pack<float>(const float* f) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                    __float_as_uint(f[2]), __float_as_uint(f[3]));
+}
+__device__ __forceinline__ unsigned pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<unsigned*>(&h);
+}
+template <> __device__ __forceinline__ uint4 pack<bf16>(const float* f) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                    pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+}
+__device__ __forceinline__ unsigned pack_f16x2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<unsigned*>(&h);
+}
+template <> __device__ __forceinline__ uint4 pack<f16>(const float* f) {
+  return make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]),
+                    pack_f16x2(f[4], f[5]), pack_f16x2(f[6], f[7]));
+}
+
+// |v| as an fp32 bit pattern. For v >= 0 (and NaN with the sign cleared)
+// unsigned order equals float order, so an unsigned max is an exact amax
+// that also lets a NaN win, as torch.amax does.
+__device__ __forceinline__ unsigned abs_bits(float v) {
+  return __float_as_uint(v) & 0x7fffffffu;
+}
+
+// ---- reductions ----------------------------------------------------------
+// Butterfly sum over aligned groups of LANES lanes (LANES a power of two
+// <= 32). Every lane of the warp must call it; each group gets its own sum.
+template <int LANES> __device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = LANES / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+template <int LANES> __device__ __forceinline__ float2 group_sum2(float2 v) {
+#pragma unroll
+  for (int o = LANES / 2; o > 0; o >>= 1) {
+    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+  }
+  return v;
+}
+
+// Sum over the CTA, same fixed order in every thread; returns the total to
+// all threads. `red` holds one float per warp. Two barriers: the second one
+// lets the caller reuse `red` right away.
+template <int THREADS> __device__ __forceinline__ float cta_sum(float v, float* red) {
+  constexpr int W = THREADS / 32;
+  v = group_sum<32>(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < W; ++i) t += red[i];
+  __syncthreads();
+  return t;
+}
+template <int THREADS> __device__ __forceinline__ float2 cta_sum2(float2 v, float2* red) {
+  constexpr int W = THREADS / 32;
+  v = group_sum2<32>(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float2 t = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < W; ++i) { t.x += red[i].x; t.y += red[i].y; }
+  __syncthreads();
+  return t;
+}
+
+// Max of per-thread amax bits over the CTA, then one atomicMax per CTA on
+// the fp32 bit pattern in global memory (the partial-then-final split of the
+// amax reduction). Must be called by all threads of the CTA.
+__device__ __forceinline__ void cta_amax_commit(unsigned bits, unsigned* amax, unsigned* red) {
+  bits = __reduce_max_sync(0xffffffffu, bits);
+  const int nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = bits;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned m = 0;
+    for (int i = 0; i < nw; ++i) m = max(m, red[i]);
+    atomicMax(amax, m);
+  }
+}
+
+}  // namespace nf

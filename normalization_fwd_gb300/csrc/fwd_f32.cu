@@ -1,0 +1,3 @@
+// Forward kernels instantiated for f32 I/O.
+#include "dispatch.cuh"
+NF_INSTANTIATE_FWD(float)

@@ -1,0 +1,231 @@
+// Forward kernels of the fused block: bias + residual add, LayerNorm or
+// RMSNorm, amax of |y| (NVIDIA/Fuser issue 1660, the layernorm + amax
+// snippet; iree-org/iree issue 9139, mean / variance / normalize over one read
+// of the input).
+//
+// Every kernel keeps a row on chip between the statistics and the normalize
+// step, so each input element is read from HBM once and each output written
+// once. The row loop is a grid-stride loop; the host sizes the grid to the
+// number of CTAs that are resident at once, so the kernels run persistently
+// and the amax partial is committed once per CTA.
+//
+//  * fwd_warp_kernel: a group of LANES lanes (8, 16 or 32) owns a row held in
+//    registers as N 16-byte vectors per lane; reductions are xor-shuffle
+//    butterflies inside the group. Rows of up to 256 vectors (2048 bf16).
+//  * fwd_cta_kernel: a CTA of THREADS threads owns a row, N vectors per
+//    thread, reductions through shared memory. Rows of up to 2048 vectors.
+//  * fwd_scalar_kernel: any hidden size and alignment; element-wise loads,
+//    the row staged in shared memory.
+#pragma once
+
+#include "common.cuh"
+
+namespace nf {
+
+constexpr int kWarpCta = 256;     // threads per CTA of the warp-per-row kernels
+constexpr int kScalarCta = 256;   // threads per CTA of the scalar kernels
+
+// One row's worth of work for the vector kernels. `G` is the number of
+// threads sharing a row (LANES or THREADS), `t` this thread's index among
+// them. `reduce` sums a float over those G threads.
+template <typename T, int G, int N, typename Reduce>
+__device__ __forceinline__ void fwd_row(const FwdArgs& a, int64_t row, bool row_ok, int t,
+                                        Reduce reduce, unsigned& amax_bits, bool write_stats) {
+  constexpr int VEC = Vec<T>::N;
+  const int H = a.hidden;
+  const int V = H / VEC;
+  const int64_t off = row * (int64_t)H;
+  const T* x = static_cast<const T*>(a.x) + off;
+  const T* res = static_cast<const T*>(a.residual) + off;
+  const T* bias = static_cast<const T*>(a.bias);
+
+  // Issue every load of the row before using any of it.
+  uint4 xr[N], rr[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int v = k * G + t;
+    if (row_ok && v < V) {
+      xr[k] = ld_vec(x + v * VEC);
+      if (a.residual) rr[k] = ld_vec(res + v * VEC);
+    }
+  }
+
+  // F1: s = (x + bias) + residual in fp32, rounded to T and stored; the
+  // statistics see the stored value.
+  float s[N][VEC];
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int v = k * G + t;
+    const bool ok = row_ok && v < V;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) s[k][e] = 0.f;
+    if (ok) {
+      unpack<T>(xr[k], s[k]);
+      if (a.bias) {
+        float b[VEC];
+        unpack<T>(ld_vec_param(bias + v * VEC), b);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) s[k][e] += b[e];
+      }
+      if (a.residual) {
+        float r[VEC];
+        unpack<T>(rr[k], r);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) s[k][e] += r[e];
+      }
+      const uint4 packed = pack<T>(s[k]);
+      if (a.out_sum) st_vec(static_cast<T*>(a.out_sum) + off + v * VEC, packed);
+      unpack<T>(packed, s[k]);
+    }
+  }
+
+  // F2: mean, then the centred sum of squares from the registers
+  // (RMSNorm: the plain sum of squares).
+  float mean = 0.f;
+  if (!a.rms) {
+    float t1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < N; ++k)
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) t1 += s[k][e];
+    mean = reduce(t1) / (float)H;
+  }
+  float t2 = 0.f;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const bool ok = row_ok && (k * G + t) < V;
+    if (ok) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const float d = s[k][e] - mean;
+        t2 = fmaf(d, d, t2);
+      }
+    }
+  }
+  const float var = reduce(t2) / (float)H;
+  const float rstd = 1.0f / sqrtf(var + a.eps);
+
+  if (row_ok && write_stats) {
+    if (a.mean) a.mean[row] = mean;
+    if (a.rstd) a.rstd[row] = rstd;
+  }
+
+  // F3: normalize and affine; F4: amax of the stored y.
+  const T* gamma = static_cast<const T*>(a.gamma);
+  const T* beta = static_cast<const T*>(a.beta);
+  T* y = static_cast<T*>(a.y) + off;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int v = k * G + t;
+    if (row_ok && v < V) {
+      float w[VEC], b[VEC], o[VEC];
+      unpack<T>(ld_vec_param(gamma + v * VEC), w);
+      if (beta) {
+        unpack<T>(ld_vec_param(beta + v * VEC), b);
+      } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) b[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const float we = a.zero_centered ? 1.0f + w[e] : w[e];
+        o[e] = fmaf((s[k][e] - mean) * rstd, we, b[e]);
+      }
+      const uint4 packed = pack<T>(o);
+      st_vec(y + v * VEC, packed);
+      if (a.amax) {
+        unpack<T>(packed, o);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) amax_bits = max(amax_bits, abs_bits(o[e]));
+      }
+    }
+  }
+}
+
+template <typename T, int LANES, int N>
+__global__ void __launch_bounds__(kWarpCta) fwd_warp_kernel(const FwdArgs a) {
+  constexpr int RPW = 32 / LANES;     // rows per warp step
+  constexpr int W = kWarpCta / 32;
+  __shared__ unsigned red_amax[W];
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LANES;
+  const int l = lane % LANES;
+  unsigned amax_bits = 0;
+  const int64_t step = (int64_t)gridDim.x * W * RPW;
+  // The loop bound is uniform over the warp so every lane takes part in the
+  // shuffles; a group past the last row runs with its loads and stores off.
+  for (int64_t base = ((int64_t)blockIdx.x * W + (threadIdx.x >> 5)) * RPW; base < a.rows;
+       base += step) {
+    const int64_t row = base + sub;
+    fwd_row<T, LANES, N>(a, row, row < a.rows, l,
+                         [](float v) { return group_sum<LANES>(v); }, amax_bits, l == 0);
+  }
+  if (a.amax) cta_amax_commit(amax_bits, a.amax, red_amax);
+}
+
+template <typename T, int THREADS, int N>
+__global__ void __launch_bounds__(THREADS) fwd_cta_kernel(const FwdArgs a) {
+  __shared__ float red[THREADS / 32];
+  __shared__ unsigned red_amax[THREADS / 32];
+  unsigned amax_bits = 0;
+  for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+    fwd_row<T, THREADS, N>(a, row, true, threadIdx.x,
+                           [&](float v) { return cta_sum<THREADS>(v, red); }, amax_bits,
+                           threadIdx.x == 0);
+  }
+  if (a.amax) cta_amax_commit(amax_bits, a.amax, red_amax);
+}
+
+// Any hidden size and alignment. Dynamic shared memory: hidden floats.
+template <typename T>
+__global__ void __launch_bounds__(kScalarCta) fwd_scalar_kernel(const FwdArgs a) {
+  extern __shared__ float srow[];
+  __shared__ float red[kScalarCta / 32];
+  __shared__ unsigned red_amax[kScalarCta / 32];
+  const int H = a.hidden;
+  const T* x = static_cast<const T*>(a.x);
+  const T* res = static_cast<const T*>(a.residual);
+  const T* bias = static_cast<const T*>(a.bias);
+  const T* gamma = static_cast<const T*>(a.gamma);
+  const T* beta = static_cast<const T*>(a.beta);
+  T* out_sum = static_cast<T*>(a.out_sum);
+  T* y = static_cast<T*>(a.y);
+  unsigned amax_bits = 0;
+  for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+    const int64_t off = row * (int64_t)H;
+    float t1 = 0.f;
+    // Each thread only ever reads back the srow entries it wrote itself.
+    for (int j = threadIdx.x; j < H; j += kScalarCta) {
+      float s = to_f(x[off + j]);
+      if (bias) s += to_f(bias[j]);
+      if (res) s += to_f(res[off + j]);
+      const T st = from_f<T>(s);
+      if (out_sum) out_sum[off + j] = st;
+      s = to_f(st);
+      srow[j] = s;
+      t1 += s;
+    }
+    const float mean = a.rms ? 0.f : cta_sum<kScalarCta>(t1, red) / (float)H;
+    float t2 = 0.f;
+    for (int j = threadIdx.x; j < H; j += kScalarCta) {
+      const float d = srow[j] - mean;
+      t2 = fmaf(d, d, t2);
+    }
+    const float var = cta_sum<kScalarCta>(t2, red) / (float)H;
+    const float rstd = 1.0f / sqrtf(var + a.eps);
+    if (threadIdx.x == 0) {
+      if (a.mean) a.mean[row] = mean;
+      if (a.rstd) a.rstd[row] = rstd;
+    }
+    for (int j = threadIdx.x; j < H; j += kScalarCta) {
+      const float w = a.zero_centered ? 1.0f + to_f(gamma[j]) : to_f(gamma[j]);
+      const float b = beta ? to_f(beta[j]) : 0.f;
+      const T o = from_f<T>(fmaf((srow[j] - mean) * rstd, w, b));
+      y[off + j] = o;
+      amax_bits = max(amax_bits, abs_bits(to_f(o)));
+    }
+  }
+  if (a.amax) cta_amax_commit(amax_bits, a.amax, red_amax);
+}
+
+}  // namespace nf

@@ -1,0 +1,151 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point its header declares, and rejects bad arguments on the host before
+touching CUDA.
+
+Every call below is built to fail validation, so no pointer it passes is ever
+dereferenced and nothing reaches the GPU even when one is present.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import normalization_fwd_gb300 as nf
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "normfuse.h")
+
+OK, NULL, ALIGN, SHAPE, UNSUPPORTED, CUDA, WORKSPACE, INVALID = range(8)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nf.build_library()
+    return nf.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:ln_status|const char\*|int|size_t)\s+(ln_\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted(
+        ["ln_fwd", "ln_bwd", "ln_bwd_workspace_bytes", "ln_status_string", "ln_last_cuda_error"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert sorted(nf.exported_symbols()) == declared_functions()
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = nf.ln_status_string(code)
+        assert s.startswith("LN_"), s
+    assert "unknown" in nf.ln_status_string(99)
+
+
+# Fake, never-dereferenced device addresses (256-byte aligned like cudaMalloc).
+X, RES, G, B, BIAS, S, Y, M, R, A = (0x7f0000000000 + i * 0x10000000 for i in range(10))
+
+
+def fwd(lib, x=X, bias=BIAS, residual=RES, gamma=G, beta=B, eps=1e-5, mode=0, zc=0,
+        out_sum=S, y=Y, mean=M, rstd=R, amax=A, rows=4, hidden=384, dtype=1):
+    return lib.ln_fwd(x, bias, residual, gamma, beta, eps, mode, zc, out_sum, y, mean, rstd,
+                      amax, None, rows, hidden, dtype)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(x=None), NULL),
+    (dict(y=None), NULL),
+    (dict(gamma=None), NULL),
+    (dict(dtype=3), UNSUPPORTED),
+    (dict(mode=2), UNSUPPORTED),
+    (dict(rows=-1), SHAPE),
+    (dict(hidden=0), SHAPE),
+    (dict(hidden=16385), SHAPE),
+    (dict(hidden=8200, dtype=0), SHAPE),           # fp32: 8192 max
+    (dict(x=X + 1), ALIGN),                        # bf16 needs 2-byte alignment
+    (dict(dtype=0, y=Y + 2), ALIGN),               # fp32 needs 4-byte alignment
+    (dict(mean=M + 2), ALIGN),
+    (dict(amax=A + 1), ALIGN),
+    (dict(eps=float("nan")), INVALID),
+    (dict(eps=-1.0), INVALID),
+    (dict(eps=float("inf")), INVALID),
+    (dict(y=X), INVALID),                          # output aliases input
+    (dict(out_sum=Y + 64), INVALID),               # outputs overlap each other
+    (dict(rstd=M + 8), INVALID),
+    (dict(amax=G + 16), INVALID),
+])
+def test_fwd_rejects_on_host(lib, kw, want):
+    assert fwd(lib, **kw) == want
+
+
+def test_fwd_unaligned_hidden_beyond_scalar_limit_is_rejected(lib):
+    # 16-byte misaligned rows fall to the scalar kernel, which stops at 8192.
+    assert fwd(lib, x=X + 2, hidden=9000) == SHAPE
+    assert fwd(lib, hidden=8194) == SHAPE          # 8194 * 2 bytes is not a multiple of 16
+
+
+def bwd(lib, dy=X, xs=RES, gamma=G, mean=M, rstd=R, dx=Y, dg=S, db=B, rows=4, hidden=384,
+        dtype=1, mode=0, zc=0, ws=A, ws_bytes=1 << 20):
+    return lib.ln_bwd(dy, xs, gamma, mean, rstd, dx, dg, db, None, rows, hidden, dtype, mode,
+                      zc, ws, ws_bytes)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(dy=None), NULL),
+    (dict(xs=None), NULL),
+    (dict(rstd=None), NULL),
+    (dict(dx=None), NULL),
+    (dict(dg=None), NULL),
+    (dict(mean=None), NULL),                       # LayerNorm needs the mean
+    (dict(dtype=-1), UNSUPPORTED),
+    (dict(mode=5), UNSUPPORTED),
+    (dict(rows=-3), SHAPE),
+    (dict(hidden=0), SHAPE),
+    (dict(dx=Y + 1), ALIGN),
+    (dict(dg=S + 2), ALIGN),
+    (dict(dx=X), INVALID),
+    (dict(dg=M), INVALID),
+    (dict(ws=R + 4), INVALID),
+])
+def test_bwd_rejects_on_host(lib, kw, want):
+    assert bwd(lib, **kw) == want
+
+
+def test_rmsnorm_ignores_mean_and_dbeta(lib):
+    # With mode = RMSNorm a NULL mean is fine; the call then fails on
+    # something else (here a NULL dx), proving the mean was not required.
+    assert bwd(lib, mode=1, mean=None, db=None, dx=None) == NULL
+    assert bwd(lib, mode=1, mean=None, dx=Y + 1) == ALIGN
+
+
+def test_workspace_query_on_host(lib):
+    out = ctypes.c_size_t(123)
+    assert lib.ln_bwd_workspace_bytes(0, 384, 1, 0, ctypes.byref(out)) == OK
+    assert out.value == 0
+    assert lib.ln_bwd_workspace_bytes(10, 384, 1, 0, None) == NULL
+    assert lib.ln_bwd_workspace_bytes(-1, 384, 1, 0, ctypes.byref(out)) == SHAPE
+    assert lib.ln_bwd_workspace_bytes(10, 0, 1, 0, ctypes.byref(out)) == SHAPE
+    assert lib.ln_bwd_workspace_bytes(10, 384, 7, 0, ctypes.byref(out)) == UNSUPPORTED
+    assert lib.ln_bwd_workspace_bytes(10, 20000, 1, 0, ctypes.byref(out)) == SHAPE
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import importlib
+    mod = importlib.import_module("normalization_fwd_gb300")
+    missing = str(tmp_path / "nope.so")
+    saved = mod._lib
+    mod._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="not built"):
+            mod.load_library(missing)
+    finally:
+        mod._lib = saved

@@ -1,0 +1,200 @@
+"""GPU parity on edge cases: every kernel family and lane layout, ragged row
+counts, empty inputs, optional operands switched off, unaligned pointers
+(scalar path), determinism, non-default streams and NaN propagation in amax.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import normalization_fwd_gb300 as nf
+import workloads as W
+from _parity import (amax_bits_got, amax_bits_of, check_elementwise, check_mean, check_rel,
+                     check_rel_l2, gpu_bwd, gpu_fwd, oracle_bwd_rows, oracle_fwd)
+from workloads import Workload, as_f64, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def wl(dtype, rows, hidden, mode, **kw):
+    base = dict(name=f"edge_{dtype}_{rows}x{hidden}_{mode}", dtype=dtype, rows=rows,
+                hidden=hidden, mode=mode, eps=1e-5, x_std=1.5, residual_std=1.0,
+                bias_std=0.2, gamma_std=0.3, beta_std=0.3 if mode == W.LAYERNORM else None,
+                amax=True)
+    base.update(kw)
+    return Workload(**base)
+
+
+def fwd_bwd_parity(lib, w, seed=0, x_override=None, **fwd_kw):
+    inp = make_inputs(w, seed=seed)
+    ref = oracle_fwd(w, inp, x_override=x_override)
+    got = gpu_fwd(lib, w, inp, x_override=x_override, **fwd_kw)
+    assert got["guards_ok"]
+    if "sum" in got:
+        check_elementwise(as_f64(got["sum"]), ref["sum"], w.dtype, "sum")
+    check_elementwise(as_f64(got["y"]), ref["y_exact"], w.dtype, "y")
+    if "rstd" in got:
+        check_rel(as_f64(got["rstd"]), ref["rstd_exact"], 1e-5, "rstd")
+    if "mean" in got:
+        check_mean(as_f64(got["mean"]), ref["mean_exact"], ref["sum"])
+    if "amax" in got:
+        assert amax_bits_got(got["amax"]) == amax_bits_of(got["y"])
+    if w.backward:
+        dt = W.TORCH_DTYPES[w.dtype]
+        x_sum = torch.from_numpy(ref["sum"]).to(dt)
+        mean = None if ref["mean"] is None else torch.from_numpy(ref["mean"]).float()
+        rstd = torch.from_numpy(ref["rstd"]).float()
+        bref = oracle_bwd_rows(w, inp["dy"], x_sum, inp["gamma"], mean, rstd, slice(None))
+        bgot = gpu_bwd(lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd)
+        assert bgot["guards_ok"]
+        check_elementwise(as_f64(bgot["dx"]), bref["dx_exact"], w.dtype, "dx")
+        check_rel_l2(as_f64(bgot["dgamma"]), bref["dgamma"], 1e-4, "dgamma")
+        if bref["dbeta"] is not None:
+            check_rel_l2(as_f64(bgot["dbeta"]), bref["dbeta"], 1e-4, "dbeta")
+    return inp, got
+
+
+# Hidden sizes that reach every family: warp exact fits (LANES x N), warp
+# with masked lanes, CTA per row (exact and masked), and the scalar kernel
+# (row width not a multiple of 16 bytes).
+HIDDEN_16BIT = [8, 56, 64, 128, 200, 256, 320, 384, 640, 768, 1000, 1024, 1280, 2048,
+                2056, 3000, 4096, 8192, 16384,          # vector paths
+                1, 2, 3, 7, 100, 1001, 4100]            # scalar path
+HIDDEN_F32 = [4, 28, 64, 96, 384, 500, 768, 1024, 1028, 2048, 4096, 8192,
+              1, 3, 7, 99, 1001]
+
+
+@pytest.mark.parametrize("mode", [W.LAYERNORM, W.RMSNORM])
+@pytest.mark.parametrize("hidden", HIDDEN_16BIT)
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_paths_16bit(cuda_lib, dtype, hidden, mode):
+    rows = 37 if hidden <= 4096 else 9
+    fwd_bwd_parity(cuda_lib, wl(dtype, rows, hidden, mode, zero_centered_gamma=hidden % 3 == 0))
+
+
+@pytest.mark.parametrize("mode", [W.LAYERNORM, W.RMSNORM])
+@pytest.mark.parametrize("hidden", HIDDEN_F32)
+def test_paths_f32(cuda_lib, hidden, mode):
+    rows = 37 if hidden <= 4096 else 9
+    fwd_bwd_parity(cuda_lib, wl("f32", rows, hidden, mode, zero_centered_gamma=hidden % 2 == 1))
+
+
+@pytest.mark.parametrize("rows", [1, 2, 3, 15, 16, 17, 31, 33, 100003])
+def test_ragged_row_counts(cuda_lib, rows):
+    # 384 bf16 = 16 lanes x 3 vectors, 2 rows per warp, 16 rows per CTA step.
+    fwd_bwd_parity(cuda_lib, wl("bf16", rows, 384, W.LAYERNORM))
+
+
+@pytest.mark.parametrize("variant", ["no_bias", "no_residual", "no_add", "no_beta",
+                                     "no_sum", "no_stats", "no_amax"])
+def test_optional_operands(cuda_lib, variant):
+    kw = {}
+    fkw = {}
+    if variant in ("no_bias", "no_add"):
+        kw["bias_std"] = None
+    if variant in ("no_residual", "no_add"):
+        kw["residual_std"] = None
+    if variant == "no_beta":
+        kw["beta_std"] = None
+    if variant == "no_sum":
+        fkw["store_sum"] = False
+    if variant == "no_stats":
+        fkw["stats"] = False
+    if variant == "no_amax":
+        kw["amax"] = False
+    w = wl("bf16", 41, 768, W.LAYERNORM, **kw)
+    if variant in ("no_sum", "no_stats"):
+        w = w.with_(backward=False)
+    fwd_bwd_parity(cuda_lib, w, **fkw)
+
+
+def test_empty_rows(cuda_lib):
+    for mode in (W.LAYERNORM, W.RMSNORM):
+        w = wl("bf16", 0, 384, mode)
+        inp = make_inputs(w, seed=1)
+        got = gpu_fwd(cuda_lib, w, inp)
+        assert got["guards_ok"] and got["y"].numel() == 0
+        assert float(got["amax"][0]) == 0.0
+        g = gpu_bwd(cuda_lib, w, inp["dy"], inp["x"], inp["gamma"],
+                    torch.zeros(0), torch.zeros(0))
+        assert g["guards_ok"]
+        assert (g["dgamma"] == 0).all()
+        if mode == W.LAYERNORM:
+            assert (g["dbeta"] == 0).all()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_unaligned_pointers_use_scalar_path(cuda_lib, dtype):
+    # Shift x by one element inside a larger buffer: 2- or 4-byte aligned but
+    # not 16-byte aligned, so the scalar kernel runs; results must still match.
+    w = wl(dtype, 29, 768, W.LAYERNORM)
+    inp = make_inputs(w, seed=2)
+    big = torch.empty(w.rows * w.hidden + 1, dtype=inp["x"].dtype, device="cuda")
+    big[1:] = inp["x"].reshape(-1).to("cuda")
+    x_shifted = big[1:].view(w.rows, w.hidden)
+    assert x_shifted.data_ptr() % 16 != 0
+    fwd_bwd_parity(cuda_lib, w, seed=2, x_override=x_shifted)
+
+
+def test_backward_is_deterministic(cuda_lib):
+    w = wl("bf16", 50001, 384, W.LAYERNORM)
+    inp = make_inputs(w, seed=3)
+    ref = oracle_fwd(w, inp)
+    x_sum = torch.from_numpy(ref["sum"]).to(torch.bfloat16)
+    mean = torch.from_numpy(ref["mean"]).float()
+    rstd = torch.from_numpy(ref["rstd"]).float()
+    a = gpu_bwd(cuda_lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd)
+    b = gpu_bwd(cuda_lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd)
+    for k in ("dx", "dgamma", "dbeta"):
+        bits = torch.int16 if a[k].element_size() == 2 else torch.int32
+        assert torch.equal(a[k].view(bits), b[k].view(bits)), k
+
+
+def test_forward_is_deterministic(cuda_lib):
+    w = wl("bf16", 20001, 8192 // 8, W.RMSNORM)
+    inp = make_inputs(w, seed=4)
+    a = gpu_fwd(cuda_lib, w, inp)
+    b = gpu_fwd(cuda_lib, w, inp)
+    for k in ("y", "sum", "rstd", "amax"):
+        bits = torch.int16 if a[k].element_size() == 2 else torch.int32
+        assert torch.equal(a[k].view(bits), b[k].view(bits)), k
+
+
+def test_side_stream(cuda_lib):
+    w = wl("f16", 1000, 640, W.LAYERNORM)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fwd_bwd_parity(cuda_lib, w, seed=5, stream=s)
+
+
+def test_amax_propagates_nan(cuda_lib):
+    w = wl("bf16", 64, 256, W.LAYERNORM, backward=False)
+    inp = make_inputs(w, seed=6)
+    inp["x"][10, 7] = float("inf")      # that row's statistics become NaN
+    got = gpu_fwd(cuda_lib, w, inp)
+    assert got["guards_ok"]
+    assert np.isnan(float(got["amax"][0]))
+    # the other rows are unaffected
+    ref = oracle_fwd(w, inp)
+    keep = np.r_[0:10, 11:64]
+    check_elementwise(as_f64(got["y"])[keep], ref["y_exact"][keep], "bf16", "y")
+
+
+def test_workspace_too_small_is_rejected(cuda_lib):
+    w = wl("bf16", 1000, 384, W.LAYERNORM)
+    need = nf.ln_bwd_workspace_bytes(w.rows, w.hidden, torch.bfloat16, "layernorm")
+    assert need > 0
+    dev = "cuda"
+    t = lambda *s, dt=torch.bfloat16: torch.zeros(*s, dtype=dt, device=dev)
+    small = torch.empty(need - 16, dtype=torch.uint8, device=dev)
+    with pytest.raises(nf.NormError, match="WORKSPACE"):
+        nf.ln_bwd(t(1000, 384), t(1000, 384), t(384), t(1000, dt=torch.float32),
+                  t(1000, dt=torch.float32), t(1000, 384), t(384, dt=torch.float32),
+                  t(384, dt=torch.float32), workspace=small)
+
+
+def test_overlapping_output_is_rejected(cuda_lib):
+    x = torch.randn(8, 384, device="cuda").to(torch.bfloat16)
+    g = torch.ones(384, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(nf.NormError, match="INVALID"):
+        nf.ln_fwd(x, None, None, g, None, 1e-5, "layernorm", False, None, x, None, None, None)
