@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import workloads as W
-from _parity import (amax_bits_got, amax_bits_of, check_elementwise, check_mean, check_rel,
+from _parity import (amax_bits_got, dx_row_scale, amax_bits_of, check_elementwise, check_mean, check_rel,
                      check_rel_l2, gpu_bwd, gpu_fwd, oracle_bwd_reductions, oracle_bwd_rows,
                      oracle_fwd, oracle_stats_full, rows_f64)
 from workloads import as_f64, make_inputs
@@ -45,10 +45,12 @@ def check_fwd(w, got, ref, rows=None):
                               w.dtype, "amax")
 
 
-def check_bwd(w, got, ref_rows, dg_ref, db_ref, rows=None):
+def check_bwd(w, got, ref_rows, dg_ref, db_ref, dy, gamma, rstd, rows=None):
     assert got["guards_ok"]
     dx = rows_f64(got["dx"], rows)
-    check_elementwise(dx, ref_rows["dx_exact"], w.dtype, "dx")
+    scale = dx_row_scale(rows_f64(dy, rows), rows_f64(gamma), rows_f64(rstd, rows),
+                         w.zero_centered_gamma)
+    check_elementwise(dx, ref_rows["dx_exact"], w.dtype, "dx", scale_rows=scale)
     check_rel_l2(as_f64(got["dgamma"]), dg_ref, 1e-4, "dgamma")
     if db_ref is not None:
         check_rel_l2(as_f64(got["dbeta"]), db_ref, 1e-4, "dbeta")
@@ -69,10 +71,10 @@ def run_fwd_bwd_small(lib, w):
     rstd = torch.from_numpy(ref["rstd"]).float()
     bref = oracle_bwd_rows(w, inp["dy"], x_sum, inp["gamma"], mean, rstd, slice(None))
     bgot = gpu_bwd(lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd)
-    check_bwd(w, bgot, bref, bref["dgamma"], bref["dbeta"])
+    check_bwd(w, bgot, bref, bref["dgamma"], bref["dbeta"], inp["dy"], inp["gamma"], rstd)
     # chain: the backward consumes the GPU forward's own outputs
     cgot = gpu_bwd(lib, w, inp["dy"], got["sum"], inp["gamma"], got.get("mean"), got["rstd"])
-    check_bwd(w, cgot, bref, bref["dgamma"], bref["dbeta"])
+    check_bwd(w, cgot, bref, bref["dgamma"], bref["dbeta"], inp["dy"], inp["gamma"], rstd)
 
 
 def test_layernorm_fp32_4096x384(cuda_lib):
@@ -98,7 +100,7 @@ def test_backward_bf16_576000x384(cuda_lib, w):
     rows = sample_rows(w.rows, 20000)
     ref_rows = oracle_bwd_rows(w, inp["dy"], inp["x"], inp["gamma"], mean, rstd, rows)
     dg, db = oracle_bwd_reductions(w, inp["dy"], inp["x"], inp["gamma"], mean, rstd)
-    check_bwd(w, got, ref_rows, dg, db, rows=rows)
+    check_bwd(w, got, ref_rows, dg, db, inp["dy"], inp["gamma"], rstd, rows=rows)
 
 
 def run_large_fwd_bwd(lib, w):
@@ -119,7 +121,7 @@ def run_large_fwd_bwd(lib, w):
     bgot = gpu_bwd(lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd)
     ref_rows = oracle_bwd_rows(w, inp["dy"], x_sum, inp["gamma"], mean, rstd, rows)
     dg, db = oracle_bwd_reductions(w, inp["dy"], x_sum, inp["gamma"], mean, rstd)
-    check_bwd(w, bgot, ref_rows, dg, db, rows=rows)
+    check_bwd(w, bgot, ref_rows, dg, db, inp["dy"], inp["gamma"], rstd, rows=rows)
     assert bgot["dx"].dtype == dt
 
 

@@ -9,7 +9,7 @@ import torch
 
 import normalization_fwd_gb300 as nf
 import workloads as W
-from _parity import (amax_bits_got, amax_bits_of, check_elementwise, check_mean, check_rel,
+from _parity import (amax_bits_got, dx_row_scale, amax_bits_of, check_elementwise, check_mean, check_rel,
                      check_rel_l2, gpu_bwd, gpu_fwd, oracle_bwd_rows, oracle_fwd)
 from workloads import Workload, as_f64, make_inputs
 
@@ -47,7 +47,9 @@ def fwd_bwd_parity(lib, w, seed=0, x_override=None, **fwd_kw):
         bref = oracle_bwd_rows(w, inp["dy"], x_sum, inp["gamma"], mean, rstd, slice(None))
         bgot = gpu_bwd(lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd)
         assert bgot["guards_ok"]
-        check_elementwise(as_f64(bgot["dx"]), bref["dx_exact"], w.dtype, "dx")
+        scale = dx_row_scale(as_f64(inp["dy"]), as_f64(inp["gamma"]), as_f64(rstd),
+                             w.zero_centered_gamma)
+        check_elementwise(as_f64(bgot["dx"]), bref["dx_exact"], w.dtype, "dx", scale_rows=scale)
         check_rel_l2(as_f64(bgot["dgamma"]), bref["dgamma"], 1e-4, "dgamma")
         if bref["dbeta"] is not None:
             check_rel_l2(as_f64(bgot["dbeta"]), bref["dbeta"], 1e-4, "dbeta")
