@@ -19,15 +19,16 @@
  *    call with the same results.
  *  - Outputs must not overlap inputs or each other.
  *  - Work is enqueued on `stream` (0 = the legacy default stream) and the call
- *    returns without waiting for it. The library calls no allocating CUDA API
- *    and no synchronising one.
+ *    returns without waiting for it. The library calls no allocating CUDA API,
+ *    and none that synchronises except ln_device_error().
  *  - Failure: arguments are validated on the host first; a validation failure
  *    returns its status before anything is enqueued and leaves every output
  *    untouched. A CUDA error from an enqueue returns LN_ERR_CUDA; the CUDA
  *    error code is then available from ln_last_cuda_error() on the calling
  *    thread. No entry point aborts, throws or prints.
- *  - Limits: 1 <= hidden <= LN_MAX_HIDDEN_VEC on the vectorised path,
- *    1 <= hidden <= LN_MAX_HIDDEN_SCALAR on the scalar path; rows >= 0.
+ *  - Limits: rows >= 0; 1 <= hidden <= LN_MAX_HIDDEN_VEC16 (bf16/fp16) or
+ *    LN_MAX_HIDDEN_VEC32 (fp32) on the vectorised path, and
+ *    1 <= hidden <= LN_MAX_HIDDEN_SCALAR on the scalar path.
  *
  * Citations are to the four pages the method comes from: NVIDIA/cutlass
  * discussion 874 (GEMM -> residual add -> LayerNorm), iree-org/iree issue
@@ -47,7 +48,8 @@
 extern "C" {
 #endif
 
-#define LN_MAX_HIDDEN_VEC 32768
+#define LN_MAX_HIDDEN_VEC16 16384
+#define LN_MAX_HIDDEN_VEC32 8192
 #define LN_MAX_HIDDEN_SCALAR 8192
 
 typedef enum { LN_F32 = 0, LN_BF16 = 1, LN_F16 = 2 } ln_dtype;
@@ -156,6 +158,16 @@ const char* ln_status_string(ln_status status);
 
 /* The cudaError_t behind the last LN_ERR_CUDA on the calling thread. */
 int ln_last_cuda_error(void);
+
+/*
+ * Device-side failure report. The pipelined kernels wait on shared-memory
+ * barriers for their bulk copies; every such wait gives up after one second,
+ * sets a bit in a device error word and lets the kernel finish early (its
+ * outputs are then not valid). This call waits for `stream`, ORs the error
+ * words of all kernels into *flags (bit 0: a wait timed out) and clears them.
+ * It synchronises `stream`; 0 in *flags means no kernel reported a failure.
+ */
+ln_status ln_device_error(cudaStream_t stream, unsigned* flags);
 
 #ifdef __cplusplus
 }

@@ -23,7 +23,7 @@ from .build import LIB_PATH, build as build_library
 __all__ = [
     "LN_F32", "LN_BF16", "LN_F16", "LN_LAYERNORM", "LN_RMSNORM", "NormError",
     "load_library", "build_library", "ln_fwd", "ln_bwd", "ln_bwd_workspace_bytes",
-    "ln_status_string", "ln_last_cuda_error", "exported_symbols",
+    "ln_status_string", "ln_last_cuda_error", "ln_device_error", "exported_symbols",
     "fused_norm_fwd", "fused_norm_bwd", "Workspace",
 ]
 
@@ -74,6 +74,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.ln_status_string.restype = ctypes.c_char_p
         lib.ln_last_cuda_error.argtypes = []
         lib.ln_last_cuda_error.restype = ci
+        lib.ln_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+        lib.ln_device_error.restype = ci
         _lib = lib
         return lib
 
@@ -81,7 +83,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
 def exported_symbols() -> list[str]:
     """Names of the C entry points this binding wraps."""
     return ["ln_fwd", "ln_bwd", "ln_bwd_workspace_bytes", "ln_status_string",
-            "ln_last_cuda_error"]
+            "ln_last_cuda_error", "ln_device_error"]
 
 
 def ln_status_string(status: int) -> str:
@@ -90,6 +92,17 @@ def ln_status_string(status: int) -> str:
 
 def ln_last_cuda_error() -> int:
     return int(load_library().ln_last_cuda_error())
+
+
+def ln_device_error(stream=None) -> int:
+    """Wait for ``stream`` and return (and clear) the kernels' device error
+    bits; 0 means no kernel reported a failed wait."""
+    lib = load_library()
+    flags = ctypes.c_uint(0)
+    st = lib.ln_device_error(_stream(stream), ctypes.byref(flags))
+    if st:
+        raise NormError(st, "ln_device_error")
+    return int(flags.value)
 
 
 def _ptr(t) -> int | None:

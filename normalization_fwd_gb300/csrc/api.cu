@@ -1,6 +1,8 @@
 // C entry points of the fused normalization library: argument validation,
 // per-device caches, dispatch to the per-dtype launchers.
 #include <math.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <mutex>
 #include <vector>
@@ -74,6 +76,14 @@ cudaError_t by_dtype(ln_dtype dt, F&& f) {
 
 }  // namespace
 
+int path_override() {
+  static const int v = [] {
+    const char* e = getenv("NORMFUSE_PATH");
+    return (e && strcmp(e, "registers") == 0) ? kPathRegisters : kPathDefault;
+  }();
+  return v;
+}
+
 int device_sm_count(int* sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -132,6 +142,19 @@ const char* ln_status_string(ln_status s) {
 }
 
 int ln_last_cuda_error(void) { return g_last_cuda_error; }
+
+ln_status ln_device_error(cudaStream_t stream, unsigned* flags) {
+  if (flags == nullptr) return LN_ERR_NULL;
+  *flags = 0;
+  cudaError_t (*readers[])(cudaStream_t, unsigned*) = {
+      take_error_fwd_f32, take_error_fwd_bf16, take_error_fwd_f16,
+      take_error_bwd_f32, take_error_bwd_bf16, take_error_bwd_f16};
+  for (auto r : readers) {
+    cudaError_t e = r(stream, flags);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return LN_OK;
+}
 
 ln_status ln_fwd(const void* x, const void* bias, const void* residual, const void* gamma,
                  const void* beta, float eps, ln_mode mode, int zero_centered_gamma,
@@ -192,7 +215,7 @@ ln_status ln_fwd(const void* x, const void* bias, const void* residual, const vo
   cudaError_t e = by_dtype(dtype, [&](auto t) {
     using T = decltype(t);
     Plan p;
-    cudaError_t r = fwd_plan<T>(rows, (int)hidden, vec, &p);
+    cudaError_t r = fwd_plan<T>(rows, (int)hidden, vec, residual != nullptr, &p);
     if (r != cudaSuccess) return r;
     return fwd_launch<T>(a, p, stream);
   });

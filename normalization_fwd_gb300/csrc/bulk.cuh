@@ -1,0 +1,245 @@
+// Bulk-copy pipeline primitives (sm_90+ PTX, used here on sm_103a): mbarrier
+// phase tracking, cp.async.bulk global -> shared copies that complete on an
+// mbarrier, and waits that give up after a time limit instead of spinning
+// forever.
+//
+// A pipelined CTA streams tiles of whole rows into a ring of `stages`
+// shared-memory slots. Thread 0 is the producer: at the top of iteration
+// `it` it issues the copies of the CTA's tile it + stages - 1 into the slot
+// that tile it - 1 just freed; all kConsumerWarps warps (thread 0's included)
+// consume tile `it`. Each slot has a `full` barrier (one arrival plus the
+// transaction bytes of its copies) and an `empty` barrier (one arrival per
+// warp). Round r of slot s waits `full` with parity r & 1 and `empty` with
+// parity (r & 1) ^ 1, so the first round finds every slot free.
+#pragma once
+
+#include "common.cuh"
+
+namespace nf {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kBulkThreads = kConsumerThreads;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
+
+// Error bits a kernel leaves in the device error word of its translation
+// unit (read and cleared by ln_device_error()).
+constexpr unsigned kErrWaitTimeout = 1u;
+static __device__ unsigned g_tu_error;
+
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Make the initialised barriers visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete; false when
+// it has not completed within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global to shared memory; completes as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// 16-byte load from shared memory. A plain load so the compiler can schedule
+// it; the "memory" clobber of the barrier waits orders it after the copy.
+__device__ __forceinline__ uint4 ld_vec_smem(const void* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+// VEC fp32 values from shared memory (VEC a multiple of 4, 16-byte aligned).
+template <int VEC>
+__device__ __forceinline__ void ld_f32_smem(const float* p, float* f) {
+#pragma unroll
+  for (int i = 0; i < VEC; i += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(p + i);
+    f[i] = v.x;
+    f[i + 1] = v.y;
+    f[i + 2] = v.z;
+    f[i + 3] = v.w;
+  }
+}
+
+// Ring layout in dynamic shared memory: `stages` slots of `slot_bytes`, then
+// the full and empty barriers.
+struct Ring {
+  unsigned char* base;
+  uint32_t slot_bytes;
+  int stages;
+  uint64_t* full;
+  uint64_t* empty;
+  __device__ unsigned char* slot(int s) const { return base + (size_t)s * slot_bytes; }
+};
+
+__device__ __forceinline__ Ring make_ring(unsigned char* smem, uint32_t slot_bytes, int stages) {
+  Ring r;
+  r.base = smem;
+  r.slot_bytes = slot_bytes;
+  r.stages = stages;
+  r.full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * slot_bytes);
+  r.empty = r.full + stages;
+  return r;
+}
+
+// Called by every thread of the CTA before the pipeline starts.
+__device__ __forceinline__ void ring_init(const Ring& r) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < r.stages; ++s) {
+      mbar_init(&r.full[s], 1);
+      mbar_init(&r.empty[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+}
+
+// After an aborted wait: wait (bounded) for every tile the producer issued
+// but the consumers did not take, so no copy is still writing into shared
+// memory when the CTA exits. Called by thread 0.
+__device__ __forceinline__ void ring_drain(const Ring& r, int64_t taken, int64_t issued) {
+  for (int64_t it = taken; it < issued; ++it) {
+    mbar_wait(&r.full[it % r.stages], (uint32_t)((it / r.stages) & 1));
+  }
+}
+
+// Issue the copies of the CTA's local tile `it` (global tile blockIdx.x +
+// it * gridDim.x): for each input (up to two) the tile's rows are one
+// contiguous bulk copy, the inputs back to back in the slot. Waits (bounded)
+// for the slot to be free; false on timeout. Thread 0 only.
+template <typename T>
+__device__ __forceinline__ bool issue_tile(const Ring& ring, const BulkCfg& c, int64_t it,
+                                           int64_t rows, int hidden, const T* in0,
+                                           const T* in1) {
+  const int s = (int)(it % ring.stages);
+  const uint32_t round = (uint32_t)(it / ring.stages);
+  if (!mbar_wait(&ring.empty[s], (round & 1) ^ 1)) return false;
+  const int64_t tile = blockIdx.x + it * gridDim.x;
+  const uint32_t row_bytes = (uint32_t)hidden * sizeof(T);
+  const int64_t r0 = tile * c.tile_rows;
+  const int64_t n = rows - r0 < c.tile_rows ? rows - r0 : c.tile_rows;
+  const uint32_t bytes = (uint32_t)n * row_bytes;
+  mbar_arrive_expect_tx(&ring.full[s], in1 ? 2 * bytes : bytes);
+  unsigned char* dst = ring.slot(s);
+  bulk_load(dst, in0 + r0 * hidden, bytes, &ring.full[s]);
+  if (in1) bulk_load(dst + (size_t)c.tile_rows * row_bytes, in1 + r0 * hidden, bytes, &ring.full[s]);
+  return true;
+}
+
+// The pipeline loop: `body(tile, slot)` for each of the CTA's tiles in order.
+// With kUniform (bodies with CTA-wide barriers) all threads agree on an
+// abort before anyone leaves the loop. Returns the tiles consumed; `issued`
+// (thread 0) the tiles issued; `aborted` is set when a wait timed out.
+template <bool kUniform, typename T, typename Body>
+__device__ __forceinline__ int64_t run_pipeline(const Ring& ring, const BulkCfg& c, int64_t rows,
+                                                int hidden, const T* in0, const T* in1,
+                                                bool& aborted, int64_t& issued, Body body) {
+  const int S = ring.stages;
+  const int64_t n_local = (c.num_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
+  if (threadIdx.x == 0) {
+    for (int64_t j = 0; j < S - 1 && j < n_local; ++j) {
+      if (!issue_tile<T>(ring, c, j, rows, hidden, in0, in1)) {
+        aborted = true;
+        break;
+      }
+      issued = j + 1;
+    }
+  }
+  int64_t it = 0;
+  for (; it < n_local; ++it) {
+    if (threadIdx.x == 0 && !aborted) {
+      const int64_t j = it + S - 1;
+      if (j < n_local) {
+        if (issue_tile<T>(ring, c, j, rows, hidden, in0, in1)) {
+          issued = j + 1;
+        } else {
+          aborted = true;
+        }
+      }
+    }
+    const int s = (int)(it % S);
+    int failed = !mbar_wait(&ring.full[s], (uint32_t)((it / S) & 1));
+    if (kUniform) failed = __syncthreads_or(failed);
+    if (failed) {
+      aborted = true;
+      break;
+    }
+    body(blockIdx.x + it * gridDim.x, ring.slot(s));
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&ring.empty[s]);
+  }
+  return it;
+}
+
+// End of a pipelined kernel, all threads: record an abort in the error word,
+// and on abort let thread 0 drain the copies still in flight. Returns true
+// when the kernel aborted (the caller then skips its epilogue).
+__device__ __forceinline__ bool pipeline_finish(const Ring& ring, bool aborted, int64_t issued,
+                                                int64_t taken, int* s_abort,
+                                                long long* s_taken) {
+  if (aborted) {
+    atomicOr(&g_tu_error, kErrWaitTimeout);
+    atomicExch(s_abort, 1);
+  }
+  if ((threadIdx.x & 31) == 0) atomicMin(s_taken, (long long)taken);
+  __syncthreads();
+  if (*s_abort) {
+    if (threadIdx.x == 0) ring_drain(ring, *s_taken, issued);
+    return true;
+  }
+  return false;
+}
+
+}  // namespace nf

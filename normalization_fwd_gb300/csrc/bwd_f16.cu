@@ -1,3 +1,3 @@
 // Backward kernels instantiated for f16 I/O.
 #include "dispatch.cuh"
-NF_INSTANTIATE_BWD(nf::f16)
+NF_INSTANTIATE_BWD(nf::f16, f16)

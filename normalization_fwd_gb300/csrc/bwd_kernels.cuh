@@ -3,35 +3,44 @@
 // An RMS/Layer norm backward has two kinds of reduction over the same inputs
 // (dy, x_sum and the per-row statistics): dx reduces over the hidden
 // dimension of one row, dgamma/dbeta over all rows. Here one persistent
-// kernel does both in a single read of the inputs: each row is loaded once
-// and kept in registers (the "persistent reduction" the PR requires) while
-// its dx is formed, and the row's dy * xhat and dy are added into per-thread
-// fp32 accumulators (the outer reduction turned into a partial accumulation).
-// At the end each CTA writes its partial dgamma/dbeta row to the workspace,
-// and bwd_finalize_kernel adds the partials of all CTAs in a fixed order.
+// kernel does both in a single read of the inputs: each row stays on chip
+// (the "persistent reduction" the PR requires) while its dx is formed, and
+// the row's dy * xhat and dy are added into per-thread fp32 accumulators (the
+// outer reduction turned into a partial accumulation). At the end each CTA
+// writes its partial dgamma/dbeta row to the workspace, and the finalize
+// kernel adds the partials of all CTAs in a fixed order.
 //
 // The row -> CTA assignment is a grid-stride loop over a grid sized from the
 // SM count, so the partials, and the finalize's fixed-order fp64 sum over
 // them, are the same on every run.
+//
+//  * bwd_bulk_warp_kernel / bwd_bulk_cta_kernel (default for 16-byte aligned
+//    rows): dy and x_sum tiles stream into a shared-memory ring by
+//    cp.async.bulk; the row is read from shared memory twice (sums, then dx)
+//    instead of being held in registers, and w = gamma (+1) sits in shared
+//    memory as fp32.
+//  * bwd_warp_kernel / bwd_cta_kernel: the row held in registers.
+//  * bwd_scalar_kernel: any hidden size and alignment.
 #pragma once
 
+#include "bulk.cuh"
 #include "common.cuh"
 #include "fwd_kernels.cuh"
 
 namespace nf {
 
-// One row for the vector kernels: loads dy and x_sum, computes dx, and adds
-// the row into acc_g (dy * xhat) and acc_b (dy). G threads share the row.
-template <typename T, int G, int N, typename Reduce2>
+// One row for the vector kernels: dx of the row, and the row added into
+// acc_g (dy * xhat) and acc_b (dy). G threads share the row, this one is `t`.
+// With kReread the second pass loads dy and x_sum again (cheap from shared
+// memory) rather than keeping xhat and g in registers across the reduction.
+template <typename T, int G, int N, typename Src, bool kReread, typename Reduce2>
 __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_ok, int t,
+                                        const T* dyrow, const T* xsrow, float mean, float rstd,
                                         Reduce2 reduce2, float (&acc_g)[N][Vec<T>::N],
                                         float (&acc_b)[N][Vec<T>::N]) {
   constexpr int VEC = Vec<T>::N;
   const int H = a.hidden;
   const int V = H / VEC;
-  const int64_t off = row * (int64_t)H;
-  const T* dy = static_cast<const T*>(a.dy) + off;
-  const T* xs = static_cast<const T*>(a.x_sum) + off;
   const T* gamma = static_cast<const T*>(a.gamma);
 
   uint4 dr[N], xr[N];
@@ -39,24 +48,18 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
     if (row_ok && v < V) {
-      dr[k] = ld_vec(dy + v * VEC);
-      xr[k] = ld_vec(xs + v * VEC);
+      dr[k] = Src::load(dyrow + v * VEC);
+      xr[k] = Src::load(xsrow + v * VEC);
     }
-  }
-  float mean = 0.f, rstd = 0.f;
-  if (row_ok) {
-    rstd = a.rstd[row];
-    if (!a.rms) mean = a.mean[row];
   }
 
   // xhat, g = dy * w, the two row sums, and the outer-reduction partials.
-  float xh[N][VEC], g[N][VEC];
+  float xh[kReread ? 1 : N][VEC], g[kReread ? 1 : N][VEC];
   float2 sums = make_float2(0.f, 0.f);
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) { xh[k][e] = 0.f; g[k][e] = 0.f; }
+    const int kk = kReread ? 0 : k;
     if (row_ok && v < V) {
       float d[VEC], xv[VEC], w[VEC];
       unpack<T>(dr[k], d);
@@ -65,11 +68,11 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         const float we = a.zero_centered ? 1.0f + w[e] : w[e];
-        xh[k][e] = (xv[e] - mean) * rstd;
-        g[k][e] = d[e] * we;
-        sums.x += g[k][e];
-        sums.y = fmaf(g[k][e], xh[k][e], sums.y);
-        acc_g[k][e] = fmaf(d[e], xh[k][e], acc_g[k][e]);
+        xh[kk][e] = (xv[e] - mean) * rstd;
+        g[kk][e] = d[e] * we;
+        sums.x += g[kk][e];
+        sums.y = fmaf(g[kk][e], xh[kk][e], sums.y);
+        acc_g[k][e] = fmaf(d[e], xh[kk][e], acc_g[k][e]);
         acc_b[k][e] += d[e];
       }
     }
@@ -77,59 +80,146 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
   sums = reduce2(sums);
   const float c1 = a.rms ? 0.f : sums.x / (float)H;
   const float c2 = sums.y / (float)H;
+  // Make the second pass load again instead of keeping the first pass's
+  // values live across the reduction.
+  if (kReread) asm volatile("" ::: "memory");
 
-  T* dx = static_cast<T*>(a.dx) + off;
+  T* dx = static_cast<T*>(a.dx) + row * (int64_t)H;
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
     if (row_ok && v < V) {
       float o[VEC];
+      if (kReread) {
+        float d[VEC], xv[VEC], w[VEC];
+        unpack<T>(Src::load(dyrow + v * VEC), d);
+        unpack<T>(Src::load(xsrow + v * VEC), xv);
+        unpack<T>(ld_vec_param(gamma + v * VEC), w);
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) o[e] = rstd * (g[k][e] - c1 - xh[k][e] * c2);
+        for (int e = 0; e < VEC; ++e) {
+          const float we = a.zero_centered ? 1.0f + w[e] : w[e];
+          const float xhe = (xv[e] - mean) * rstd;
+          o[e] = rstd * (d[e] * we - c1 - xhe * c2);
+        }
+      } else {
+        const int kk = kReread ? 0 : k;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[e] = rstd * (g[kk][e] - c1 - xh[kk][e] * c2);
+      }
       st_vec(dx + v * VEC, pack<T>(o));
     }
   }
 }
 
-template <typename T, int LANES, int N>
-__global__ void __launch_bounds__(kWarpCta) bwd_warp_kernel(const BwdArgs a) {
+// The row body of the pipelined kernels: dy and x_sum rows in shared memory,
+// w = gamma (+1) as fp32 in shared memory. Both passes read shared memory, so
+// only the accumulators stay in registers across the reduction.
+template <typename T, int G, int N, typename Reduce2>
+__device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool row_ok, int t,
+                                             const T* dyrow, const T* xsrow, const float* w_s,
+                                             float mean, float rstd, Reduce2 reduce2,
+                                             float (&acc_g)[N][Vec<T>::N],
+                                             float (&acc_b)[N][Vec<T>::N]) {
   constexpr int VEC = Vec<T>::N;
-  constexpr int RPW = 32 / LANES;
-  constexpr int W = kWarpCta / 32;
-  constexpr int SLOT = LANES * VEC;   // columns covered by one vector slot
-  __shared__ float red[W][SLOT];
+  const int H = a.hidden;
+  const int V = H / VEC;
+  float2 sums = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int v = k * G + t;
+    if (row_ok && v < V) {
+      float d[VEC], xv[VEC], w[VEC];
+      unpack<T>(ld_vec_smem(dyrow + v * VEC), d);
+      unpack<T>(ld_vec_smem(xsrow + v * VEC), xv);
+      ld_f32_smem<VEC>(w_s + v * VEC, w);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const float xh = (xv[e] - mean) * rstd;
+        const float g = d[e] * w[e];
+        sums.x += g;
+        sums.y = fmaf(g, xh, sums.y);
+        acc_g[k][e] = fmaf(d[e], xh, acc_g[k][e]);
+        acc_b[k][e] += d[e];
+      }
+    }
+  }
+  sums = reduce2(sums);
+  const float c1 = a.rms ? 0.f : sums.x / (float)H;
+  const float c2 = sums.y / (float)H;
+  const float a1 = -rstd * c1;
+  const float a2 = -rstd * c2;
+  asm volatile("" ::: "memory");   // the second pass reads shared memory again
+
+  T* dx = static_cast<T*>(a.dx) + row * (int64_t)H;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int v = k * G + t;
+    if (row_ok && v < V) {
+      float d[VEC], xv[VEC], w[VEC], o[VEC];
+      unpack<T>(ld_vec_smem(dyrow + v * VEC), d);
+      unpack<T>(ld_vec_smem(xsrow + v * VEC), xv);
+      ld_f32_smem<VEC>(w_s + v * VEC, w);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const float xh = (xv[e] - mean) * rstd;
+        // rstd * (g - c1 - xhat * c2)
+        o[e] = fmaf(xh, a2, fmaf(d[e] * w[e], rstd, a1));
+      }
+      st_vec(dx + v * VEC, pack<T>(o));
+    }
+  }
+}
+
+// w = gamma, or 1 + gamma, as fp32 in shared memory; all threads call it.
+template <typename T>
+__device__ __forceinline__ void stage_weight(const BwdArgs& a, float* w_s) {
+  const T* gamma = static_cast<const T*>(a.gamma);
+  for (int j = threadIdx.x; j < a.hidden; j += blockDim.x) {
+    const float g = to_f(gamma[j]);
+    w_s[j] = a.zero_centered ? 1.0f + g : g;
+  }
+  __syncthreads();
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void zero_acc(float (&acc_g)[N][Vec<T>::N],
+                                         float (&acc_b)[N][Vec<T>::N]) {
+#pragma unroll
+  for (int k = 0; k < N; ++k)
+#pragma unroll
+    for (int e = 0; e < Vec<T>::N; ++e) {
+      acc_g[k][e] = 0.f;
+      acc_b[k][e] = 0.f;
+    }
+}
+
+// Partials of a lane-group kernel: W warps, each with 32 / LANES groups that
+// hold the same columns. Groups of a warp are added by a fixed butterfly,
+// then the warps through shared memory in warp order, one vector slot at a
+// time. Slot k covers columns [k * LANES * VEC, (k + 1) * LANES * VEC). All
+// threads of the CTA call this (threads of warps >= W only pass barriers).
+template <typename T, int LANES, int N, int W>
+__device__ __forceinline__ void store_group_partials(const BwdArgs& a,
+                                                     float (&acc_g)[N][Vec<T>::N],
+                                                     float (&acc_b)[N][Vec<T>::N],
+                                                     float (*red)[LANES * Vec<T>::N]) {
+  constexpr int VEC = Vec<T>::N;
+  constexpr int SLOT = LANES * VEC;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int sub = lane / LANES;
   const int l = lane % LANES;
-
-  float acc_g[N][VEC], acc_b[N][VEC];
+  if (warp < W) {
 #pragma unroll
-  for (int k = 0; k < N; ++k)
+    for (int o = LANES; o < 32; o <<= 1)
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) { acc_g[k][e] = 0.f; acc_b[k][e] = 0.f; }
-
-  const int64_t step = (int64_t)gridDim.x * W * RPW;
-  for (int64_t base = ((int64_t)blockIdx.x * W + warp) * RPW; base < a.rows; base += step) {
-    const int64_t row = base + sub;
-    bwd_row<T, LANES, N>(a, row, row < a.rows, l,
-                         [](float2 v) { return group_sum2<LANES>(v); }, acc_g, acc_b);
+      for (int k = 0; k < N; ++k)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          acc_g[k][e] += __shfl_xor_sync(0xffffffffu, acc_g[k][e], o);
+          acc_b[k][e] += __shfl_xor_sync(0xffffffffu, acc_b[k][e], o);
+        }
   }
-
-  // Groups of one warp that share columns: fixed butterfly.
-#pragma unroll
-  for (int o = LANES; o < 32; o <<= 1)
-#pragma unroll
-    for (int k = 0; k < N; ++k)
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        acc_g[k][e] += __shfl_xor_sync(0xffffffffu, acc_g[k][e], o);
-        acc_b[k][e] += __shfl_xor_sync(0xffffffffu, acc_b[k][e], o);
-      }
-
-  // Warps of the CTA: one vector slot at a time through shared memory, then
-  // a fixed-order sum over the warps. Slot k covers columns
-  // [k * SLOT, (k + 1) * SLOT), lane l holding l * VEC .. l * VEC + VEC - 1.
   const int H = a.hidden;
   const int C = a.rms ? H : 2 * H;
   float* ws = a.ws + (int64_t)blockIdx.x * C;
@@ -137,12 +227,12 @@ __global__ void __launch_bounds__(kWarpCta) bwd_warp_kernel(const BwdArgs a) {
   for (int which = 0; which < nacc; ++which) {
 #pragma unroll
     for (int k = 0; k < N; ++k) {
-      if (sub == 0) {
+      if (warp < W && sub == 0) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) red[warp][l * VEC + e] = which ? acc_b[k][e] : acc_g[k][e];
       }
       __syncthreads();
-      for (int c = threadIdx.x; c < SLOT; c += kWarpCta) {
+      for (int c = threadIdx.x; c < SLOT; c += blockDim.x) {
         const int col = k * SLOT + c;
         if (col < H) {
           float t = 0.f;
@@ -156,28 +246,19 @@ __global__ void __launch_bounds__(kWarpCta) bwd_warp_kernel(const BwdArgs a) {
   }
 }
 
-template <typename T, int THREADS, int N>
-__global__ void __launch_bounds__(THREADS) bwd_cta_kernel(const BwdArgs a) {
+// Partials of a CTA-per-row kernel: every column belongs to one thread.
+template <typename T, int G, int N>
+__device__ __forceinline__ void store_thread_partials(const BwdArgs& a, int t,
+                                                      float (&acc_g)[N][Vec<T>::N],
+                                                      float (&acc_b)[N][Vec<T>::N]) {
   constexpr int VEC = Vec<T>::N;
-  __shared__ float2 red[THREADS / 32];
-  float acc_g[N][VEC], acc_b[N][VEC];
-#pragma unroll
-  for (int k = 0; k < N; ++k)
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) { acc_g[k][e] = 0.f; acc_b[k][e] = 0.f; }
-
-  for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
-    bwd_row<T, THREADS, N>(a, row, true, threadIdx.x,
-                           [&](float2 v) { return cta_sum2<THREADS>(v, red); }, acc_g, acc_b);
-  }
-  // Each column belongs to exactly one thread of the CTA.
   const int H = a.hidden;
   const int V = H / VEC;
   const int C = a.rms ? H : 2 * H;
   float* ws = a.ws + (int64_t)blockIdx.x * C;
 #pragma unroll
   for (int k = 0; k < N; ++k) {
-    const int v = k * THREADS + threadIdx.x;
+    const int v = k * G + t;
     if (v < V) {
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
@@ -187,6 +268,158 @@ __global__ void __launch_bounds__(THREADS) bwd_cta_kernel(const BwdArgs a) {
     }
   }
 }
+
+// ---- register kernels ------------------------------------------------------
+
+template <typename T, int LANES, int N>
+__global__ void __launch_bounds__(kWarpCta) bwd_warp_kernel(const BwdArgs a) {
+  constexpr int RPW = 32 / LANES;
+  constexpr int W = kWarpCta / 32;
+  __shared__ float red[W][LANES * Vec<T>::N];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int sub = lane / LANES;
+  const int l = lane % LANES;
+  const T* dy = static_cast<const T*>(a.dy);
+  const T* xs = static_cast<const T*>(a.x_sum);
+  float acc_g[N][Vec<T>::N], acc_b[N][Vec<T>::N];
+  zero_acc<T, N>(acc_g, acc_b);
+
+  const int64_t step = (int64_t)gridDim.x * W * RPW;
+  for (int64_t base = ((int64_t)blockIdx.x * W + warp) * RPW; base < a.rows; base += step) {
+    const int64_t row = base + sub;
+    const bool ok = row < a.rows;
+    const float rstd = ok ? a.rstd[row] : 0.f;
+    const float mean = (ok && !a.rms) ? a.mean[row] : 0.f;
+    const int64_t off = row * (int64_t)a.hidden;
+    bwd_row<T, LANES, N, FromGlobal, false>(a, row, ok, l, dy + off, xs + off, mean, rstd,
+                                            [](float2 v) { return group_sum2<LANES>(v); },
+                                            acc_g, acc_b);
+  }
+  store_group_partials<T, LANES, N, W>(a, acc_g, acc_b, red);
+}
+
+template <typename T, int THREADS, int N>
+__global__ void __launch_bounds__(THREADS) bwd_cta_kernel(const BwdArgs a) {
+  __shared__ float2 red[THREADS / 32];
+  const T* dy = static_cast<const T*>(a.dy);
+  const T* xs = static_cast<const T*>(a.x_sum);
+  float acc_g[N][Vec<T>::N], acc_b[N][Vec<T>::N];
+  zero_acc<T, N>(acc_g, acc_b);
+  for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+    const float rstd = a.rstd[row];
+    const float mean = a.rms ? 0.f : a.mean[row];
+    const int64_t off = row * (int64_t)a.hidden;
+    bwd_row<T, THREADS, N, FromGlobal, false>(
+        a, row, true, threadIdx.x, dy + off, xs + off, mean, rstd,
+        [&](float2 v) { return cta_sum2<THREADS>(v, red); }, acc_g, acc_b);
+  }
+  store_thread_partials<T, THREADS, N>(a, threadIdx.x, acc_g, acc_b);
+}
+
+// ---- bulk-copy pipelined kernels ------------------------------------------
+
+template <typename T, int LANES, int N>
+__global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const BwdArgs a,
+                                                                         const BulkCfg c) {
+  constexpr int RPW = 32 / LANES;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ float red[kConsumerWarps][LANES * Vec<T>::N];
+  __shared__ int s_abort;
+  __shared__ long long s_taken;
+  const int H = a.hidden;
+  const uint32_t in_bytes = (uint32_t)c.tile_rows * H * sizeof(T);
+  const Ring ring = make_ring(smem, 2 * in_bytes, c.stages);
+  float* w_s = reinterpret_cast<float*>(ring.empty + c.stages);
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    s_taken = 0x7fffffffffffffffll;
+  }
+  stage_weight<T>(a, w_s);
+  ring_init(ring);
+
+  const int lane = threadIdx.x & 31;
+  const int l = lane % LANES;
+  const int local = (threadIdx.x >> 5) * RPW + lane / LANES;   // row within the tile
+  float acc_g[N][Vec<T>::N], acc_b[N][Vec<T>::N];
+  zero_acc<T, N>(acc_g, acc_b);
+  // Statistics of this group's row in a tile, loaded one tile ahead.
+  auto load_stats = [&](int64_t tile, float& m, float& r) {
+    const int64_t row = tile * c.tile_rows + local;
+    m = 0.f;
+    r = 0.f;
+    if (tile < c.num_tiles && row < a.rows) {
+      r = a.rstd[row];
+      if (!a.rms) m = a.mean[row];
+    }
+  };
+  float nm, nr;
+  load_stats(blockIdx.x, nm, nr);
+  bool aborted = false;
+  int64_t issued = 0;
+  const int64_t taken = run_pipeline<false, T>(
+      ring, c, a.rows, H, static_cast<const T*>(a.dy), static_cast<const T*>(a.x_sum), aborted,
+      issued, [&](int64_t tile, unsigned char* slot) {
+        const float mean = nm, rstd = nr;
+        load_stats(tile + gridDim.x, nm, nr);
+        const int64_t row = tile * c.tile_rows + local;
+        const T* dys = reinterpret_cast<const T*>(slot) + (size_t)local * H;
+        const T* xss = reinterpret_cast<const T*>(slot + in_bytes) + (size_t)local * H;
+        bwd_row_smem<T, LANES, N>(a, row, row < a.rows, l, dys, xss, w_s, mean, rstd,
+                                  [](float2 v) { return group_sum2<LANES>(v); }, acc_g, acc_b);
+      });
+  if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;
+  store_group_partials<T, LANES, N, kConsumerWarps>(a, acc_g, acc_b, red);
+}
+
+template <typename T, int N>
+__global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_cta_kernel(const BwdArgs a,
+                                                                        const BulkCfg c) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ float2 red[kConsumerWarps];
+  __shared__ int s_abort;
+  __shared__ long long s_taken;
+  const int H = a.hidden;
+  const uint32_t in_bytes = (uint32_t)H * sizeof(T);   // one row per tile
+  const Ring ring = make_ring(smem, 2 * in_bytes, c.stages);
+  float* w_s = reinterpret_cast<float*>(ring.empty + c.stages);
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    s_taken = 0x7fffffffffffffffll;
+  }
+  stage_weight<T>(a, w_s);
+  ring_init(ring);
+
+  float acc_g[N][Vec<T>::N], acc_b[N][Vec<T>::N];
+  zero_acc<T, N>(acc_g, acc_b);
+  auto load_stats = [&](int64_t row, float& m, float& r) {
+    m = 0.f;
+    r = 0.f;
+    if (row < a.rows) {
+      r = a.rstd[row];
+      if (!a.rms) m = a.mean[row];
+    }
+  };
+  float nm, nr;
+  load_stats(blockIdx.x, nm, nr);
+  bool aborted = false;
+  int64_t issued = 0;
+  const int64_t taken = run_pipeline<true, T>(
+      ring, c, a.rows, H, static_cast<const T*>(a.dy), static_cast<const T*>(a.x_sum), aborted,
+      issued, [&](int64_t row, unsigned char* slot) {
+        const float mean = nm, rstd = nr;
+        load_stats(row + gridDim.x, nm, nr);
+        const T* dys = reinterpret_cast<const T*>(slot);
+        const T* xss = reinterpret_cast<const T*>(slot + in_bytes);
+        bwd_row_smem<T, kBulkThreads, N>(a, row, true, threadIdx.x, dys, xss, w_s, mean, rstd,
+                                         [&](float2 v) { return cta_sum2<kBulkThreads>(v, red); },
+                                         acc_g, acc_b);
+      });
+  if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;
+  store_thread_partials<T, kBulkThreads, N>(a, threadIdx.x, acc_g, acc_b);
+}
+
+// ---- scalar kernel ----------------------------------------------------------
 
 // Any hidden size and alignment. Dynamic shared memory: 4 * hidden floats
 // (two per-row staging arrays and the two column accumulators); column j

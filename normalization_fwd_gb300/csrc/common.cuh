@@ -54,6 +54,13 @@ struct BwdArgs {
   int zero_centered;
 };
 
+// Launch parameters of the pipelined (bulk-copy) kernels.
+struct BulkCfg {
+  int stages;          // ring slots
+  int tile_rows;       // rows per tile
+  int64_t num_tiles;   // ceil(rows / tile_rows)
+};
+
 // ---- scalar conversions --------------------------------------------------
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(bf16 v) { return __bfloat162float(v); }

@@ -1,3 +1,3 @@
 // Forward kernels instantiated for f16 I/O.
 #include "dispatch.cuh"
-NF_INSTANTIATE_FWD(nf::f16)
+NF_INSTANTIATE_FWD(nf::f16, f16)

@@ -1,3 +1,3 @@
 // Forward kernels instantiated for f32 I/O.
 #include "dispatch.cuh"
-NF_INSTANTIATE_FWD(float)
+NF_INSTANTIATE_FWD(float, f32)

@@ -5,38 +5,49 @@
 //
 // Every kernel keeps a row on chip between the statistics and the normalize
 // step, so each input element is read from HBM once and each output written
-// once. The row loop is a grid-stride loop; the host sizes the grid to the
-// number of CTAs that are resident at once, so the kernels run persistently
-// and the amax partial is committed once per CTA.
+// once. Row loops are grid-stride loops over a grid sized to the CTAs that
+// are resident at once (persistent kernels), so the amax partial is
+// committed once per CTA.
 //
-//  * fwd_warp_kernel: a group of LANES lanes (8, 16 or 32) owns a row held in
-//    registers as N 16-byte vectors per lane; reductions are xor-shuffle
-//    butterflies inside the group. Rows of up to 256 vectors (2048 bf16).
-//  * fwd_cta_kernel: a CTA of THREADS threads owns a row, N vectors per
-//    thread, reductions through shared memory. Rows of up to 2048 vectors.
+//  * fwd_bulk_warp_kernel / fwd_bulk_cta_kernel (default for 16-byte aligned
+//    rows): tiles of rows stream into a shared-memory ring by cp.async.bulk
+//    (issued by thread 0 a few tiles ahead) and 8 warps normalize them from
+//    shared memory (a lane group of LANES lanes per row, or all 256 threads
+//    per row for rows longer than 256 vectors).
+//  * fwd_warp_kernel / fwd_cta_kernel: the same row body with the row loaded
+//    straight into registers (128-bit loads); used when the ring does not fit.
 //  * fwd_scalar_kernel: any hidden size and alignment; element-wise loads,
 //    the row staged in shared memory.
 #pragma once
 
+#include "bulk.cuh"
 #include "common.cuh"
 
 namespace nf {
 
-constexpr int kWarpCta = 256;     // threads per CTA of the warp-per-row kernels
+constexpr int kWarpCta = 256;     // threads per CTA of the register kernels
 constexpr int kScalarCta = 256;   // threads per CTA of the scalar kernels
 
-// One row's worth of work for the vector kernels. `G` is the number of
-// threads sharing a row (LANES or THREADS), `t` this thread's index among
-// them. `reduce` sums a float over those G threads.
-template <typename T, int G, int N, typename Reduce>
+// Where a row's 16-byte vectors come from.
+struct FromGlobal {
+  static __device__ __forceinline__ uint4 load(const void* p) { return ld_vec(p); }
+};
+struct FromSmem {
+  static __device__ __forceinline__ uint4 load(const void* p) { return ld_vec_smem(p); }
+};
+
+// One row for the vector kernels. `G` threads share the row, this one is
+// `t`; `xrow` / `rrow` point at the row's x and residual (global or shared
+// memory, per Src; rrow is null without a residual). `reduce` sums a float
+// over the G threads.
+template <typename T, int G, int N, typename Src, typename Reduce>
 __device__ __forceinline__ void fwd_row(const FwdArgs& a, int64_t row, bool row_ok, int t,
-                                        Reduce reduce, unsigned& amax_bits, bool write_stats) {
+                                        const T* xrow, const T* rrow, Reduce reduce,
+                                        unsigned& amax_bits, bool write_stats) {
   constexpr int VEC = Vec<T>::N;
   const int H = a.hidden;
   const int V = H / VEC;
   const int64_t off = row * (int64_t)H;
-  const T* x = static_cast<const T*>(a.x) + off;
-  const T* res = static_cast<const T*>(a.residual) + off;
   const T* bias = static_cast<const T*>(a.bias);
 
   // Issue every load of the row before using any of it.
@@ -45,8 +56,8 @@ __device__ __forceinline__ void fwd_row(const FwdArgs& a, int64_t row, bool row_
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
     if (row_ok && v < V) {
-      xr[k] = ld_vec(x + v * VEC);
-      if (a.residual) rr[k] = ld_vec(res + v * VEC);
+      xr[k] = Src::load(xrow + v * VEC);
+      if (rrow) rr[k] = Src::load(rrow + v * VEC);
     }
   }
 
@@ -61,13 +72,13 @@ __device__ __forceinline__ void fwd_row(const FwdArgs& a, int64_t row, bool row_
     for (int e = 0; e < VEC; ++e) s[k][e] = 0.f;
     if (ok) {
       unpack<T>(xr[k], s[k]);
-      if (a.bias) {
+      if (bias) {
         float b[VEC];
         unpack<T>(ld_vec_param(bias + v * VEC), b);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) s[k][e] += b[e];
       }
-      if (a.residual) {
+      if (rrow) {
         float r[VEC];
         unpack<T>(rr[k], r);
 #pragma unroll
@@ -142,6 +153,8 @@ __device__ __forceinline__ void fwd_row(const FwdArgs& a, int64_t row, bool row_
   }
 }
 
+// ---- register kernels ------------------------------------------------------
+
 template <typename T, int LANES, int N>
 __global__ void __launch_bounds__(kWarpCta) fwd_warp_kernel(const FwdArgs a) {
   constexpr int RPW = 32 / LANES;     // rows per warp step
@@ -150,6 +163,8 @@ __global__ void __launch_bounds__(kWarpCta) fwd_warp_kernel(const FwdArgs a) {
   const int lane = threadIdx.x & 31;
   const int sub = lane / LANES;
   const int l = lane % LANES;
+  const T* x = static_cast<const T*>(a.x);
+  const T* res = static_cast<const T*>(a.residual);
   unsigned amax_bits = 0;
   const int64_t step = (int64_t)gridDim.x * W * RPW;
   // The loop bound is uniform over the warp so every lane takes part in the
@@ -157,8 +172,10 @@ __global__ void __launch_bounds__(kWarpCta) fwd_warp_kernel(const FwdArgs a) {
   for (int64_t base = ((int64_t)blockIdx.x * W + (threadIdx.x >> 5)) * RPW; base < a.rows;
        base += step) {
     const int64_t row = base + sub;
-    fwd_row<T, LANES, N>(a, row, row < a.rows, l,
-                         [](float v) { return group_sum<LANES>(v); }, amax_bits, l == 0);
+    const int64_t off = row * (int64_t)a.hidden;
+    fwd_row<T, LANES, N, FromGlobal>(a, row, row < a.rows, l, x + off, res ? res + off : nullptr,
+                                     [](float v) { return group_sum<LANES>(v); }, amax_bits,
+                                     l == 0);
   }
   if (a.amax) cta_amax_commit(amax_bits, a.amax, red_amax);
 }
@@ -167,14 +184,101 @@ template <typename T, int THREADS, int N>
 __global__ void __launch_bounds__(THREADS) fwd_cta_kernel(const FwdArgs a) {
   __shared__ float red[THREADS / 32];
   __shared__ unsigned red_amax[THREADS / 32];
+  const T* x = static_cast<const T*>(a.x);
+  const T* res = static_cast<const T*>(a.residual);
   unsigned amax_bits = 0;
   for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
-    fwd_row<T, THREADS, N>(a, row, true, threadIdx.x,
-                           [&](float v) { return cta_sum<THREADS>(v, red); }, amax_bits,
-                           threadIdx.x == 0);
+    const int64_t off = row * (int64_t)a.hidden;
+    fwd_row<T, THREADS, N, FromGlobal>(a, row, true, threadIdx.x, x + off,
+                                       res ? res + off : nullptr,
+                                       [&](float v) { return cta_sum<THREADS>(v, red); },
+                                       amax_bits, threadIdx.x == 0);
   }
   if (a.amax) cta_amax_commit(amax_bits, a.amax, red_amax);
 }
+
+// ---- bulk-copy pipelined kernels ------------------------------------------
+
+// Commit the CTA's amax partial (all threads; no-op without amax).
+__device__ __forceinline__ void commit_amax(const FwdArgs& a, unsigned amax_bits,
+                                            unsigned* red_amax) {
+  if (a.amax) cta_amax_commit(amax_bits, a.amax, red_amax);
+}
+
+template <typename T, int LANES, int N>
+__global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_warp_kernel(const FwdArgs a,
+                                                                         const BulkCfg c) {
+  constexpr int RPW = 32 / LANES;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ unsigned red_amax[kConsumerWarps];
+  __shared__ int s_abort;
+  __shared__ long long s_taken;
+  const int H = a.hidden;
+  const int n_in = a.residual ? 2 : 1;
+  const uint32_t in_bytes = (uint32_t)c.tile_rows * H * sizeof(T);
+  const Ring ring = make_ring(smem, n_in * in_bytes, c.stages);
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    s_taken = 0x7fffffffffffffffll;
+  }
+  ring_init(ring);
+
+  const int lane = threadIdx.x & 31;
+  const int l = lane % LANES;
+  const int local = (threadIdx.x >> 5) * RPW + lane / LANES;   // row within the tile
+  bool aborted = false;
+  int64_t issued = 0;
+  unsigned amax_bits = 0;
+  const int64_t taken = run_pipeline<false, T>(
+      ring, c, a.rows, H, static_cast<const T*>(a.x), static_cast<const T*>(a.residual), aborted,
+      issued, [&](int64_t tile, unsigned char* slot) {
+        const int64_t row = tile * c.tile_rows + local;
+        const T* xs = reinterpret_cast<const T*>(slot) + (size_t)local * H;
+        const T* rs = a.residual ? reinterpret_cast<const T*>(slot + in_bytes) + (size_t)local * H
+                                 : nullptr;
+        fwd_row<T, LANES, N, FromSmem>(a, row, row < a.rows, l, xs, rs,
+                                       [](float v) { return group_sum<LANES>(v); }, amax_bits,
+                                       l == 0);
+      });
+  if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;
+  commit_amax(a, amax_bits, red_amax);
+}
+
+template <typename T, int N>
+__global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_cta_kernel(const FwdArgs a,
+                                                                        const BulkCfg c) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ float red[kConsumerWarps];
+  __shared__ unsigned red_amax[kConsumerWarps];
+  __shared__ int s_abort;
+  __shared__ long long s_taken;
+  const int H = a.hidden;
+  const int n_in = a.residual ? 2 : 1;
+  const uint32_t in_bytes = (uint32_t)H * sizeof(T);   // one row per tile
+  const Ring ring = make_ring(smem, n_in * in_bytes, c.stages);
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    s_taken = 0x7fffffffffffffffll;
+  }
+  ring_init(ring);
+
+  bool aborted = false;
+  int64_t issued = 0;
+  unsigned amax_bits = 0;
+  const int64_t taken = run_pipeline<true, T>(
+      ring, c, a.rows, H, static_cast<const T*>(a.x), static_cast<const T*>(a.residual), aborted,
+      issued, [&](int64_t row, unsigned char* slot) {
+        const T* xs = reinterpret_cast<const T*>(slot);
+        const T* rs = a.residual ? reinterpret_cast<const T*>(slot + in_bytes) : nullptr;
+        fwd_row<T, kBulkThreads, N, FromSmem>(
+            a, row, true, threadIdx.x, xs, rs,
+            [&](float v) { return cta_sum<kBulkThreads>(v, red); }, amax_bits, threadIdx.x == 0);
+      });
+  if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;
+  commit_amax(a, amax_bits, red_amax);
+}
+
+// ---- scalar kernel ----------------------------------------------------------
 
 // Any hidden size and alignment. Dynamic shared memory: hidden floats.
 template <typename T>

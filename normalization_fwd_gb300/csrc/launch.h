@@ -17,20 +17,37 @@ constexpr int kMaxHiddenScalar = 8192;    // scalar kernels (shared-memory stage
 // Which kernel a call runs and how it is launched.
 struct Plan {
   const void* fn = nullptr;
-  int kind = -1;       // 0 warp-per-row, 1 CTA-per-row, 2 scalar
-  int group = 0;       // lanes per row (kind 0) or threads per CTA (kind 1, 2)
+  bool bulk = false;   // pipelined kernel taking (args, BulkCfg)
+  int kind = -1;       // 0 lane group per row, 1 CTA per row, 2 scalar
+  int group = 0;       // threads sharing a row
   int n = 0;           // 16-byte vectors per thread per row
   int block = 0;
-  size_t smem = 0;
+  size_t smem = 0;     // dynamic shared memory
   int grid = 0;        // CTAs; for the backward also the number of partials
   int ws_cols = 0;     // backward: floats per partial row
+  BulkCfg cfg = {0, 0, 0};
 };
 
 // Per-device facts, cached (api.cu).
 int device_sm_count(int* sms);                                  // returns cudaError_t
 int resident_blocks(const void* fn, int block, size_t smem, int* out);  // returns cudaError_t
 
-template <typename T> cudaError_t fwd_plan(int64_t rows, int hidden, bool vec, Plan* p);
+// Kernel family override from the NORMFUSE_PATH environment variable
+// ("registers" selects the register kernels for aligned rows), read once.
+constexpr int kPathDefault = 0;
+constexpr int kPathRegisters = 1;
+int path_override();
+
+// Read and clear the device error word of each kernel translation unit.
+cudaError_t take_error_fwd_f32(cudaStream_t st, unsigned* out);
+cudaError_t take_error_fwd_bf16(cudaStream_t st, unsigned* out);
+cudaError_t take_error_fwd_f16(cudaStream_t st, unsigned* out);
+cudaError_t take_error_bwd_f32(cudaStream_t st, unsigned* out);
+cudaError_t take_error_bwd_bf16(cudaStream_t st, unsigned* out);
+cudaError_t take_error_bwd_f16(cudaStream_t st, unsigned* out);
+
+template <typename T>
+cudaError_t fwd_plan(int64_t rows, int hidden, bool vec, bool has_residual, Plan* p);
 template <typename T> cudaError_t fwd_launch(const FwdArgs& a, const Plan& p, cudaStream_t st);
 template <typename T> cudaError_t bwd_plan(int64_t rows, int hidden, bool rms, bool vec, Plan* p);
 template <typename T>

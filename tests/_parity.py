@@ -84,6 +84,7 @@ def gpu_fwd(lib, w, inp, *, store_sum=True, stats=True, amax=None, stream=None,
     lib.ln_fwd(x, bias, res, gamma, beta, w.eps, w.mode, w.zero_centered_gamma,
                g.get("sum"), g["y"], g.get("mean"), g.get("rstd"), g.get("amax"), stream)
     torch.cuda.synchronize()
+    assert lib.ln_device_error() == 0, "a kernel reported a failed wait"
     result = {k: v.t.cpu() for k, v in outs.items()}
     result["guards_ok"] = all(v.guards_intact() for v in outs.values())
     return result
@@ -106,6 +107,7 @@ def gpu_bwd(lib, w, dy, x_sum, gamma, mean, rstd, *, need_dbeta=True, workspace=
     lib.ln_bwd(dy, x_sum, gamma, mean, rstd, g["dx"], g["dgamma"], g.get("dbeta"), stream,
                mode=w.mode, zero_centered_gamma=w.zero_centered_gamma, workspace=workspace)
     torch.cuda.synchronize()
+    assert lib.ln_device_error() == 0, "a kernel reported a failed wait"
     result = {k: v.t.cpu() for k, v in outs.items()}
     result["guards_ok"] = all(v.guards_intact() for v in outs.values())
     return result

@@ -35,7 +35,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
-        ["ln_fwd", "ln_bwd", "ln_bwd_workspace_bytes", "ln_status_string", "ln_last_cuda_error"])
+        ["ln_fwd", "ln_bwd", "ln_bwd_workspace_bytes", "ln_status_string", "ln_last_cuda_error",
+         "ln_device_error"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -136,6 +137,10 @@ def test_workspace_query_on_host(lib):
     assert lib.ln_bwd_workspace_bytes(10, 0, 1, 0, ctypes.byref(out)) == SHAPE
     assert lib.ln_bwd_workspace_bytes(10, 384, 7, 0, ctypes.byref(out)) == UNSUPPORTED
     assert lib.ln_bwd_workspace_bytes(10, 20000, 1, 0, ctypes.byref(out)) == SHAPE
+
+
+def test_device_error_query_rejects_null(lib):
+    assert lib.ln_device_error(None, None) == NULL
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
