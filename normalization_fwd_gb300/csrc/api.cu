@@ -147,8 +147,9 @@ ln_status ln_device_error(cudaStream_t stream, unsigned* flags) {
   if (flags == nullptr) return LN_ERR_NULL;
   *flags = 0;
   cudaError_t (*readers[])(cudaStream_t, unsigned*) = {
-      take_error_fwd_f32, take_error_fwd_bf16, take_error_fwd_f16,
-      take_error_bwd_f32, take_error_bwd_bf16, take_error_bwd_f16};
+      take_error_fwd_bulk_f32,    take_error_fwd_bulk_bf16,    take_error_fwd_bulk_f16,
+      take_error_bwd_bulk_ln_f32, take_error_bwd_bulk_ln_bf16, take_error_bwd_bulk_ln_f16,
+      take_error_bwd_bulk_rms_f32, take_error_bwd_bulk_rms_bf16, take_error_bwd_bulk_rms_f16};
   for (auto r : readers) {
     cudaError_t e = r(stream, flags);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -215,7 +216,8 @@ ln_status ln_fwd(const void* x, const void* bias, const void* residual, const vo
   cudaError_t e = by_dtype(dtype, [&](auto t) {
     using T = decltype(t);
     Plan p;
-    cudaError_t r = fwd_plan<T>(rows, (int)hidden, vec, residual != nullptr, &p);
+    const int n_params = 1 + (bias != nullptr) + (beta != nullptr);
+    cudaError_t r = fwd_plan<T>(rows, (int)hidden, vec, residual != nullptr, n_params, &p);
     if (r != cudaSuccess) return r;
     return fwd_launch<T>(a, p, stream);
   });

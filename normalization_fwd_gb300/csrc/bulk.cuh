@@ -17,9 +17,6 @@
 
 namespace nf {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kBulkThreads = kConsumerThreads;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
 
 // Error bits a kernel leaves in the device error word of its translation

@@ -113,8 +113,9 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
 
 // The row body of the pipelined kernels: dy and x_sum rows in shared memory,
 // w = gamma (+1) as fp32 in shared memory. Both passes read shared memory, so
-// only the accumulators stay in registers across the reduction.
-template <typename T, int G, int N, typename Reduce2>
+// only the accumulators stay in registers across the reduction. kRms drops
+// the mean, c1 and the dbeta accumulators at compile time.
+template <typename T, int G, int N, bool kRms, typename Reduce2>
 __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool row_ok, int t,
                                              const T* dyrow, const T* xsrow, const float* w_s,
                                              float mean, float rstd, Reduce2 reduce2,
@@ -134,20 +135,20 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
       ld_f32_smem<VEC>(w_s + v * VEC, w);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        const float xh = (xv[e] - mean) * rstd;
+        const float xh = (kRms ? xv[e] : xv[e] - mean) * rstd;
         const float g = d[e] * w[e];
-        sums.x += g;
+        if (!kRms) sums.x += g;
         sums.y = fmaf(g, xh, sums.y);
         acc_g[k][e] = fmaf(d[e], xh, acc_g[k][e]);
-        acc_b[k][e] += d[e];
+        if (!kRms) acc_b[k][e] += d[e];
       }
     }
   }
   sums = reduce2(sums);
-  const float c1 = a.rms ? 0.f : sums.x / (float)H;
+  // dx = rstd * (g - c1 - xhat * c2) = (x - mean) * b2 + (g * rstd + a1)
   const float c2 = sums.y / (float)H;
-  const float a1 = -rstd * c1;
-  const float a2 = -rstd * c2;
+  const float a1 = kRms ? 0.f : -rstd * (sums.x / (float)H);
+  const float b2 = -rstd * rstd * c2;
   asm volatile("" ::: "memory");   // the second pass reads shared memory again
 
   T* dx = static_cast<T*>(a.dx) + row * (int64_t)H;
@@ -161,9 +162,8 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
       ld_f32_smem<VEC>(w_s + v * VEC, w);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        const float xh = (xv[e] - mean) * rstd;
-        // rstd * (g - c1 - xhat * c2)
-        o[e] = fmaf(xh, a2, fmaf(d[e] * w[e], rstd, a1));
+        const float xm = kRms ? xv[e] : xv[e] - mean;
+        o[e] = fmaf(xm, b2, fmaf(d[e] * w[e], rstd, a1));
       }
       st_vec(dx + v * VEC, pack<T>(o));
     }
@@ -198,7 +198,7 @@ __device__ __forceinline__ void zero_acc(float (&acc_g)[N][Vec<T>::N],
 // then the warps through shared memory in warp order, one vector slot at a
 // time. Slot k covers columns [k * LANES * VEC, (k + 1) * LANES * VEC). All
 // threads of the CTA call this (threads of warps >= W only pass barriers).
-template <typename T, int LANES, int N, int W>
+template <typename T, int LANES, int N, int W, bool kRms>
 __device__ __forceinline__ void store_group_partials(const BwdArgs& a,
                                                      float (&acc_g)[N][Vec<T>::N],
                                                      float (&acc_b)[N][Vec<T>::N],
@@ -217,19 +217,21 @@ __device__ __forceinline__ void store_group_partials(const BwdArgs& a,
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
           acc_g[k][e] += __shfl_xor_sync(0xffffffffu, acc_g[k][e], o);
-          acc_b[k][e] += __shfl_xor_sync(0xffffffffu, acc_b[k][e], o);
+          if (!kRms) acc_b[k][e] += __shfl_xor_sync(0xffffffffu, acc_b[k][e], o);
         }
   }
+  const bool rms = kRms || a.rms;
   const int H = a.hidden;
-  const int C = a.rms ? H : 2 * H;
+  const int C = rms ? H : 2 * H;
   float* ws = a.ws + (int64_t)blockIdx.x * C;
-  const int nacc = a.rms ? 1 : 2;
+  const int nacc = rms ? 1 : 2;
   for (int which = 0; which < nacc; ++which) {
 #pragma unroll
     for (int k = 0; k < N; ++k) {
       if (warp < W && sub == 0) {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) red[warp][l * VEC + e] = which ? acc_b[k][e] : acc_g[k][e];
+        for (int e = 0; e < VEC; ++e)
+          red[warp][l * VEC + e] = (!kRms && which) ? acc_b[k][e] : acc_g[k][e];
       }
       __syncthreads();
       for (int c = threadIdx.x; c < SLOT; c += blockDim.x) {
@@ -247,14 +249,15 @@ __device__ __forceinline__ void store_group_partials(const BwdArgs& a,
 }
 
 // Partials of a CTA-per-row kernel: every column belongs to one thread.
-template <typename T, int G, int N>
+template <typename T, int G, int N, bool kRms>
 __device__ __forceinline__ void store_thread_partials(const BwdArgs& a, int t,
                                                       float (&acc_g)[N][Vec<T>::N],
                                                       float (&acc_b)[N][Vec<T>::N]) {
   constexpr int VEC = Vec<T>::N;
+  const bool rms = kRms || a.rms;
   const int H = a.hidden;
   const int V = H / VEC;
-  const int C = a.rms ? H : 2 * H;
+  const int C = rms ? H : 2 * H;
   float* ws = a.ws + (int64_t)blockIdx.x * C;
 #pragma unroll
   for (int k = 0; k < N; ++k) {
@@ -263,7 +266,7 @@ __device__ __forceinline__ void store_thread_partials(const BwdArgs& a, int t,
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         ws[v * VEC + e] = acc_g[k][e];
-        if (!a.rms) ws[H + v * VEC + e] = acc_b[k][e];
+        if (!rms) ws[H + v * VEC + e] = acc_b[k][e];
       }
     }
   }
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(kWarpCta) bwd_warp_kernel(const BwdArgs a) {
                                             [](float2 v) { return group_sum2<LANES>(v); },
                                             acc_g, acc_b);
   }
-  store_group_partials<T, LANES, N, W>(a, acc_g, acc_b, red);
+  store_group_partials<T, LANES, N, W, false>(a, acc_g, acc_b, red);
 }
 
 template <typename T, int THREADS, int N>
@@ -314,12 +317,12 @@ __global__ void __launch_bounds__(THREADS) bwd_cta_kernel(const BwdArgs a) {
         a, row, true, threadIdx.x, dy + off, xs + off, mean, rstd,
         [&](float2 v) { return cta_sum2<THREADS>(v, red); }, acc_g, acc_b);
   }
-  store_thread_partials<T, THREADS, N>(a, threadIdx.x, acc_g, acc_b);
+  store_thread_partials<T, THREADS, N, false>(a, threadIdx.x, acc_g, acc_b);
 }
 
 // ---- bulk-copy pipelined kernels ------------------------------------------
 
-template <typename T, int LANES, int N>
+template <typename T, int LANES, int N, bool kRms>
 __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const BwdArgs a,
                                                                          const BulkCfg c) {
   constexpr int RPW = 32 / LANES;
@@ -365,14 +368,15 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
         const int64_t row = tile * c.tile_rows + local;
         const T* dys = reinterpret_cast<const T*>(slot) + (size_t)local * H;
         const T* xss = reinterpret_cast<const T*>(slot + in_bytes) + (size_t)local * H;
-        bwd_row_smem<T, LANES, N>(a, row, row < a.rows, l, dys, xss, w_s, mean, rstd,
-                                  [](float2 v) { return group_sum2<LANES>(v); }, acc_g, acc_b);
+        bwd_row_smem<T, LANES, N, kRms>(a, row, row < a.rows, l, dys, xss, w_s, mean, rstd,
+                                        [](float2 v) { return group_sum2<LANES>(v); }, acc_g,
+                                        acc_b);
       });
   if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;
-  store_group_partials<T, LANES, N, kConsumerWarps>(a, acc_g, acc_b, red);
+  store_group_partials<T, LANES, N, kConsumerWarps, kRms>(a, acc_g, acc_b, red);
 }
 
-template <typename T, int N>
+template <typename T, int N, bool kRms>
 __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_cta_kernel(const BwdArgs a,
                                                                         const BulkCfg c) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -411,12 +415,12 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_cta_kernel(const Bwd
         load_stats(row + gridDim.x, nm, nr);
         const T* dys = reinterpret_cast<const T*>(slot);
         const T* xss = reinterpret_cast<const T*>(slot + in_bytes);
-        bwd_row_smem<T, kBulkThreads, N>(a, row, true, threadIdx.x, dys, xss, w_s, mean, rstd,
-                                         [&](float2 v) { return cta_sum2<kBulkThreads>(v, red); },
-                                         acc_g, acc_b);
+        bwd_row_smem<T, kBulkThreads, N, kRms>(
+            a, row, true, threadIdx.x, dys, xss, w_s, mean, rstd,
+            [&](float2 v) { return cta_sum2<kBulkThreads>(v, red); }, acc_g, acc_b);
       });
   if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;
-  store_thread_partials<T, kBulkThreads, N>(a, threadIdx.x, acc_g, acc_b);
+  store_thread_partials<T, kBulkThreads, N, kRms>(a, threadIdx.x, acc_g, acc_b);
 }
 
 // ---- scalar kernel ----------------------------------------------------------

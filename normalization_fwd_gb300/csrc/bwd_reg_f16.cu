@@ -1,0 +1,6 @@
+// Register and scalar backward kernels, f16 I/O.
+#include "tables.cuh"
+
+const void* nf::bwd_reg_table_f16(int kind, int group, int n) {
+  return bwd_reg_table_impl<nf::f16>(kind, group, n);
+}

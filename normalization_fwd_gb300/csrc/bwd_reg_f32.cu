@@ -1,0 +1,6 @@
+// Register and scalar backward kernels, f32 I/O.
+#include "tables.cuh"
+
+const void* nf::bwd_reg_table_f32(int kind, int group, int n) {
+  return bwd_reg_table_impl<float>(kind, group, n);
+}

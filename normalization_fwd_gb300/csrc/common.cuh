@@ -12,6 +12,12 @@ namespace nf {
 using bf16 = __nv_bfloat16;
 using f16 = __half;
 
+// Block shapes shared by the kernels and the host-side planner.
+constexpr int kWarpCta = 256;          // threads per CTA of the register kernels
+constexpr int kScalarCta = 256;        // threads per CTA of the scalar kernels
+constexpr int kConsumerWarps = 8;      // warps of a pipelined CTA
+constexpr int kBulkThreads = kConsumerWarps * 32;
+
 // Elements per 16-byte vector.
 template <typename T> struct Vec;
 template <> struct Vec<float> { static constexpr int N = 4; };
@@ -143,6 +149,39 @@ template <> __device__ __forceinline__ uint4 pack<f16>(const float* f) {
 // that also lets a NaN win, as torch.amax does.
 __device__ __forceinline__ unsigned abs_bits(float v) {
   return __float_as_uint(v) & 0x7fffffffu;
+}
+
+// Running amax over stored 16-byte vectors. For 16-bit types the
+// accumulator holds two halves (|y| bit patterns compared as unsigned 16-bit
+// lanes, which orders non-negative bf16/fp16 values like the values and lets
+// NaN win); amax_bits<T>() turns it into the fp32 bit pattern of the max.
+template <typename T> __device__ __forceinline__ void amax_update(unsigned& acc, const uint4& u);
+template <> __device__ __forceinline__ void amax_update<float>(unsigned& acc, const uint4& u) {
+  acc = max(acc, u.x & 0x7fffffffu);
+  acc = max(acc, u.y & 0x7fffffffu);
+  acc = max(acc, u.z & 0x7fffffffu);
+  acc = max(acc, u.w & 0x7fffffffu);
+}
+__device__ __forceinline__ void amax_update_16(unsigned& acc, const uint4& u) {
+  acc = __vmaxu2(acc, u.x & 0x7fff7fffu);
+  acc = __vmaxu2(acc, u.y & 0x7fff7fffu);
+  acc = __vmaxu2(acc, u.z & 0x7fff7fffu);
+  acc = __vmaxu2(acc, u.w & 0x7fff7fffu);
+}
+template <> __device__ __forceinline__ void amax_update<bf16>(unsigned& acc, const uint4& u) {
+  amax_update_16(acc, u);
+}
+template <> __device__ __forceinline__ void amax_update<f16>(unsigned& acc, const uint4& u) {
+  amax_update_16(acc, u);
+}
+template <typename T> __device__ __forceinline__ unsigned amax_bits(unsigned acc);
+template <> __device__ __forceinline__ unsigned amax_bits<float>(unsigned acc) { return acc; }
+template <> __device__ __forceinline__ unsigned amax_bits<bf16>(unsigned acc) {
+  return max(acc & 0xffffu, acc >> 16) << 16;   // bf16 bits are the top half of fp32 bits
+}
+template <> __device__ __forceinline__ unsigned amax_bits<f16>(unsigned acc) {
+  const unsigned short m = (unsigned short)max(acc & 0xffffu, acc >> 16);
+  return __float_as_uint(__half2float(__ushort_as_half(m)));
 }
 
 // ---- reductions ----------------------------------------------------------

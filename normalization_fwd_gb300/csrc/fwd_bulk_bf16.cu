@@ -1,0 +1,9 @@
+// Pipelined forward kernels, bf16 I/O.
+#include "tables.cuh"
+
+const void* nf::fwd_bulk_table_bf16(int kind, int group, int n) {
+  return fwd_bulk_table_impl<nf::bf16>(kind, group, n);
+}
+cudaError_t nf::take_error_fwd_bulk_bf16(cudaStream_t st, unsigned* out) {
+  return take_tu_error(st, out);
+}

@@ -25,9 +25,6 @@
 
 namespace nf {
 
-constexpr int kWarpCta = 256;     // threads per CTA of the register kernels
-constexpr int kScalarCta = 256;   // threads per CTA of the scalar kernels
-
 // Where a row's 16-byte vectors come from.
 struct FromGlobal {
   static __device__ __forceinline__ uint4 load(const void* p) { return ld_vec(p); }
@@ -43,7 +40,7 @@ struct FromSmem {
 template <typename T, int G, int N, typename Src, typename Reduce>
 __device__ __forceinline__ void fwd_row(const FwdArgs& a, int64_t row, bool row_ok, int t,
                                         const T* xrow, const T* rrow, Reduce reduce,
-                                        unsigned& amax_bits, bool write_stats) {
+                                        unsigned& amax_acc, bool write_stats) {
   constexpr int VEC = Vec<T>::N;
   const int H = a.hidden;
   const int V = H / VEC;
@@ -101,6 +98,7 @@ __device__ __forceinline__ void fwd_row(const FwdArgs& a, int64_t row, bool row_
       for (int e = 0; e < VEC; ++e) t1 += s[k][e];
     mean = reduce(t1) / (float)H;
   }
+  // Centre in place (s - mean is needed twice).
   float t2 = 0.f;
 #pragma unroll
   for (int k = 0; k < N; ++k) {
@@ -108,8 +106,8 @@ __device__ __forceinline__ void fwd_row(const FwdArgs& a, int64_t row, bool row_
     if (ok) {
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        const float d = s[k][e] - mean;
-        t2 = fmaf(d, d, t2);
+        s[k][e] -= mean;
+        t2 = fmaf(s[k][e], s[k][e], t2);
       }
     }
   }
@@ -140,15 +138,11 @@ __device__ __forceinline__ void fwd_row(const FwdArgs& a, int64_t row, bool row_
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         const float we = a.zero_centered ? 1.0f + w[e] : w[e];
-        o[e] = fmaf((s[k][e] - mean) * rstd, we, b[e]);
+        o[e] = fmaf(s[k][e] * rstd, we, b[e]);
       }
       const uint4 packed = pack<T>(o);
       st_vec(y + v * VEC, packed);
-      if (a.amax) {
-        unpack<T>(packed, o);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) amax_bits = max(amax_bits, abs_bits(o[e]));
-      }
+      if (a.amax) amax_update<T>(amax_acc, packed);
     }
   }
 }
@@ -165,7 +159,7 @@ __global__ void __launch_bounds__(kWarpCta) fwd_warp_kernel(const FwdArgs a) {
   const int l = lane % LANES;
   const T* x = static_cast<const T*>(a.x);
   const T* res = static_cast<const T*>(a.residual);
-  unsigned amax_bits = 0;
+  unsigned amax_acc = 0;
   const int64_t step = (int64_t)gridDim.x * W * RPW;
   // The loop bound is uniform over the warp so every lane takes part in the
   // shuffles; a group past the last row runs with its loads and stores off.
@@ -174,10 +168,10 @@ __global__ void __launch_bounds__(kWarpCta) fwd_warp_kernel(const FwdArgs a) {
     const int64_t row = base + sub;
     const int64_t off = row * (int64_t)a.hidden;
     fwd_row<T, LANES, N, FromGlobal>(a, row, row < a.rows, l, x + off, res ? res + off : nullptr,
-                                     [](float v) { return group_sum<LANES>(v); }, amax_bits,
+                                     [](float v) { return group_sum<LANES>(v); }, amax_acc,
                                      l == 0);
   }
-  if (a.amax) cta_amax_commit(amax_bits, a.amax, red_amax);
+  if (a.amax) cta_amax_commit(amax_bits<T>(amax_acc), a.amax, red_amax);
 }
 
 template <typename T, int THREADS, int N>
@@ -186,23 +180,128 @@ __global__ void __launch_bounds__(THREADS) fwd_cta_kernel(const FwdArgs a) {
   __shared__ unsigned red_amax[THREADS / 32];
   const T* x = static_cast<const T*>(a.x);
   const T* res = static_cast<const T*>(a.residual);
-  unsigned amax_bits = 0;
+  unsigned amax_acc = 0;
   for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
     const int64_t off = row * (int64_t)a.hidden;
     fwd_row<T, THREADS, N, FromGlobal>(a, row, true, threadIdx.x, x + off,
                                        res ? res + off : nullptr,
                                        [&](float v) { return cta_sum<THREADS>(v, red); },
-                                       amax_bits, threadIdx.x == 0);
+                                       amax_acc, threadIdx.x == 0);
   }
-  if (a.amax) cta_amax_commit(amax_bits, a.amax, red_amax);
+  if (a.amax) cta_amax_commit(amax_bits<T>(amax_acc), a.amax, red_amax);
 }
 
 // ---- bulk-copy pipelined kernels ------------------------------------------
 
-// Commit the CTA's amax partial (all threads; no-op without amax).
-__device__ __forceinline__ void commit_amax(const FwdArgs& a, unsigned amax_bits,
-                                            unsigned* red_amax) {
-  if (a.amax) cta_amax_commit(amax_bits, a.amax, red_amax);
+// Per-column parameters as fp32 in shared memory, staged once per CTA:
+// w = gamma (+1 for zero-centered gamma), bias and beta (when present).
+struct FwdParams {
+  const float* w;
+  const float* bias;   // null without bias
+  const float* beta;   // null without beta
+};
+
+template <typename T>
+__device__ __forceinline__ FwdParams stage_fwd_params(const FwdArgs& a, float* p_s) {
+  const int H = a.hidden;
+  const T* gamma = static_cast<const T*>(a.gamma);
+  const T* bias = static_cast<const T*>(a.bias);
+  const T* beta = static_cast<const T*>(a.beta);
+  float* w_s = p_s;
+  float* bias_s = bias ? p_s + H : nullptr;
+  float* beta_s = beta ? p_s + (bias ? 2 : 1) * H : nullptr;
+  for (int j = threadIdx.x; j < H; j += blockDim.x) {
+    const float g = to_f(gamma[j]);
+    w_s[j] = a.zero_centered ? 1.0f + g : g;
+    if (bias_s) bias_s[j] = to_f(bias[j]);
+    if (beta_s) beta_s[j] = to_f(beta[j]);
+  }
+  __syncthreads();
+  return {w_s, bias_s, beta_s};
+}
+
+// The row body of the pipelined kernels: x and residual rows in shared
+// memory (ring slot), parameters as fp32 in shared memory.
+template <typename T, int G, int N, typename Reduce>
+__device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool row_ok, int t,
+                                             const T* xrow, const T* rrow, const FwdParams& p,
+                                             Reduce reduce, unsigned& amax_acc, bool write_stats) {
+  constexpr int VEC = Vec<T>::N;
+  const int H = a.hidden;
+  const int V = H / VEC;
+  T* sum_row = a.out_sum ? static_cast<T*>(a.out_sum) + row * (int64_t)H : nullptr;
+  T* y_row = static_cast<T*>(a.y) + row * (int64_t)H;
+
+  // F1: s = (x + bias) + residual in fp32, stored rounded; the statistics
+  // see the stored value.
+  float s[N][VEC];
+  float t1 = 0.f;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int v = k * G + t;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) s[k][e] = 0.f;
+    if (row_ok && v < V) {
+      unpack<T>(ld_vec_smem(xrow + v * VEC), s[k]);
+      if (p.bias) {
+        float b[VEC];
+        ld_f32_smem<VEC>(p.bias + v * VEC, b);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) s[k][e] += b[e];
+      }
+      if (rrow) {
+        float r[VEC];
+        unpack<T>(ld_vec_smem(rrow + v * VEC), r);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) s[k][e] += r[e];
+      }
+      const uint4 packed = pack<T>(s[k]);
+      if (sum_row) st_vec(sum_row + v * VEC, packed);
+      unpack<T>(packed, s[k]);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) t1 += s[k][e];
+    }
+  }
+
+  // F2: mean, then the centred sum of squares (RMSNorm: mean 0).
+  const float mean = a.rms ? 0.f : reduce(t1) / (float)H;
+  float t2 = 0.f;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    if (row_ok && (k * G + t) < V) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        s[k][e] -= mean;
+        t2 = fmaf(s[k][e], s[k][e], t2);
+      }
+    }
+  }
+  const float rstd = 1.0f / sqrtf(reduce(t2) / (float)H + a.eps);
+  if (row_ok && write_stats) {
+    if (a.mean) a.mean[row] = mean;
+    if (a.rstd) a.rstd[row] = rstd;
+  }
+
+  // F3: y = (s - mean) * rstd * w + beta; F4: amax of the stored y.
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int v = k * G + t;
+    if (row_ok && v < V) {
+      float w[VEC], o[VEC];
+      ld_f32_smem<VEC>(p.w + v * VEC, w);
+      if (p.beta) {
+        ld_f32_smem<VEC>(p.beta + v * VEC, o);
+      } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) o[e] = fmaf(s[k][e] * rstd, w[e], o[e]);
+      const uint4 packed = pack<T>(o);
+      st_vec(y_row + v * VEC, packed);
+      if (a.amax) amax_update<T>(amax_acc, packed);
+    }
+  }
 }
 
 template <typename T, int LANES, int N>
@@ -221,6 +320,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_warp_kernel(const Fw
     s_abort = 0;
     s_taken = 0x7fffffffffffffffll;
   }
+  const FwdParams p = stage_fwd_params<T>(a, reinterpret_cast<float*>(ring.empty + c.stages));
   ring_init(ring);
 
   const int lane = threadIdx.x & 31;
@@ -228,7 +328,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_warp_kernel(const Fw
   const int local = (threadIdx.x >> 5) * RPW + lane / LANES;   // row within the tile
   bool aborted = false;
   int64_t issued = 0;
-  unsigned amax_bits = 0;
+  unsigned amax_acc = 0;
   const int64_t taken = run_pipeline<false, T>(
       ring, c, a.rows, H, static_cast<const T*>(a.x), static_cast<const T*>(a.residual), aborted,
       issued, [&](int64_t tile, unsigned char* slot) {
@@ -236,12 +336,11 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_warp_kernel(const Fw
         const T* xs = reinterpret_cast<const T*>(slot) + (size_t)local * H;
         const T* rs = a.residual ? reinterpret_cast<const T*>(slot + in_bytes) + (size_t)local * H
                                  : nullptr;
-        fwd_row<T, LANES, N, FromSmem>(a, row, row < a.rows, l, xs, rs,
-                                       [](float v) { return group_sum<LANES>(v); }, amax_bits,
-                                       l == 0);
+        fwd_row_smem<T, LANES, N>(a, row, row < a.rows, l, xs, rs, p,
+                                  [](float v) { return group_sum<LANES>(v); }, amax_acc, l == 0);
       });
   if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;
-  commit_amax(a, amax_bits, red_amax);
+  if (a.amax) cta_amax_commit(amax_bits<T>(amax_acc), a.amax, red_amax);
 }
 
 template <typename T, int N>
@@ -260,22 +359,23 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_cta_kernel(const Fwd
     s_abort = 0;
     s_taken = 0x7fffffffffffffffll;
   }
+  const FwdParams p = stage_fwd_params<T>(a, reinterpret_cast<float*>(ring.empty + c.stages));
   ring_init(ring);
 
   bool aborted = false;
   int64_t issued = 0;
-  unsigned amax_bits = 0;
+  unsigned amax_acc = 0;
   const int64_t taken = run_pipeline<true, T>(
       ring, c, a.rows, H, static_cast<const T*>(a.x), static_cast<const T*>(a.residual), aborted,
       issued, [&](int64_t row, unsigned char* slot) {
         const T* xs = reinterpret_cast<const T*>(slot);
         const T* rs = a.residual ? reinterpret_cast<const T*>(slot + in_bytes) : nullptr;
-        fwd_row<T, kBulkThreads, N, FromSmem>(
-            a, row, true, threadIdx.x, xs, rs,
-            [&](float v) { return cta_sum<kBulkThreads>(v, red); }, amax_bits, threadIdx.x == 0);
+        fwd_row_smem<T, kBulkThreads, N>(a, row, true, threadIdx.x, xs, rs, p,
+                                         [&](float v) { return cta_sum<kBulkThreads>(v, red); },
+                                         amax_acc, threadIdx.x == 0);
       });
   if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;
-  commit_amax(a, amax_bits, red_amax);
+  if (a.amax) cta_amax_commit(amax_bits<T>(amax_acc), a.amax, red_amax);
 }
 
 // ---- scalar kernel ----------------------------------------------------------
@@ -294,7 +394,7 @@ __global__ void __launch_bounds__(kScalarCta) fwd_scalar_kernel(const FwdArgs a)
   const T* beta = static_cast<const T*>(a.beta);
   T* out_sum = static_cast<T*>(a.out_sum);
   T* y = static_cast<T*>(a.y);
-  unsigned amax_bits = 0;
+  unsigned amax_u = 0;
   for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
     const int64_t off = row * (int64_t)H;
     float t1 = 0.f;
@@ -326,10 +426,10 @@ __global__ void __launch_bounds__(kScalarCta) fwd_scalar_kernel(const FwdArgs a)
       const float b = beta ? to_f(beta[j]) : 0.f;
       const T o = from_f<T>(fmaf((srow[j] - mean) * rstd, w, b));
       y[off + j] = o;
-      amax_bits = max(amax_bits, abs_bits(to_f(o)));
+      amax_u = max(amax_u, abs_bits(to_f(o)));
     }
   }
-  if (a.amax) cta_amax_commit(amax_bits, a.amax, red_amax);
+  if (a.amax) cta_amax_commit(amax_u, a.amax, red_amax);
 }
 
 }  // namespace nf

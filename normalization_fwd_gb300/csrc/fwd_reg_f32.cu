@@ -1,0 +1,6 @@
+// Register and scalar forward kernels, f32 I/O.
+#include "tables.cuh"
+
+const void* nf::fwd_reg_table_f32(int kind, int group, int n) {
+  return fwd_reg_table_impl<float>(kind, group, n);
+}

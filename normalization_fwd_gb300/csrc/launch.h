@@ -38,16 +38,26 @@ constexpr int kPathDefault = 0;
 constexpr int kPathRegisters = 1;
 int path_override();
 
-// Read and clear the device error word of each kernel translation unit.
-cudaError_t take_error_fwd_f32(cudaStream_t st, unsigned* out);
-cudaError_t take_error_fwd_bf16(cudaStream_t st, unsigned* out);
-cudaError_t take_error_fwd_f16(cudaStream_t st, unsigned* out);
-cudaError_t take_error_bwd_f32(cudaStream_t st, unsigned* out);
-cudaError_t take_error_bwd_bf16(cudaStream_t st, unsigned* out);
-cudaError_t take_error_bwd_f16(cudaStream_t st, unsigned* out);
+// Kernel tables, one per family and dtype, each defined in its own
+// translation unit: (kind, lanes or threads, vectors per thread) -> kernel.
+#define NF_DECLARE_TABLES(NAME)                                           \
+  const void* fwd_bulk_table_##NAME(int kind, int group, int n);          \
+  const void* fwd_reg_table_##NAME(int kind, int group, int n);           \
+  const void* bwd_bulk_ln_table_##NAME(int kind, int group, int n);       \
+  const void* bwd_bulk_rms_table_##NAME(int kind, int group, int n);      \
+  const void* bwd_reg_table_##NAME(int kind, int group, int n);           \
+  cudaError_t take_error_fwd_bulk_##NAME(cudaStream_t st, unsigned* out); \
+  cudaError_t take_error_bwd_bulk_ln_##NAME(cudaStream_t st, unsigned* out); \
+  cudaError_t take_error_bwd_bulk_rms_##NAME(cudaStream_t st, unsigned* out);
+NF_DECLARE_TABLES(f32)
+NF_DECLARE_TABLES(bf16)
+NF_DECLARE_TABLES(f16)
+#undef NF_DECLARE_TABLES
 
+// n_params: parameter rows (w, and bias / beta when given).
 template <typename T>
-cudaError_t fwd_plan(int64_t rows, int hidden, bool vec, bool has_residual, Plan* p);
+cudaError_t fwd_plan(int64_t rows, int hidden, bool vec, bool has_residual, int n_params,
+                     Plan* p);
 template <typename T> cudaError_t fwd_launch(const FwdArgs& a, const Plan& p, cudaStream_t st);
 template <typename T> cudaError_t bwd_plan(int64_t rows, int hidden, bool rms, bool vec, Plan* p);
 template <typename T>

@@ -1,0 +1,208 @@
+// Host-side planning and launching: which kernel runs a call, its grid,
+// block and shared memory, and the launch itself. Kernels come from the
+// per-family tables of the kernel translation units (tables.cuh).
+#include <algorithm>
+
+#include "launch.h"
+
+namespace nf {
+
+// Shape -> kernel family. Rows of up to 256 vectors go to a lane group of a
+// warp (exact fit preferred: LANES * N == vectors per row), longer rows to a
+// whole CTA; unaligned or odd-width rows to the scalar kernel.
+struct Choice {
+  int kind, group, n;
+};
+inline Choice choose(int hidden, int vec_elems, bool vec) {
+  if (!vec) return {2, kScalarCta, 0};
+  const int V = hidden / vec_elems;
+  if (V <= 256) {
+    for (int lanes : {32, 16, 8}) {
+      if (V % lanes == 0) {
+        const int n = V / lanes;
+        if (n <= 8 && n != 7) return {0, lanes, n};
+      }
+    }
+    for (int lanes : {8, 16, 32}) {
+      if (lanes * 8 >= V) {
+        int n = (V + lanes - 1) / lanes;
+        if (n == 7) n = 8;
+        return {0, lanes, n};
+      }
+    }
+  }
+  for (int threads : {128, 256, 512}) {
+    if (threads * 4 >= V) {
+      const int n = (V + threads - 1) / threads;
+      return {1, threads, n < 3 ? 3 : n};
+    }
+  }
+  return {-1, 0, 0};
+}
+
+// Vectors per consumer thread when the 256 consumers of a pipelined CTA
+// share one row (rows of more than 256 vectors).
+inline int bulk_cta_n(int hidden, int vec_elems) {
+  const int V = hidden / vec_elems;
+  int n = (V + kBulkThreads - 1) / kBulkThreads;
+  if (n == 7) n = 8;
+  return n < 2 ? 2 : n;
+}
+
+// The kernel tables of one dtype.
+template <typename T> struct Tables;
+#define NF_TABLES(T, NAME)                                                          \
+  template <> struct Tables<T> {                                                    \
+    static const void* fwd_bulk(int k, int g, int n) { return fwd_bulk_table_##NAME(k, g, n); } \
+    static const void* fwd_reg(int k, int g, int n) { return fwd_reg_table_##NAME(k, g, n); }   \
+    static const void* bwd_bulk(int k, int g, int n, bool rms) {                    \
+      return rms ? bwd_bulk_rms_table_##NAME(k, g, n) : bwd_bulk_ln_table_##NAME(k, g, n); \
+    }                                                                               \
+    static const void* bwd_reg(int k, int g, int n) { return bwd_reg_table_##NAME(k, g, n); }   \
+  };
+NF_TABLES(float, f32)
+NF_TABLES(bf16, bf16)
+NF_TABLES(f16, f16)
+#undef NF_TABLES
+
+// Ring sizing: the slots of one CTA should fill about kRingTarget bytes so
+// two pipelined CTAs fit on an SM; never fewer than 2 nor more than 8 slots.
+constexpr size_t kRingTarget = 104 * 1024;
+constexpr size_t kMaxDynSmem = 200 * 1024;
+
+// Fill in a pipelined plan; false when the ring does not fit. `extra`:
+// shared bytes after the ring's barriers (the backward's fp32 weight row).
+inline bool fill_bulk(Plan* p, const Choice& c, int64_t rows, int hidden, size_t esize, int n_in,
+                      size_t extra) {
+  const int tile_rows = c.kind == 0 ? kConsumerWarps * (32 / c.group) : 1;
+  const size_t slot = (size_t)n_in * tile_rows * hidden * esize;
+  const size_t room = kRingTarget > extra ? kRingTarget - extra : 0;
+  int stages = (int)std::min<size_t>(8, std::max<size_t>(2, room / slot));
+  size_t smem = (size_t)stages * slot + 2 * stages * sizeof(uint64_t) + extra;
+  if (smem > kMaxDynSmem) return false;
+  p->bulk = true;
+  p->kind = c.kind;
+  p->group = c.kind == 0 ? c.group : kBulkThreads;
+  p->n = c.n;
+  p->block = kBulkThreads;
+  p->smem = smem;
+  p->cfg.stages = stages;
+  p->cfg.tile_rows = tile_rows;
+  p->cfg.num_tiles = (rows + tile_rows - 1) / tile_rows;
+  return true;
+}
+
+// Fill block, shared memory and the rows one CTA covers per loop step of the
+// register or scalar kernels.
+inline int64_t fill_shape(Plan* p, const Choice& c, int hidden, bool bwd) {
+  p->bulk = false;
+  p->kind = c.kind;
+  p->group = c.group;
+  p->n = c.n;
+  if (c.kind == 0) {
+    p->block = kWarpCta;
+    p->smem = 0;
+    return (kWarpCta / 32) * (32 / c.group);
+  }
+  if (c.kind == 1) {
+    p->block = c.group;
+    p->smem = 0;
+    return 1;
+  }
+  p->block = kScalarCta;
+  p->smem = (size_t)hidden * sizeof(float) * (bwd ? 4 : 1);
+  return 1;
+}
+
+// Persistent grid: every CTA resident at once, never more CTAs than row steps.
+inline cudaError_t size_grid(Plan* p, int64_t steps) {
+  if (p->fn == nullptr) return cudaErrorInvalidValue;
+  if (p->smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(p->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)p->smem);
+    if (e != cudaSuccess) return e;
+  }
+  int sms = 0, per_sm = 0;
+  cudaError_t e = (cudaError_t)device_sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  e = (cudaError_t)resident_blocks(p->fn, p->block, p->smem, &per_sm);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  p->grid = (int)std::max<int64_t>(1, std::min<int64_t>(steps, (int64_t)per_sm * sms));
+  return cudaSuccess;
+}
+
+// Plan shared by both directions. n_in: streamed [rows, hidden] inputs;
+// n_params: [hidden] parameter rows the pipelined kernels stage in shared
+// memory as fp32.
+template <typename T>
+cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, int n_in,
+                      int n_params, Plan* p) {
+  Choice c = choose(hidden, Vec<T>::N, vec);
+  const bool want_bulk = vec && path_override() != kPathRegisters;
+  if (want_bulk) {
+    Choice b = c;
+    if (c.kind == 1) b.n = bulk_cta_n(hidden, Vec<T>::N);
+    const size_t extra = (size_t)n_params * hidden * sizeof(float);
+    if (fill_bulk(p, b, rows, hidden, sizeof(T), n_in, extra)) {
+      p->fn = bwd ? Tables<T>::bwd_bulk(b.kind, b.group, b.n, rms)
+                  : Tables<T>::fwd_bulk(b.kind, b.group, b.n);
+      return size_grid(p, p->cfg.num_tiles);
+    }
+  }
+  p->fn = bwd ? Tables<T>::bwd_reg(c.kind, c.group, c.n) : Tables<T>::fwd_reg(c.kind, c.group, c.n);
+  const int64_t rpc = fill_shape(p, c, hidden, bwd);
+  return size_grid(p, (rows + rpc - 1) / rpc);
+}
+
+template <typename T>
+cudaError_t fwd_plan(int64_t rows, int hidden, bool vec, bool has_residual, int n_params,
+                     Plan* p) {
+  return make_plan<T>(rows, hidden, vec, false, false, has_residual ? 2 : 1, n_params, p);
+}
+
+// Pipelined kernels take (args, BulkCfg); the others take (args) only.
+inline cudaError_t launch_plan(const Plan& p, void* args0, cudaStream_t st) {
+  BulkCfg cfg = p.cfg;
+  void* args_bulk[] = {args0, &cfg};
+  void* args_one[] = {args0};
+  return cudaLaunchKernel(p.fn, dim3(p.grid), dim3(p.block), p.bulk ? args_bulk : args_one,
+                          p.smem, st);
+}
+
+template <typename T> cudaError_t fwd_launch(const FwdArgs& a, const Plan& p, cudaStream_t st) {
+  return launch_plan(p, const_cast<FwdArgs*>(&a), st);
+}
+
+template <typename T> cudaError_t bwd_plan(int64_t rows, int hidden, bool rms, bool vec, Plan* p) {
+  cudaError_t e = make_plan<T>(rows, hidden, vec, true, rms, 2, 1, p);
+  p->ws_cols = rms ? hidden : 2 * hidden;
+  return e;
+}
+
+template <typename T>
+cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, float* dgamma, float* dbeta,
+                       cudaStream_t st) {
+  cudaError_t e = launch_plan(p, const_cast<BwdArgs*>(&a), st);
+  if (e != cudaSuccess) return e;
+  return launch_bwd_finalize(a.ws, p.grid, p.ws_cols, a.hidden, dgamma, a.rms ? nullptr : dbeta,
+                             st);
+}
+
+}  // namespace nf
+
+template cudaError_t nf::fwd_plan<float>(int64_t, int, bool, bool, int, nf::Plan*);
+template cudaError_t nf::fwd_plan<nf::bf16>(int64_t, int, bool, bool, int, nf::Plan*);
+template cudaError_t nf::fwd_plan<nf::f16>(int64_t, int, bool, bool, int, nf::Plan*);
+template cudaError_t nf::bwd_plan<float>(int64_t, int, bool, bool, nf::Plan*);
+template cudaError_t nf::bwd_plan<nf::bf16>(int64_t, int, bool, bool, nf::Plan*);
+template cudaError_t nf::bwd_plan<nf::f16>(int64_t, int, bool, bool, nf::Plan*);
+template cudaError_t nf::fwd_launch<float>(const nf::FwdArgs&, const nf::Plan&, cudaStream_t);
+template cudaError_t nf::fwd_launch<nf::bf16>(const nf::FwdArgs&, const nf::Plan&, cudaStream_t);
+template cudaError_t nf::fwd_launch<nf::f16>(const nf::FwdArgs&, const nf::Plan&, cudaStream_t);
+template cudaError_t nf::bwd_launch<float>(const nf::BwdArgs&, const nf::Plan&, float*, float*,
+                                           cudaStream_t);
+template cudaError_t nf::bwd_launch<nf::bf16>(const nf::BwdArgs&, const nf::Plan&, float*, float*,
+                                              cudaStream_t);
+template cudaError_t nf::bwd_launch<nf::f16>(const nf::BwdArgs&, const nf::Plan&, float*, float*,
+                                             cudaStream_t);

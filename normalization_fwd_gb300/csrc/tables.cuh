@@ -1,0 +1,130 @@
+// Kernel tables: (family, lanes or threads, vectors per thread) -> kernel.
+// Included by the kernel translation units, each of which instantiates one
+// family for one dtype (so the instantiations compile in parallel) and
+// exposes it through a plain function declared in launch.h.
+#pragma once
+
+#include "bwd_kernels.cuh"
+#include "fwd_kernels.cuh"
+#include "launch.h"
+
+namespace nf {
+
+#define NF_WARP_CASES(KERNEL, T, L)                \
+  switch (n) {                                     \
+    case 1: return (const void*)KERNEL<T, L, 1>;   \
+    case 2: return (const void*)KERNEL<T, L, 2>;   \
+    case 3: return (const void*)KERNEL<T, L, 3>;   \
+    case 4: return (const void*)KERNEL<T, L, 4>;   \
+    case 5: return (const void*)KERNEL<T, L, 5>;   \
+    case 6: return (const void*)KERNEL<T, L, 6>;   \
+    case 8: return (const void*)KERNEL<T, L, 8>;   \
+    default: return nullptr;                       \
+  }
+#define NF_CTA_CASES(KERNEL, T, TH)                \
+  switch (n) {                                     \
+    case 3: return (const void*)KERNEL<T, TH, 3>;  \
+    case 4: return (const void*)KERNEL<T, TH, 4>;  \
+    default: return nullptr;                       \
+  }
+#define NF_BULK_WARP_CASES_M(KERNEL, T, L, M)      \
+  switch (n) {                                     \
+    case 1: return (const void*)KERNEL<T, L, 1, M>; \
+    case 2: return (const void*)KERNEL<T, L, 2, M>; \
+    case 3: return (const void*)KERNEL<T, L, 3, M>; \
+    case 4: return (const void*)KERNEL<T, L, 4, M>; \
+    case 5: return (const void*)KERNEL<T, L, 5, M>; \
+    case 6: return (const void*)KERNEL<T, L, 6, M>; \
+    case 8: return (const void*)KERNEL<T, L, 8, M>; \
+    default: return nullptr;                       \
+  }
+#define NF_BULK_CTA_CASES_M(KERNEL, T, M)          \
+  switch (n) {                                     \
+    case 2: return (const void*)KERNEL<T, 2, M>;   \
+    case 3: return (const void*)KERNEL<T, 3, M>;   \
+    case 4: return (const void*)KERNEL<T, 4, M>;   \
+    case 5: return (const void*)KERNEL<T, 5, M>;   \
+    case 6: return (const void*)KERNEL<T, 6, M>;   \
+    case 8: return (const void*)KERNEL<T, 8, M>;   \
+    default: return nullptr;                       \
+  }
+#define NF_BULK_CTA_CASES(KERNEL, T)               \
+  switch (n) {                                     \
+    case 2: return (const void*)KERNEL<T, 2>;      \
+    case 3: return (const void*)KERNEL<T, 3>;      \
+    case 4: return (const void*)KERNEL<T, 4>;      \
+    case 5: return (const void*)KERNEL<T, 5>;      \
+    case 6: return (const void*)KERNEL<T, 6>;      \
+    case 8: return (const void*)KERNEL<T, 8>;      \
+    default: return nullptr;                       \
+  }
+
+template <typename T> const void* fwd_bulk_table_impl(int kind, int group, int n) {
+  if (kind == 0) {
+    if (group == 8) { NF_WARP_CASES(fwd_bulk_warp_kernel, T, 8) }
+    if (group == 16) { NF_WARP_CASES(fwd_bulk_warp_kernel, T, 16) }
+    if (group == 32) { NF_WARP_CASES(fwd_bulk_warp_kernel, T, 32) }
+  } else if (kind == 1) {
+    NF_BULK_CTA_CASES(fwd_bulk_cta_kernel, T)
+  }
+  return nullptr;
+}
+
+template <typename T> const void* fwd_reg_table_impl(int kind, int group, int n) {
+  if (kind == 0) {
+    if (group == 8) { NF_WARP_CASES(fwd_warp_kernel, T, 8) }
+    if (group == 16) { NF_WARP_CASES(fwd_warp_kernel, T, 16) }
+    if (group == 32) { NF_WARP_CASES(fwd_warp_kernel, T, 32) }
+  } else if (kind == 1) {
+    if (group == 128) { NF_CTA_CASES(fwd_cta_kernel, T, 128) }
+    if (group == 256) { NF_CTA_CASES(fwd_cta_kernel, T, 256) }
+    if (group == 512) { NF_CTA_CASES(fwd_cta_kernel, T, 512) }
+  } else if (kind == 2) {
+    return (const void*)fwd_scalar_kernel<T>;
+  }
+  return nullptr;
+}
+
+template <typename T, bool kRms> const void* bwd_bulk_table_impl(int kind, int group, int n) {
+  if (kind == 0) {
+    if (group == 8) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 8, kRms) }
+    if (group == 16) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 16, kRms) }
+    if (group == 32) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 32, kRms) }
+  } else if (kind == 1) {
+    NF_BULK_CTA_CASES_M(bwd_bulk_cta_kernel, T, kRms)
+  }
+  return nullptr;
+}
+
+template <typename T> const void* bwd_reg_table_impl(int kind, int group, int n) {
+  if (kind == 0) {
+    if (group == 8) { NF_WARP_CASES(bwd_warp_kernel, T, 8) }
+    if (group == 16) { NF_WARP_CASES(bwd_warp_kernel, T, 16) }
+    if (group == 32) { NF_WARP_CASES(bwd_warp_kernel, T, 32) }
+  } else if (kind == 1) {
+    if (group == 128) { NF_CTA_CASES(bwd_cta_kernel, T, 128) }
+    if (group == 256) { NF_CTA_CASES(bwd_cta_kernel, T, 256) }
+    if (group == 512) { NF_CTA_CASES(bwd_cta_kernel, T, 512) }
+  } else if (kind == 2) {
+    return (const void*)bwd_scalar_kernel<T>;
+  }
+  return nullptr;
+}
+
+// Read and clear this translation unit's device error word, after `st`.
+static inline cudaError_t take_tu_error(cudaStream_t st, unsigned* out) {
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_tu_error, sizeof(v), 0,
+                                            cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return e;
+  if (v) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_tu_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  }
+  *out |= v;
+  return e;
+}
+
+}  // namespace nf
