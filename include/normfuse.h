@@ -52,6 +52,9 @@ extern "C" {
 #define LN_MAX_HIDDEN_VEC32 8192
 #define LN_MAX_HIDDEN_SCALAR 8192
 
+/* Size of the static device scratch array behind ln_bwd_noalloc (16 MiB). */
+#define LN_NOALLOC_SCRATCH_BYTES (16u << 20)
+
 typedef enum { LN_F32 = 0, LN_BF16 = 1, LN_F16 = 2 } ln_dtype;
 typedef enum { LN_LAYERNORM = 0, LN_RMSNORM = 1 } ln_mode;
 typedef enum {
@@ -62,7 +65,9 @@ typedef enum {
   LN_ERR_UNSUPPORTED = 4, /* unknown dtype or mode */
   LN_ERR_CUDA = 5,        /* a CUDA call failed; see ln_last_cuda_error() */
   LN_ERR_WORKSPACE = 6,   /* backward workspace missing, misaligned or too small */
-  LN_ERR_INVALID = 7      /* eps negative or not finite; outputs overlap inputs */
+  LN_ERR_INVALID = 7,     /* eps negative or not finite; outputs overlap inputs */
+  LN_ERR_SCRATCH_LIMIT = 8 /* ln_bwd_noalloc: the shape needs more scratch than
+                              LN_NOALLOC_SCRATCH_BYTES */
 } ln_status;
 
 /*
@@ -152,6 +157,40 @@ ln_status ln_bwd(const void* dy, const void* x_sum, const void* gamma,
  */
 ln_status ln_bwd_workspace_bytes(int64_t rows, int64_t hidden, ln_dtype dtype,
                                  ln_mode mode, size_t* bytes);
+
+/*
+ * ln_bwd_noalloc: ln_bwd for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that must not call cudaMalloc or any allocator around a backward pass: code
+ * recorded into a CUDA graph or running under a framework that owns every
+ * device allocation through its own pool, runtimes with a fixed device memory
+ * budget set up front, and callers on a path where an allocation (which may
+ * synchronise the device) is not allowed. It computes exactly what ln_bwd
+ * computes, with the same kernels, arguments and results; the difference is
+ * that the per-CTA dgamma/dbeta partials go to a static device array of
+ * LN_NOALLOC_SCRATCH_BYTES inside the library instead of a caller workspace.
+ *
+ * - The array is part of the library image: every GPU that loads the library
+ *   holds it until the process exits. No call allocates or frees anything.
+ * - Set-up: the first call on a device looks up the array's device address
+ *   (with that device current) and caches it; make that first call before any
+ *   stream capture that includes it.
+ * - Limit: shapes whose partials need more than LN_NOALLOC_SCRATCH_BYTES
+ *   (ln_bwd_workspace_bytes() reports the need) return LN_ERR_SCRATCH_LIMIT
+ *   before anything is enqueued. At 2 CTAs per SM on 152 SMs that is about
+ *   hidden <= 6800 for LayerNorm and hidden <= 13700 for RMSNorm.
+ * - Every call on a device shares the one array and nothing in it needs to
+ *   start at zero (each call overwrites the partials it reads). Calls whose
+ *   execution overlaps on the GPU (different streams, or different host
+ *   threads) race on the array; serialise them, e.g. on one stream.
+ * - Other arguments, errors and results: as ln_bwd.
+ */
+ln_status ln_bwd_noalloc(const void* dy, const void* x_sum, const void* gamma,
+                         const float* mean, const float* rstd, void* dx,
+                         float* dgamma, float* dbeta, cudaStream_t stream,
+                         int64_t rows, int64_t hidden, ln_dtype dtype,
+                         ln_mode mode, int zero_centered_gamma);
 
 /* Static, human-readable name of a status code. */
 const char* ln_status_string(ln_status status);

@@ -23,7 +23,8 @@ from .build import LIB_PATH, build as build_library
 __all__ = [
     "LN_F32", "LN_BF16", "LN_F16", "LN_LAYERNORM", "LN_RMSNORM", "NormError",
     "load_library", "build_library", "ln_fwd", "ln_bwd", "ln_bwd_workspace_bytes",
-    "ln_status_string", "ln_last_cuda_error", "ln_device_error", "exported_symbols",
+    "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc",
+    "exported_symbols",
     "fused_norm_fwd", "fused_norm_bwd", "Workspace",
 ]
 
@@ -76,6 +77,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.ln_last_cuda_error.restype = ci
         lib.ln_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
         lib.ln_device_error.restype = ci
+        lib.ln_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, ci, ci]
+        lib.ln_bwd_noalloc.restype = ci
         _lib = lib
         return lib
 
@@ -83,7 +86,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
 def exported_symbols() -> list[str]:
     """Names of the C entry points this binding wraps."""
     return ["ln_fwd", "ln_bwd", "ln_bwd_workspace_bytes", "ln_status_string",
-            "ln_last_cuda_error", "ln_device_error"]
+            "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc"]
 
 
 def ln_status_string(status: int) -> str:
@@ -192,6 +195,24 @@ def ln_bwd(dy, x_sum, gamma, mean, rstd, dx, dgamma, dbeta, stream=None, *, mode
                     _mode(mode), int(bool(zero_centered_gamma)), _ptr(workspace), ws_bytes)
     if st:
         raise NormError(st, "ln_bwd")
+
+
+def ln_bwd_noalloc(dy, x_sum, gamma, mean, rstd, dx, dgamma, dbeta, stream=None, *,
+                   mode="layernorm", zero_centered_gamma=False) -> None:
+    """``ln_bwd`` without a workspace: the library's static scratch array holds
+    the partials, so neither this call nor the library allocates memory.
+
+    For callers that cannot allocate device memory around the backward
+    (see ``ln_bwd_noalloc`` in include/normfuse.h for the size limit and the
+    rule that calls overlapping on the GPU race on the shared array).
+    """
+    lib = load_library()
+    rows, hidden = _shape(dy)
+    st = lib.ln_bwd_noalloc(_ptr(dy), _ptr(x_sum), _ptr(gamma), _ptr(mean), _ptr(rstd),
+                            _ptr(dx), _ptr(dgamma), _ptr(dbeta), _stream(stream), rows, hidden,
+                            _dtype(dy), _mode(mode), int(bool(zero_centered_gamma)))
+    if st:
+        raise NormError(st, "ln_bwd_noalloc")
 
 
 class Workspace:

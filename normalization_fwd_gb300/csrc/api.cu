@@ -137,11 +137,16 @@ const char* ln_status_string(ln_status s) {
     case LN_ERR_CUDA: return "LN_ERR_CUDA: a CUDA call failed (see ln_last_cuda_error)";
     case LN_ERR_WORKSPACE: return "LN_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case LN_ERR_INVALID: return "LN_ERR_INVALID: bad eps, or outputs overlap inputs";
+    case LN_ERR_SCRATCH_LIMIT:
+      return "LN_ERR_SCRATCH_LIMIT: the shape needs more scratch than the library's static "
+             "array (LN_NOALLOC_SCRATCH_BYTES) holds; use ln_bwd with a workspace";
   }
   return "unknown ln_status";
 }
 
 int ln_last_cuda_error(void) { return g_last_cuda_error; }
+
+void nf_set_last_cuda_error(int e) { g_last_cuda_error = e; }
 
 ln_status ln_device_error(cudaStream_t stream, unsigned* flags) {
   if (flags == nullptr) return LN_ERR_NULL;

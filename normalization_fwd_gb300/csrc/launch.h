@@ -69,3 +69,6 @@ cudaError_t launch_bwd_finalize(const float* ws, int P, int C, int H, float* dga
                                 float* dbeta, cudaStream_t st);
 
 }  // namespace nf
+
+// Record the cudaError_t that ln_last_cuda_error() reports (api.cu).
+extern "C" void nf_set_last_cuda_error(int e);

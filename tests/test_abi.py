@@ -17,7 +17,7 @@ import normalization_fwd_gb300 as nf
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "normfuse.h")
 
-OK, NULL, ALIGN, SHAPE, UNSUPPORTED, CUDA, WORKSPACE, INVALID = range(8)
+OK, NULL, ALIGN, SHAPE, UNSUPPORTED, CUDA, WORKSPACE, INVALID, SCRATCH_LIMIT = range(9)
 
 
 @pytest.fixture(scope="module")
@@ -36,7 +36,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["ln_fwd", "ln_bwd", "ln_bwd_workspace_bytes", "ln_status_string", "ln_last_cuda_error",
-         "ln_device_error"])
+         "ln_device_error", "ln_bwd_noalloc"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         s = nf.ln_status_string(code)
         assert s.startswith("LN_"), s
     assert "unknown" in nf.ln_status_string(99)
