@@ -97,16 +97,56 @@ __device__ __forceinline__ uint4 ld_vec_smem(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
 
-// VEC fp32 values from shared memory (VEC a multiple of 4, 16-byte aligned).
-template <int VEC>
-__device__ __forceinline__ void ld_f32_smem(const float* p, float* f) {
+// A [hidden] parameter row (gamma with the zero-centered +1 folded in, bias,
+// beta) as fp32, read by 16-byte vector slot v. Staged rows live in shared
+// memory in a split layout: for 8-element vectors the first four elements of
+// every vector come first ([v * 4, v * 4 + 4)), the last four after them
+// ([hidden / 2 + v * 4, ...)), so consecutive lanes read consecutive 16-byte
+// words (no bank conflicts). Unstaged rows are read from global memory in
+// the I/O dtype.
+template <typename T>
+struct ParamRow {
+  const float* s;      // staged row, or null
+  const T* g;          // the row in global memory
+  int hidden;
+  bool plus_one;       // add 1 to values read from global (zero-centered gamma)
+
+  static __device__ __forceinline__ int staged_index(int i, int hidden) {
+    constexpr int VEC = Vec<T>::N;
+    if (VEC == 4) return i;
+    const int v = i / VEC, e = i % VEC;
+    return (e < 4 ? 0 : hidden / 2) + v * 4 + (e & 3);
+  }
+
+  template <bool kStaged>
+  __device__ __forceinline__ void load(int v, float* out) const {
+    constexpr int VEC = Vec<T>::N;
+    if (kStaged) {
+      const float4 a = *reinterpret_cast<const float4*>(s + v * 4);
+      out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+      if (VEC == 8) {
+        const float4 b = *reinterpret_cast<const float4*>(s + hidden / 2 + v * 4);
+        out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+      }
+    } else {
+      // A coherent load: the compiler reloads it after the "memory" barrier
+      // between the two passes instead of keeping it live in registers.
+      unpack<T>(*reinterpret_cast<const uint4*>(g + v * VEC), out);
+      if (plus_one) {
 #pragma unroll
-  for (int i = 0; i < VEC; i += 4) {
-    const float4 v = *reinterpret_cast<const float4*>(p + i);
-    f[i] = v.x;
-    f[i + 1] = v.y;
-    f[i + 2] = v.z;
-    f[i + 3] = v.w;
+        for (int e = 0; e < VEC; ++e) out[e] += 1.0f;
+      }
+    }
+  }
+};
+
+// Stage a parameter row into shared memory (split layout); all threads call
+// it. Values get +1 when `plus_one`.
+template <typename T>
+__device__ __forceinline__ void stage_param_row(const T* g, int hidden, bool plus_one, float* s) {
+  for (int i = threadIdx.x; i < hidden; i += blockDim.x) {
+    const float x = to_f(g[i]);
+    s[ParamRow<T>::staged_index(i, hidden)] = plus_one ? 1.0f + x : x;
   }
 }
 

@@ -115,9 +115,9 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
 // w = gamma (+1) as fp32 in shared memory. Both passes read shared memory, so
 // only the accumulators stay in registers across the reduction. kRms drops
 // the mean, c1 and the dbeta accumulators at compile time.
-template <typename T, int G, int N, bool kRms, typename Reduce2>
+template <typename T, int G, int N, bool kRms, bool kStaged, typename Reduce2>
 __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool row_ok, int t,
-                                             const T* dyrow, const T* xsrow, const float* w_s,
+                                             const T* dyrow, const T* xsrow, const ParamRow<T>& wr,
                                              float mean, float rstd, Reduce2 reduce2,
                                              float (&acc_g)[N][Vec<T>::N],
                                              float (&acc_b)[N][Vec<T>::N]) {
@@ -132,7 +132,7 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
       float d[VEC], xv[VEC], w[VEC];
       unpack<T>(ld_vec_smem(dyrow + v * VEC), d);
       unpack<T>(ld_vec_smem(xsrow + v * VEC), xv);
-      ld_f32_smem<VEC>(w_s + v * VEC, w);
+      wr.template load<kStaged>(v, w);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         const float xh = (kRms ? xv[e] : xv[e] - mean) * rstd;
@@ -159,7 +159,7 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
       float d[VEC], xv[VEC], w[VEC], o[VEC];
       unpack<T>(ld_vec_smem(dyrow + v * VEC), d);
       unpack<T>(ld_vec_smem(xsrow + v * VEC), xv);
-      ld_f32_smem<VEC>(w_s + v * VEC, w);
+      wr.template load<kStaged>(v, w);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         const float xm = kRms ? xv[e] : xv[e] - mean;
@@ -168,17 +168,6 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
       st_vec(dx + v * VEC, pack<T>(o));
     }
   }
-}
-
-// w = gamma, or 1 + gamma, as fp32 in shared memory; all threads call it.
-template <typename T>
-__device__ __forceinline__ void stage_weight(const BwdArgs& a, float* w_s) {
-  const T* gamma = static_cast<const T*>(a.gamma);
-  for (int j = threadIdx.x; j < a.hidden; j += blockDim.x) {
-    const float g = to_f(gamma[j]);
-    w_s[j] = a.zero_centered ? 1.0f + g : g;
-  }
-  __syncthreads();
 }
 
 template <typename T, int N>
@@ -338,7 +327,8 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
     s_abort = 0;
     s_taken = 0x7fffffffffffffffll;
   }
-  stage_weight<T>(a, w_s);
+  const ParamRow<T> wr = {w_s, static_cast<const T*>(a.gamma), H, a.zero_centered != 0};
+  stage_param_row<T>(wr.g, H, wr.plus_one, w_s);
   ring_init(ring);
 
   const int lane = threadIdx.x & 31;
@@ -368,7 +358,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
         const int64_t row = tile * c.tile_rows + local;
         const T* dys = reinterpret_cast<const T*>(slot) + (size_t)local * H;
         const T* xss = reinterpret_cast<const T*>(slot + in_bytes) + (size_t)local * H;
-        bwd_row_smem<T, LANES, N, kRms>(a, row, row < a.rows, l, dys, xss, w_s, mean, rstd,
+        bwd_row_smem<T, LANES, N, kRms, true>(a, row, row < a.rows, l, dys, xss, wr, mean, rstd,
                                         [](float2 v) { return group_sum2<LANES>(v); }, acc_g,
                                         acc_b);
       });
@@ -386,12 +376,11 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_cta_kernel(const Bwd
   const int H = a.hidden;
   const uint32_t in_bytes = (uint32_t)H * sizeof(T);   // one row per tile
   const Ring ring = make_ring(smem, 2 * in_bytes, c.stages);
-  float* w_s = reinterpret_cast<float*>(ring.empty + c.stages);
   if (threadIdx.x == 0) {
     s_abort = 0;
     s_taken = 0x7fffffffffffffffll;
   }
-  stage_weight<T>(a, w_s);
+  const ParamRow<T> wr = {nullptr, static_cast<const T*>(a.gamma), H, a.zero_centered != 0};
   ring_init(ring);
 
   float acc_g[N][Vec<T>::N], acc_b[N][Vec<T>::N];
@@ -415,8 +404,8 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_cta_kernel(const Bwd
         load_stats(row + gridDim.x, nm, nr);
         const T* dys = reinterpret_cast<const T*>(slot);
         const T* xss = reinterpret_cast<const T*>(slot + in_bytes);
-        bwd_row_smem<T, kBulkThreads, N, kRms>(
-            a, row, true, threadIdx.x, dys, xss, w_s, mean, rstd,
+        bwd_row_smem<T, kBulkThreads, N, kRms, false>(
+            a, row, true, threadIdx.x, dys, xss, wr, mean, rstd,
             [&](float2 v) { return cta_sum2<kBulkThreads>(v, red); }, acc_g, acc_b);
       });
   if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;

@@ -193,38 +193,38 @@ __global__ void __launch_bounds__(THREADS) fwd_cta_kernel(const FwdArgs a) {
 
 // ---- bulk-copy pipelined kernels ------------------------------------------
 
-// Per-column parameters as fp32 in shared memory, staged once per CTA:
-// w = gamma (+1 for zero-centered gamma), bias and beta (when present).
+// Per-column parameters of the forward: w = gamma (+1 for zero-centered
+// gamma), bias and beta (absent ones have a null global pointer). The lane
+// group kernels stage them in shared memory once per CTA; the CTA-per-row
+// kernels read them from global memory, leaving shared memory to the ring.
+template <typename T>
 struct FwdParams {
-  const float* w;
-  const float* bias;   // null without bias
-  const float* beta;   // null without beta
+  ParamRow<T> w, bias, beta;
 };
 
 template <typename T>
-__device__ __forceinline__ FwdParams stage_fwd_params(const FwdArgs& a, float* p_s) {
+__device__ __forceinline__ FwdParams<T> fwd_params(const FwdArgs& a, float* p_s) {
   const int H = a.hidden;
-  const T* gamma = static_cast<const T*>(a.gamma);
   const T* bias = static_cast<const T*>(a.bias);
   const T* beta = static_cast<const T*>(a.beta);
-  float* w_s = p_s;
-  float* bias_s = bias ? p_s + H : nullptr;
-  float* beta_s = beta ? p_s + (bias ? 2 : 1) * H : nullptr;
-  for (int j = threadIdx.x; j < H; j += blockDim.x) {
-    const float g = to_f(gamma[j]);
-    w_s[j] = a.zero_centered ? 1.0f + g : g;
-    if (bias_s) bias_s[j] = to_f(bias[j]);
-    if (beta_s) beta_s[j] = to_f(beta[j]);
+  FwdParams<T> p;
+  p.w = {p_s, static_cast<const T*>(a.gamma), H, a.zero_centered != 0};
+  p.bias = {p_s && bias ? p_s + H : nullptr, bias, H, false};
+  p.beta = {p_s && beta ? p_s + (bias ? 2 : 1) * H : nullptr, beta, H, false};
+  if (p_s) {
+    stage_param_row<T>(p.w.g, H, p.w.plus_one, p_s);
+    if (bias) stage_param_row<T>(bias, H, false, const_cast<float*>(p.bias.s));
+    if (beta) stage_param_row<T>(beta, H, false, const_cast<float*>(p.beta.s));
+    __syncthreads();
   }
-  __syncthreads();
-  return {w_s, bias_s, beta_s};
+  return p;
 }
 
 // The row body of the pipelined kernels: x and residual rows in shared
 // memory (ring slot), parameters as fp32 in shared memory.
-template <typename T, int G, int N, typename Reduce>
+template <typename T, int G, int N, bool kStaged, typename Reduce>
 __device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool row_ok, int t,
-                                             const T* xrow, const T* rrow, const FwdParams& p,
+                                             const T* xrow, const T* rrow, const FwdParams<T>& p,
                                              Reduce reduce, unsigned& amax_acc, bool write_stats) {
   constexpr int VEC = Vec<T>::N;
   const int H = a.hidden;
@@ -243,9 +243,9 @@ __device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool
     for (int e = 0; e < VEC; ++e) s[k][e] = 0.f;
     if (row_ok && v < V) {
       unpack<T>(ld_vec_smem(xrow + v * VEC), s[k]);
-      if (p.bias) {
+      if (p.bias.g) {
         float b[VEC];
-        ld_f32_smem<VEC>(p.bias + v * VEC, b);
+        p.bias.template load<kStaged>(v, b);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) s[k][e] += b[e];
       }
@@ -288,9 +288,9 @@ __device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool
     const int v = k * G + t;
     if (row_ok && v < V) {
       float w[VEC], o[VEC];
-      ld_f32_smem<VEC>(p.w + v * VEC, w);
-      if (p.beta) {
-        ld_f32_smem<VEC>(p.beta + v * VEC, o);
+      p.w.template load<kStaged>(v, w);
+      if (p.beta.g) {
+        p.beta.template load<kStaged>(v, o);
       } else {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) o[e] = 0.f;
@@ -305,7 +305,7 @@ __device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool
 }
 
 template <typename T, int LANES, int N>
-__global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_warp_kernel(const FwdArgs a,
+__global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 3 : 2) fwd_bulk_warp_kernel(const FwdArgs a,
                                                                          const BulkCfg c) {
   constexpr int RPW = 32 / LANES;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_warp_kernel(const Fw
     s_abort = 0;
     s_taken = 0x7fffffffffffffffll;
   }
-  const FwdParams p = stage_fwd_params<T>(a, reinterpret_cast<float*>(ring.empty + c.stages));
+  const FwdParams<T> p = fwd_params<T>(a, reinterpret_cast<float*>(ring.empty + c.stages));
   ring_init(ring);
 
   const int lane = threadIdx.x & 31;
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_warp_kernel(const Fw
         const T* xs = reinterpret_cast<const T*>(slot) + (size_t)local * H;
         const T* rs = a.residual ? reinterpret_cast<const T*>(slot + in_bytes) + (size_t)local * H
                                  : nullptr;
-        fwd_row_smem<T, LANES, N>(a, row, row < a.rows, l, xs, rs, p,
+        fwd_row_smem<T, LANES, N, true>(a, row, row < a.rows, l, xs, rs, p,
                                   [](float v) { return group_sum<LANES>(v); }, amax_acc, l == 0);
       });
   if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_cta_kernel(const Fwd
     s_abort = 0;
     s_taken = 0x7fffffffffffffffll;
   }
-  const FwdParams p = stage_fwd_params<T>(a, reinterpret_cast<float*>(ring.empty + c.stages));
+  const FwdParams<T> p = fwd_params<T>(a, nullptr);
   ring_init(ring);
 
   bool aborted = false;
@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_cta_kernel(const Fwd
       issued, [&](int64_t row, unsigned char* slot) {
         const T* xs = reinterpret_cast<const T*>(slot);
         const T* rs = a.residual ? reinterpret_cast<const T*>(slot + in_bytes) : nullptr;
-        fwd_row_smem<T, kBulkThreads, N>(a, row, true, threadIdx.x, xs, rs, p,
+        fwd_row_smem<T, kBulkThreads, N, false>(a, row, true, threadIdx.x, xs, rs, p,
                                          [&](float v) { return cta_sum<kBulkThreads>(v, red); },
                                          amax_acc, threadIdx.x == 0);
       });

@@ -65,18 +65,20 @@ NF_TABLES(bf16, bf16)
 NF_TABLES(f16, f16)
 #undef NF_TABLES
 
-// Ring sizing: the slots of one CTA should fill about kRingTarget bytes so
-// two pipelined CTAs fit on an SM; never fewer than 2 nor more than 8 slots.
+// Ring sizing: the slots of one CTA should fill about `target` bytes (so two
+// or three pipelined CTAs fit on an SM); never fewer than 2 nor more than 8
+// slots. The lane-group forward (<= 74 registers) runs three CTAs per SM.
 constexpr size_t kRingTarget = 104 * 1024;
+constexpr size_t kRingTargetFwdGroup = 68 * 1024;
 constexpr size_t kMaxDynSmem = 200 * 1024;
 
 // Fill in a pipelined plan; false when the ring does not fit. `extra`:
 // shared bytes after the ring's barriers (the backward's fp32 weight row).
 inline bool fill_bulk(Plan* p, const Choice& c, int64_t rows, int hidden, size_t esize, int n_in,
-                      size_t extra) {
+                      size_t extra, size_t target) {
   const int tile_rows = c.kind == 0 ? kConsumerWarps * (32 / c.group) : 1;
   const size_t slot = (size_t)n_in * tile_rows * hidden * esize;
-  const size_t room = kRingTarget > extra ? kRingTarget - extra : 0;
+  const size_t room = target > extra ? target - extra : 0;
   int stages = (int)std::min<size_t>(8, std::max<size_t>(2, room / slot));
   size_t smem = (size_t)stages * slot + 2 * stages * sizeof(uint64_t) + extra;
   if (smem > kMaxDynSmem) return false;
@@ -143,8 +145,11 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, in
   if (want_bulk) {
     Choice b = c;
     if (c.kind == 1) b.n = bulk_cta_n(hidden, Vec<T>::N);
-    const size_t extra = (size_t)n_params * hidden * sizeof(float);
-    if (fill_bulk(p, b, rows, hidden, sizeof(T), n_in, extra)) {
+    // Lane-group kernels stage the parameter rows in shared memory as fp32;
+    // CTA-per-row kernels read them from global memory.
+    const size_t extra = b.kind == 0 ? (size_t)n_params * hidden * sizeof(float) : 0;
+    const size_t target = (!bwd && b.kind == 0 && b.n <= 4) ? kRingTargetFwdGroup : kRingTarget;
+    if (fill_bulk(p, b, rows, hidden, sizeof(T), n_in, extra, target)) {
       p->fn = bwd ? Tables<T>::bwd_bulk(b.kind, b.group, b.n, rms)
                   : Tables<T>::fwd_bulk(b.kind, b.group, b.n);
       return size_grid(p, p->cfg.num_tiles);
