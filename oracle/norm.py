@@ -164,7 +164,9 @@ def norm_bwd(dy, x_sum, gamma, mean, rstd, mode: str,
       input (and so, through the identity add, to x and to residual);
       ``dx_exact`` unrounded;
     * ``dgamma``: sum over rows of dy * xhat (float64);
-    * ``dbeta``: sum over rows of dy (float64; None for RMSNorm).
+    * ``dbeta``: sum over rows of dy (float64; None for RMSNorm);
+    * ``dbias``: sum over rows of dx_exact, the gradient of the bias through
+      the forward's add (float64).
 
     With xhat = (x_sum - mean) * rstd (RMSNorm: x_sum * rstd), g = dy * w,
     c1 = mean_j g, c2 = mean_j g * xhat, the inner (per-row) reduction is
@@ -195,5 +197,9 @@ def norm_bwd(dy, x_sum, gamma, mean, rstd, mode: str,
     # B2/B3: outer reductions over the rows.
     dgamma = (dy * xhat).sum(axis=0)
     dbeta = dy.sum(axis=0) if mode == LAYERNORM else None
+    # The forward adds bias to every row, so its gradient is the column sum
+    # of the gradient of the normalization input (Fuser 1660's add feeding
+    # the norm whose backward PR 165370 fuses).
+    dbias = dx_exact.sum(axis=0)
     return {"dx": dx, "dx_exact": dx_exact, "dgamma": dgamma, "dbeta": dbeta,
-            "xhat": xhat}
+            "dbias": dbias, "xhat": xhat}

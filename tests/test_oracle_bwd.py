@@ -60,7 +60,7 @@ def test_central_finite_differences(mode, zc):
     bwd = norm_bwd(c["dy"], fwd["sum"], c["gamma"], fwd["mean_exact"], fwd["rstd_exact"],
                    mode, zc, "f64")
     grads = {"x": bwd["dx_exact"], "residual": bwd["dx_exact"],
-             "bias": bwd["dx_exact"].sum(axis=0), "gamma": bwd["dgamma"]}
+             "bias": bwd["dbias"], "gamma": bwd["dgamma"]}
     if mode == LAYERNORM:
         grads["beta"] = bwd["dbeta"]
     for name, want in grads.items():
@@ -94,6 +94,7 @@ def test_matches_torch_autograd_fp64(mode, zc):
     (y * torch.from_numpy(c["dy"])).sum().backward()
     np.testing.assert_allclose(bwd["dx_exact"], t["x"].grad.numpy(), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(bwd["dgamma"], t["gamma"].grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(bwd["dbias"], t["bias"].grad.numpy(), rtol=1e-10, atol=1e-12)
     if mode == LAYERNORM:
         np.testing.assert_allclose(bwd["dbeta"], t["beta"].grad.numpy(), rtol=1e-12, atol=1e-12)
 
