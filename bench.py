@@ -218,6 +218,24 @@ class Step:
         return [(k, t) for k, t in out if t is not None]
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The max of a per-rank timing over all ranks (all_reduce MAX); the
+    value itself when running alone. Works with NCCL (CUDA tensor) and gloo
+    (CPU tensor)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(rows_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job rows/s of `world` replicas, each stepping `rows_per_rank`
+    rows in `ms_per_step` (the slowest rank's time)."""
+    return world * rows_per_rank / (ms_per_step * 1e-3)
+
+
 def nbytes(t) -> int:
     return t.numel() * t.element_size()
 
@@ -332,11 +350,7 @@ def run_ours(args, w, rank, world, local_rank):
     torch.cuda.synchronize(device)
     t_host1 = time.time()
     barrier()
-    elapsed = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([elapsed], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(start.elapsed_time(end), world, device)
     clocks = None
     if sampler is not None:
         time.sleep(0.25)
@@ -349,7 +363,9 @@ def run_ours(args, w, rank, world, local_rank):
     # every output read back, each step
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(step, stream, device, min(args.e2e_steps, max(K, 1)))
+        del step
+        torch.cuda.empty_cache()
+        e2e = run_e2e(nf, w, inp_host, device, min(args.e2e_steps, max(K, 1)))
 
     if rank != 0:
         return
@@ -374,7 +390,7 @@ def run_ours(args, w, rank, world, local_rank):
                          f"{secs:.1f} s on 1 host thread"}
     ms_step = elapsed / K
     line = {
-        "metric": METRIC, "value": world * w.rows / (ms_step * 1e-3), "unit": "rows/s",
+        "metric": METRIC, "value": replica_throughput(w.rows, world, ms_step), "unit": "rows/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": config_of(w, world), "roofline": roofline,
@@ -385,34 +401,57 @@ def run_ours(args, w, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-def run_e2e(step, stream, device, steps):
-    h2d = step.h2d_tensors()
-    d2h = step.d2h_tensors()
-    host_in = {k: t.detach().to("cpu").pin_memory() for k, t in h2d}
-    host_out = {k: torch.empty(t.shape, dtype=t.dtype).pin_memory() for k, t in d2h}
+def run_e2e(nf, w, inp_host, device, steps):
+    """The same fwd + bwd step end to end from pinned host memory: every step
+    copies its inputs host -> device, runs ln_fwd and ln_bwd, and copies every
+    output device -> host. Two buffer sets alternate so step i + 1's upload
+    (copy stream) overlaps step i's compute (compute stream) and download
+    (a third stream); each direction has its own copy engine."""
+    sets = [Step(nf, w, inp_host, device) for _ in range(2)]
+    h2d = [s.h2d_tensors() for s in sets]
+    d2h = [s.d2h_tensors() for s in sets]
+    host_in = {k: t.detach().to("cpu").pin_memory() for k, t in h2d[0]}
+    host_out = [{k: torch.empty(t.shape, dtype=t.dtype).pin_memory() for k, t in d} for d in d2h]
+    up, comp, down = (torch.cuda.Stream(device) for _ in range(3))
+    uploaded = [torch.cuda.Event() for _ in sets]
+    computed = [torch.cuda.Event() for _ in sets]
+    downloaded = [torch.cuda.Event() for _ in sets]
 
-    def one():
-        for k, t in h2d:
-            t.copy_(host_in[k], non_blocking=True)
-        step.fwd(stream)
-        step.bwd(stream)
-        for k, t in d2h:
-            host_out[k].copy_(t, non_blocking=True)
+    def one(i):
+        b = i % 2
+        if i >= 2:                      # set b is free once its last use is done
+            up.wait_event(computed[b])
+            up.wait_event(downloaded[b])
+        with torch.cuda.stream(up):
+            for k, t in h2d[b]:
+                t.copy_(host_in[k], non_blocking=True)
+            uploaded[b].record(up)
+        comp.wait_event(uploaded[b])
+        sets[b].fwd(comp)
+        sets[b].bwd(comp)
+        computed[b].record(comp)
+        down.wait_event(computed[b])
+        with torch.cuda.stream(down):
+            for k, t in d2h[b]:
+                host_out[b][k].copy_(t, non_blocking=True)
+            downloaded[b].record(down)
 
-    for _ in range(2):
-        one()
+    for i in range(2):
+        one(i)
     torch.cuda.synchronize(device)
     a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        one()
-    b.record(stream)
+    z = torch.cuda.Event(enable_timing=True)
+    a.record(up)
+    for i in range(steps):
+        one(i)
+    down.wait_event(computed[(steps - 1) % 2])
+    z.record(down)
     torch.cuda.synchronize(device)
-    ms = a.elapsed_time(b) / steps
-    return {"value": step.w.rows / (ms * 1e-3), "unit": "rows/s", "ms_per_step": ms,
-            "steps": steps, "h2d_bytes_per_step": sum(nbytes(t) for _, t in h2d),
-            "d2h_bytes_per_step": sum(nbytes(t) for _, t in d2h)}
+    ms = a.elapsed_time(z) / steps
+    return {"value": w.rows / (ms * 1e-3), "unit": "rows/s", "ms_per_step": ms,
+            "steps": steps, "h2d_bytes_per_step": sum(nbytes(t) for _, t in h2d[0]),
+            "d2h_bytes_per_step": sum(nbytes(t) for _, t in d2h[0]),
+            "pipeline": "2 buffer sets; upload, compute and download on 3 streams"}
 
 
 def main():
