@@ -150,10 +150,33 @@ ln_status ln_bwd(const void* dy, const void* x_sum, const void* gamma,
                  size_t workspace_bytes);
 
 /*
- * Bytes of workspace ln_bwd needs for this shape on the current device (the
- * maximum over the vectorised and the scalar kernel, so it holds whatever
- * the pointers' alignment). Queries device attributes; returns LN_ERR_CUDA
- * when no device is usable.
+ * ln_bwd_ex: ln_bwd plus the gradient of the forward's bias.
+ *
+ * The forward adds `bias` to every row before the norm (NVIDIA/Fuser issue
+ * 1660), so dbias = sum over rows of dx, the gradient of the norm's input;
+ * the gradients of x and of residual are dx itself (identity add). dbias is
+ * a third column reduction over the rows, accumulated in the same persistent
+ * kernel from the fp32 dx (before its rounding to dtype) and added up by the
+ * same fixed-order finalize (pytorch/pytorch PR 165370's partial
+ * accumulation of the outer reductions).
+ *
+ * dbias     [hidden] fp32, NULL = not computed (then identical to ln_bwd).
+ * Every other argument, the workspace rule and the errors are those of
+ * ln_bwd; ln_bwd_workspace_bytes() covers both entry points.
+ */
+ln_status ln_bwd_ex(const void* dy, const void* x_sum, const void* gamma,
+                    const float* mean, const float* rstd, void* dx,
+                    float* dgamma, float* dbeta, float* dbias,
+                    cudaStream_t stream, int64_t rows, int64_t hidden,
+                    ln_dtype dtype, ln_mode mode, int zero_centered_gamma,
+                    void* workspace, size_t workspace_bytes);
+
+/*
+ * Bytes of workspace ln_bwd / ln_bwd_ex need for this shape on the current
+ * device (the maximum over the vectorised and the scalar kernel and over
+ * the layouts with and without dbias, so it holds whatever the pointers'
+ * alignment). Queries device attributes; returns LN_ERR_CUDA when no device
+ * is usable.
  */
 ln_status ln_bwd_workspace_bytes(int64_t rows, int64_t hidden, ln_dtype dtype,
                                  ln_mode mode, size_t* bytes);

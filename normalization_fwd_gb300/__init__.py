@@ -22,7 +22,7 @@ from .build import LIB_PATH, build as build_library
 
 __all__ = [
     "LN_F32", "LN_BF16", "LN_F16", "LN_LAYERNORM", "LN_RMSNORM", "NormError",
-    "load_library", "build_library", "ln_fwd", "ln_bwd", "ln_bwd_workspace_bytes",
+    "load_library", "build_library", "ln_fwd", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes",
     "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc",
     "exported_symbols",
     "fused_norm_fwd", "fused_norm_bwd", "Workspace",
@@ -69,6 +69,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.ln_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, ci, ci,
                                vp, sz]
         lib.ln_bwd.restype = ci
+        lib.ln_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, ci, ci,
+                                  vp, sz]
+        lib.ln_bwd_ex.restype = ci
         lib.ln_bwd_workspace_bytes.argtypes = [i64, i64, ci, ci, ctypes.POINTER(sz)]
         lib.ln_bwd_workspace_bytes.restype = ci
         lib.ln_status_string.argtypes = [ci]
@@ -85,7 +88,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
 
 def exported_symbols() -> list[str]:
     """Names of the C entry points this binding wraps."""
-    return ["ln_fwd", "ln_bwd", "ln_bwd_workspace_bytes", "ln_status_string",
+    return ["ln_fwd", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes", "ln_status_string",
             "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc"]
 
 
@@ -215,6 +218,24 @@ def ln_bwd_noalloc(dy, x_sum, gamma, mean, rstd, dx, dgamma, dbeta, stream=None,
         raise NormError(st, "ln_bwd_noalloc")
 
 
+def ln_bwd_ex(dy, x_sum, gamma, mean, rstd, dx, dgamma, dbeta, dbias, stream=None, *,
+              mode="layernorm", zero_centered_gamma=False, workspace=None) -> None:
+    """``ln_bwd`` that also writes ``dbias`` (fp32 [hidden], the column sum of
+    dx: the gradient of the forward's bias); dbias may be None."""
+    lib = load_library()
+    rows, hidden = _shape(dy)
+    if workspace is None and rows > 0:
+        need = ln_bwd_workspace_bytes(rows, hidden, dy.dtype, mode)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dy.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.ln_bwd_ex(_ptr(dy), _ptr(x_sum), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),
+                       _ptr(dgamma), _ptr(dbeta), _ptr(dbias), _stream(stream), rows, hidden,
+                       _dtype(dy), _mode(mode), int(bool(zero_centered_gamma)),
+                       _ptr(workspace), ws_bytes)
+    if st:
+        raise NormError(st, "ln_bwd_ex")
+
+
 class Workspace:
     """A reusable backward workspace, grown on demand (allocated through torch)."""
 
@@ -252,15 +273,22 @@ def fused_norm_fwd(x, gamma, beta=None, *, bias=None, residual=None, eps=1e-5,
 
 
 def fused_norm_bwd(dy, x_sum, gamma, mean, rstd, *, mode="layernorm", zero_centered_gamma=False,
-                   need_dbeta=True, workspace: Workspace | None = None, stream=None):
-    """Allocate the outputs with torch and run ``ln_bwd``; returns dx, dgamma, dbeta."""
+                   need_dbeta=True, need_dbias=False, workspace: Workspace | None = None,
+                   stream=None):
+    """Allocate the outputs with torch and run ``ln_bwd`` (``ln_bwd_ex`` when
+    ``need_dbias``); returns dx, dgamma, dbeta, dbias."""
     rows, hidden = _shape(dy)
     rms = _mode(mode) == LN_RMSNORM
     dx = torch.empty_like(dy)
     dgamma = torch.empty(hidden, dtype=torch.float32, device=dy.device)
     dbeta = (torch.empty(hidden, dtype=torch.float32, device=dy.device)
              if (need_dbeta and not rms) else None)
+    dbias = torch.empty(hidden, dtype=torch.float32, device=dy.device) if need_dbias else None
     ws = workspace.get(rows, hidden, dy.dtype, mode) if workspace is not None else None
-    ln_bwd(dy, x_sum, gamma, mean, rstd, dx, dgamma, dbeta, stream, mode=mode,
-           zero_centered_gamma=zero_centered_gamma, workspace=ws)
-    return {"dx": dx, "dgamma": dgamma, "dbeta": dbeta}
+    if need_dbias:
+        ln_bwd_ex(dy, x_sum, gamma, mean, rstd, dx, dgamma, dbeta, dbias, stream, mode=mode,
+                  zero_centered_gamma=zero_centered_gamma, workspace=ws)
+    else:
+        ln_bwd(dy, x_sum, gamma, mean, rstd, dx, dgamma, dbeta, stream, mode=mode,
+               zero_centered_gamma=zero_centered_gamma, workspace=ws)
+    return {"dx": dx, "dgamma": dgamma, "dbeta": dbeta, "dbias": dbias}

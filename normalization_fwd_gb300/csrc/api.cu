@@ -152,9 +152,14 @@ ln_status ln_device_error(cudaStream_t stream, unsigned* flags) {
   if (flags == nullptr) return LN_ERR_NULL;
   *flags = 0;
   cudaError_t (*readers[])(cudaStream_t, unsigned*) = {
-      take_error_fwd_bulk_f32,    take_error_fwd_bulk_bf16,    take_error_fwd_bulk_f16,
-      take_error_bwd_bulk_ln_f32, take_error_bwd_bulk_ln_bf16, take_error_bwd_bulk_ln_f16,
-      take_error_bwd_bulk_rms_f32, take_error_bwd_bulk_rms_bf16, take_error_bwd_bulk_rms_f16};
+      take_error_fwd_bulk_f32,          take_error_fwd_bulk_bf16,
+      take_error_fwd_bulk_f16,          take_error_bwd_bulk_ln_f32,
+      take_error_bwd_bulk_ln_bf16,      take_error_bwd_bulk_ln_f16,
+      take_error_bwd_bulk_rms_f32,      take_error_bwd_bulk_rms_bf16,
+      take_error_bwd_bulk_rms_f16,      take_error_bwd_bulk_ln_dbias_f32,
+      take_error_bwd_bulk_ln_dbias_bf16, take_error_bwd_bulk_ln_dbias_f16,
+      take_error_bwd_bulk_rms_dbias_f32, take_error_bwd_bulk_rms_dbias_bf16,
+      take_error_bwd_bulk_rms_dbias_f16};
   for (auto r : readers) {
     cudaError_t e = r(stream, flags);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -230,11 +235,11 @@ ln_status ln_fwd(const void* x, const void* bias, const void* residual, const vo
   return LN_OK;
 }
 
-static cudaError_t bwd_plan_any(ln_dtype dtype, int64_t rows, int hidden, bool rms, bool vec,
-                                Plan* p) {
+static cudaError_t bwd_plan_any(ln_dtype dtype, int64_t rows, int hidden, bool rms, bool dbias,
+                                bool vec, Plan* p) {
   return by_dtype(dtype, [&](auto t) {
     using T = decltype(t);
-    return bwd_plan<T>(rows, hidden, rms, vec, p);
+    return bwd_plan<T>(rows, hidden, rms, dbias, vec, p);
   });
 }
 
@@ -255,8 +260,9 @@ ln_status ln_bwd_workspace_bytes(int64_t rows, int64_t hidden, ln_dtype dtype, l
     const bool vec = v == 1;
     if (vec && !vec_possible) continue;
     if (!vec && hidden > max_hidden(dtype, false)) continue;
+    // Sized for the largest layout (with dbias), so it serves ln_bwd_ex too.
     Plan p;
-    cudaError_t e = bwd_plan_any(dtype, rows, (int)hidden, rms, vec, &p);
+    cudaError_t e = bwd_plan_any(dtype, rows, (int)hidden, rms, true, vec, &p);
     if (e != cudaSuccess) return cuda_fail(e);
     const size_t b = (size_t)p.grid * (size_t)p.ws_cols * sizeof(float);
     if (b > need) need = b;
@@ -269,6 +275,15 @@ ln_status ln_bwd(const void* dy, const void* x_sum, const void* gamma, const flo
                  const float* rstd, void* dx, float* dgamma, float* dbeta, cudaStream_t stream,
                  int64_t rows, int64_t hidden, ln_dtype dtype, ln_mode mode,
                  int zero_centered_gamma, void* workspace, size_t workspace_bytes) {
+  return ln_bwd_ex(dy, x_sum, gamma, mean, rstd, dx, dgamma, dbeta, nullptr, stream, rows,
+                   hidden, dtype, mode, zero_centered_gamma, workspace, workspace_bytes);
+}
+
+ln_status ln_bwd_ex(const void* dy, const void* x_sum, const void* gamma, const float* mean,
+                    const float* rstd, void* dx, float* dgamma, float* dbeta, float* dbias,
+                    cudaStream_t stream, int64_t rows, int64_t hidden, ln_dtype dtype,
+                    ln_mode mode, int zero_centered_gamma, void* workspace,
+                    size_t workspace_bytes) {
   if (dtype != LN_F32 && dtype != LN_BF16 && dtype != LN_F16) return LN_ERR_UNSUPPORTED;
   if (mode != LN_LAYERNORM && mode != LN_RMSNORM) return LN_ERR_UNSUPPORTED;
   if (rows < 0 || hidden < 1) return LN_ERR_SHAPE;
@@ -285,7 +300,8 @@ ln_status ln_bwd(const void* dy, const void* x_sum, const void* gamma, const flo
   const void* tensors[] = {dy, x_sum, gamma, dx};
   for (const void* p : tensors)
     if (!aligned(p, es)) return LN_ERR_ALIGN;
-  if (!aligned(mean, 4) || !aligned(rstd, 4) || !aligned(dgamma, 4) || !aligned(dbeta, 4))
+  if (!aligned(mean, 4) || !aligned(rstd, 4) || !aligned(dgamma, 4) || !aligned(dbeta, 4) ||
+      !aligned(dbias, 4))
     return LN_ERR_ALIGN;
   bool vec = (hidden * (int64_t)es) % 16 == 0;
   for (const void* p : tensors)
@@ -296,17 +312,19 @@ ln_status ln_bwd(const void* dy, const void* x_sum, const void* gamma, const flo
   }
   const size_t mat = (size_t)rows * (size_t)hidden * es;
   const size_t hb = (size_t)hidden * es, h4 = (size_t)hidden * 4, r4 = (size_t)rows * 4;
-  const Range outs[] = {{dx, mat}, {dgamma, h4}, {dbeta, h4}, {workspace, workspace_bytes}};
+  const Range outs[] = {{dx, mat}, {dgamma, h4}, {dbeta, h4}, {dbias, h4},
+                        {workspace, workspace_bytes}};
   const Range ins[] = {{dy, mat}, {x_sum, mat}, {gamma, hb}, {mean, r4}, {rstd, r4}};
-  if (any_overlap(outs, 4, ins, 5)) return LN_ERR_INVALID;
+  if (any_overlap(outs, 5, ins, 5)) return LN_ERR_INVALID;
 
   if (rows == 0) {
     cudaError_t e = cudaMemsetAsync(dgamma, 0, h4, stream);
     if (e == cudaSuccess && dbeta) e = cudaMemsetAsync(dbeta, 0, h4, stream);
+    if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, h4, stream);
     return e == cudaSuccess ? LN_OK : cuda_fail(e);
   }
   Plan p;
-  cudaError_t e = bwd_plan_any(dtype, rows, (int)hidden, rms, vec, &p);
+  cudaError_t e = bwd_plan_any(dtype, rows, (int)hidden, rms, dbias != nullptr, vec, &p);
   if (e != cudaSuccess) return cuda_fail(e);
   const size_t need = (size_t)p.grid * (size_t)p.ws_cols * sizeof(float);
   if (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < need)
@@ -325,9 +343,11 @@ ln_status ln_bwd(const void* dy, const void* x_sum, const void* gamma, const flo
   a.inv_hidden = 1.0f / (float)hidden;
   a.rms = rms ? 1 : 0;
   a.zero_centered = zero_centered_gamma ? 1 : 0;
+  a.has_dbias = dbias != nullptr ? 1 : 0;
+  a.ws_cols = p.ws_cols;
   e = by_dtype(dtype, [&](auto t) {
     using T = decltype(t);
-    return bwd_launch<T>(a, p, dgamma, dbeta, stream);
+    return bwd_launch<T>(a, p, dgamma, dbeta, dbias, stream);
   });
   if (e != cudaSuccess) return cuda_fail(e);
   return LN_OK;

@@ -4,13 +4,13 @@
 // forever.
 //
 // A pipelined CTA streams tiles of whole rows into a ring of `stages`
-// shared-memory slots. Thread 0 is the producer: at the top of iteration
-// `it` it issues the copies of the CTA's tile it + stages - 1 into the slot
-// that tile it - 1 just freed; all kConsumerWarps warps (thread 0's included)
-// consume tile `it`. Each slot has a `full` barrier (one arrival plus the
-// transaction bytes of its copies) and an `empty` barrier (one arrival per
-// warp). Round r of slot s waits `full` with parity r & 1 and `empty` with
-// parity (r & 1) ^ 1, so the first round finds every slot free.
+// shared-memory slots, every slot in flight at once. Thread 0 fills all
+// slots first; after that the warp that releases a slot last (a per-slot
+// arrival counter tells it) refills it at once with the CTA's tile
+// it + stages, so no thread ever waits for a slot to drain. Each slot has a
+// `full` barrier (one arrival plus the transaction bytes of its copies) and
+// an `empty` barrier (one arrival per warp). Round r of slot s waits `full`
+// with parity r & 1 and `empty` with parity (r & 1) ^ 1.
 #pragma once
 
 #include "common.cuh"
@@ -91,10 +91,23 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// 16-byte load from shared memory. A plain load so the compiler can schedule
-// it; the "memory" clobber of the barrier waits orders it after the copy.
+// 16-byte loads from shared memory, always as ld.shared (a generic load of
+// a shared address would take the slower L1TEX path). Volatile, so they stay
+// after the barrier waits (volatile asm keeps its order) and are never merged
+// with an earlier load of the same address.
 __device__ __forceinline__ uint4 ld_vec_smem(const void* p) {
-  return *reinterpret_cast<const uint4*>(p);
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+__device__ __forceinline__ float4 ld_f4_smem(const float* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
 }
 
 // A [hidden] parameter row (gamma with the zero-centered +1 folded in, bias,
@@ -118,14 +131,36 @@ struct ParamRow {
     return (e < 4 ? 0 : hidden / 2) + v * 4 + (e & 3);
   }
 
+  // The same values as fp32 pairs.
+  template <bool kStaged>
+  __device__ __forceinline__ void load2(int v, float2* out) const {
+    constexpr int VEC = Vec<T>::N;
+    if (kStaged) {
+      const float4 a = ld_f4_smem(s + v * 4);
+      out[0] = make_float2(a.x, a.y);
+      out[1] = make_float2(a.z, a.w);
+      if (VEC == 8) {
+        const float4 b = ld_f4_smem(s + hidden / 2 + v * 4);
+        out[2] = make_float2(b.x, b.y);
+        out[3] = make_float2(b.z, b.w);
+      }
+    } else {
+      unpack2<T>(*reinterpret_cast<const uint4*>(g + v * VEC), out);
+      if (plus_one) {
+#pragma unroll
+        for (int i = 0; i < VEC / 2; ++i) out[i] = add2(out[i], splat2(1.0f));
+      }
+    }
+  }
+
   template <bool kStaged>
   __device__ __forceinline__ void load(int v, float* out) const {
     constexpr int VEC = Vec<T>::N;
     if (kStaged) {
-      const float4 a = *reinterpret_cast<const float4*>(s + v * 4);
+      const float4 a = ld_f4_smem(s + v * 4);
       out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
       if (VEC == 8) {
-        const float4 b = *reinterpret_cast<const float4*>(s + hidden / 2 + v * 4);
+        const float4 b = ld_f4_smem(s + hidden / 2 + v * 4);
         out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
       }
     } else {
@@ -150,16 +185,26 @@ __device__ __forceinline__ void stage_param_row(const T* g, int hidden, bool plu
   }
 }
 
-// Ring layout in dynamic shared memory: `stages` slots of `slot_bytes`, then
-// the full and empty barriers.
+// Ring layout in dynamic shared memory: `stages` slots of `slot_bytes`, the
+// full and empty barriers, the per-slot release counters, then (16-byte
+// aligned) whatever the kernel keeps after the ring.
 struct Ring {
   unsigned char* base;
   uint32_t slot_bytes;
   int stages;
   uint64_t* full;
   uint64_t* empty;
+  unsigned* released;     // warps that released the slot in its current round
+  long long* issued;      // tiles issued so far (for the drain after an abort)
+  unsigned char* after;   // first byte after the ring
   __device__ unsigned char* slot(int s) const { return base + (size_t)s * slot_bytes; }
 };
+
+// Bytes of the ring's bookkeeping after its slots (host and device agree).
+__host__ __device__ constexpr size_t ring_aux_bytes(int stages) {
+  return ((size_t)stages * (2 * sizeof(uint64_t) + sizeof(unsigned)) + sizeof(long long) + 15) &
+         ~(size_t)15;
+}
 
 __device__ __forceinline__ Ring make_ring(unsigned char* smem, uint32_t slot_bytes, int stages) {
   Ring r;
@@ -168,6 +213,9 @@ __device__ __forceinline__ Ring make_ring(unsigned char* smem, uint32_t slot_byt
   r.stages = stages;
   r.full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * slot_bytes);
   r.empty = r.full + stages;
+  r.issued = reinterpret_cast<long long*>(r.empty + stages);
+  r.released = reinterpret_cast<unsigned*>(r.issued + 1);
+  r.after = smem + (size_t)stages * slot_bytes + ring_aux_bytes(stages);
   return r;
 }
 
@@ -177,7 +225,9 @@ __device__ __forceinline__ void ring_init(const Ring& r) {
     for (int s = 0; s < r.stages; ++s) {
       mbar_init(&r.full[s], 1);
       mbar_init(&r.empty[s], kConsumerWarps);
+      r.released[s] = 0;
     }
+    *r.issued = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -217,35 +267,27 @@ __device__ __forceinline__ bool issue_tile(const Ring& ring, const BulkCfg& c, i
 
 // The pipeline loop: `body(tile, slot)` for each of the CTA's tiles in order.
 // With kUniform (bodies with CTA-wide barriers) all threads agree on an
-// abort before anyone leaves the loop. Returns the tiles consumed; `issued`
-// (thread 0) the tiles issued; `aborted` is set when a wait timed out.
+// abort before anyone leaves the loop. Returns the tiles consumed; `aborted`
+// is set when a wait timed out.
 template <bool kUniform, typename T, typename Body>
 __device__ __forceinline__ int64_t run_pipeline(const Ring& ring, const BulkCfg& c, int64_t rows,
                                                 int hidden, const T* in0, const T* in1,
-                                                bool& aborted, int64_t& issued, Body body) {
+                                                bool& aborted, Body body) {
   const int S = ring.stages;
   const int64_t n_local = (c.num_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
   if (threadIdx.x == 0) {
-    for (int64_t j = 0; j < S - 1 && j < n_local; ++j) {
+    int64_t j = 0;
+    for (; j < S && j < n_local; ++j) {
       if (!issue_tile<T>(ring, c, j, rows, hidden, in0, in1)) {
         aborted = true;
         break;
       }
-      issued = j + 1;
     }
+    *ring.issued = j;
   }
+  __syncthreads();
   int64_t it = 0;
   for (; it < n_local; ++it) {
-    if (threadIdx.x == 0 && !aborted) {
-      const int64_t j = it + S - 1;
-      if (j < n_local) {
-        if (issue_tile<T>(ring, c, j, rows, hidden, in0, in1)) {
-          issued = j + 1;
-        } else {
-          aborted = true;
-        }
-      }
-    }
     const int s = (int)(it % S);
     int failed = !mbar_wait(&ring.full[s], (uint32_t)((it / S) & 1));
     if (kUniform) failed = __syncthreads_or(failed);
@@ -255,7 +297,21 @@ __device__ __forceinline__ int64_t run_pipeline(const Ring& ring, const BulkCfg&
     }
     body(blockIdx.x + it * gridDim.x, ring.slot(s));
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&ring.empty[s]);
+    if ((threadIdx.x & 31) == 0) {
+      mbar_arrive(&ring.empty[s]);
+      if (atomicAdd(&ring.released[s], 1u) == kConsumerWarps - 1) {
+        // This warp released the slot last: reset its counter and refill it.
+        atomicExch(&ring.released[s], 0u);
+        const int64_t j = it + S;
+        if (j < n_local) {
+          if (issue_tile<T>(ring, c, j, rows, hidden, in0, in1)) {
+            atomicMax(ring.issued, (long long)(j + 1));
+          } else {
+            aborted = true;
+          }
+        }
+      }
+    }
   }
   return it;
 }
@@ -263,9 +319,8 @@ __device__ __forceinline__ int64_t run_pipeline(const Ring& ring, const BulkCfg&
 // End of a pipelined kernel, all threads: record an abort in the error word,
 // and on abort let thread 0 drain the copies still in flight. Returns true
 // when the kernel aborted (the caller then skips its epilogue).
-__device__ __forceinline__ bool pipeline_finish(const Ring& ring, bool aborted, int64_t issued,
-                                                int64_t taken, int* s_abort,
-                                                long long* s_taken) {
+__device__ __forceinline__ bool pipeline_finish(const Ring& ring, bool aborted, int64_t taken,
+                                                int* s_abort, long long* s_taken) {
   if (aborted) {
     atomicOr(&g_tu_error, kErrWaitTimeout);
     atomicExch(s_abort, 1);
@@ -273,7 +328,7 @@ __device__ __forceinline__ bool pipeline_finish(const Ring& ring, bool aborted, 
   if ((threadIdx.x & 31) == 0) atomicMin(s_taken, (long long)taken);
   __syncthreads();
   if (*s_abort) {
-    if (threadIdx.x == 0) ring_drain(ring, *s_taken, issued);
+    if (threadIdx.x == 0) ring_drain(ring, *s_taken, *ring.issued);
     return true;
   }
   return false;

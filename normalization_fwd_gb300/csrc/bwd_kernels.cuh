@@ -112,43 +112,49 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
 }
 
 // The row body of the pipelined kernels: dy and x_sum rows in shared memory,
-// w = gamma (+1) as fp32 in shared memory. Both passes read shared memory, so
-// only the accumulators stay in registers across the reduction. kRms drops
-// the mean, c1 and the dbeta accumulators at compile time.
-template <typename T, int G, int N, bool kRms, bool kStaged, typename Reduce2>
+// w = gamma (+1) staged in shared memory (kStaged) or read from global. Both
+// passes read shared memory, so only the accumulators stay in registers
+// across the reduction. Values are fp32 pairs (packed fp32 math). kRms drops
+// the mean, c1 and the dbeta accumulators at compile time; kBias adds the
+// row's fp32 dx into the dbias accumulators.
+template <typename T, int G, int N, bool kRms, bool kBias, bool kStaged, typename Reduce2>
 __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool row_ok, int t,
                                              const T* dyrow, const T* xsrow, const ParamRow<T>& wr,
                                              float mean, float rstd, Reduce2 reduce2,
-                                             float (&acc_g)[N][Vec<T>::N],
-                                             float (&acc_b)[N][Vec<T>::N]) {
+                                             float2 (&acc_g)[N][Vec<T>::N / 2],
+                                             float2 (&acc_b)[N][Vec<T>::N / 2],
+                                             float2 (&acc_d)[N][Vec<T>::N / 2]) {
   constexpr int VEC = Vec<T>::N;
+  constexpr int P = VEC / 2;
   const int H = a.hidden;
   const int V = H / VEC;
-  float2 sums = make_float2(0.f, 0.f);
+  const float2 neg_mean = splat2(-mean);
+  const float2 r2 = splat2(rstd);
+  float2 sx = splat2(0.f), sy = splat2(0.f);
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
     if (row_ok && v < V) {
-      float d[VEC], xv[VEC], w[VEC];
-      unpack<T>(ld_vec_smem(dyrow + v * VEC), d);
-      unpack<T>(ld_vec_smem(xsrow + v * VEC), xv);
-      wr.template load<kStaged>(v, w);
+      float2 d[P], xv[P], w[P];
+      unpack2<T>(ld_vec_smem(dyrow + v * VEC), d);
+      unpack2<T>(ld_vec_smem(xsrow + v * VEC), xv);
+      wr.template load2<kStaged>(v, w);
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        const float xh = (kRms ? xv[e] : xv[e] - mean) * rstd;
-        const float g = d[e] * w[e];
-        if (!kRms) sums.x += g;
-        sums.y = fmaf(g, xh, sums.y);
-        acc_g[k][e] = fmaf(d[e], xh, acc_g[k][e]);
-        if (!kRms) acc_b[k][e] += d[e];
+      for (int i = 0; i < P; ++i) {
+        const float2 xh = mul2(kRms ? xv[i] : add2(xv[i], neg_mean), r2);
+        const float2 g = mul2(d[i], w[i]);
+        if (!kRms) sx = add2(sx, g);
+        sy = fma2(g, xh, sy);
+        acc_g[k][i] = fma2(d[i], xh, acc_g[k][i]);
+        if (!kRms) acc_b[k][i] = add2(acc_b[k][i], d[i]);
       }
     }
   }
-  sums = reduce2(sums);
+  const float2 sums = reduce2(make_float2(sx.x + sx.y, sy.x + sy.y));
   // dx = rstd * (g - c1 - xhat * c2) = (x - mean) * b2 + (g * rstd + a1)
   const float c2 = sums.y / (float)H;
-  const float a1 = kRms ? 0.f : -rstd * (sums.x / (float)H);
-  const float b2 = -rstd * rstd * c2;
+  const float2 a1 = splat2(kRms ? 0.f : -rstd * (sums.x / (float)H));
+  const float2 b2 = splat2(-rstd * rstd * c2);
   asm volatile("" ::: "memory");   // the second pass reads shared memory again
 
   T* dx = static_cast<T*>(a.dx) + row * (int64_t)H;
@@ -156,18 +162,40 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
     if (row_ok && v < V) {
-      float d[VEC], xv[VEC], w[VEC], o[VEC];
-      unpack<T>(ld_vec_smem(dyrow + v * VEC), d);
-      unpack<T>(ld_vec_smem(xsrow + v * VEC), xv);
-      wr.template load<kStaged>(v, w);
+      float2 d[P], xv[P], w[P], o[P];
+      unpack2<T>(ld_vec_smem(dyrow + v * VEC), d);
+      unpack2<T>(ld_vec_smem(xsrow + v * VEC), xv);
+      wr.template load2<kStaged>(v, w);
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        const float xm = kRms ? xv[e] : xv[e] - mean;
-        o[e] = fmaf(xm, b2, fmaf(d[e] * w[e], rstd, a1));
+      for (int i = 0; i < P; ++i) {
+        const float2 xm = kRms ? xv[i] : add2(xv[i], neg_mean);
+        o[i] = fma2(xm, b2, fma2(mul2(d[i], w[i]), r2, a1));
+        if (kBias) acc_d[k][i] = add2(acc_d[k][i], o[i]);
       }
-      st_vec(dx + v * VEC, pack<T>(o));
+      st_vec(dx + v * VEC, pack2<T>(o));
     }
   }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void zero_acc2(float2 (&acc)[N][Vec<T>::N / 2]) {
+#pragma unroll
+  for (int k = 0; k < N; ++k)
+#pragma unroll
+    for (int i = 0; i < Vec<T>::N / 2; ++i) acc[k][i] = splat2(0.f);
+}
+
+// The pipelined kernels' partials: the pair accumulators as plain floats.
+template <typename T, int N>
+__device__ __forceinline__ void unpair_acc(const float2 (&p)[N][Vec<T>::N / 2],
+                                           float (&f)[N][Vec<T>::N]) {
+#pragma unroll
+  for (int k = 0; k < N; ++k)
+#pragma unroll
+    for (int i = 0; i < Vec<T>::N / 2; ++i) {
+      f[k][2 * i] = p[k][i].x;
+      f[k][2 * i + 1] = p[k][i].y;
+    }
 }
 
 template <typename T, int N>
@@ -182,15 +210,25 @@ __device__ __forceinline__ void zero_acc(float (&acc_g)[N][Vec<T>::N],
     }
 }
 
+// Column offset of each partial row in the workspace: dgamma at 0, dbeta
+// at hidden (LayerNorm), dbias after them.
+__device__ __forceinline__ int partial_offset(const BwdArgs& a, int which) {
+  if (which == 0) return 0;
+  if (which == 1) return a.hidden;
+  return a.rms ? a.hidden : 2 * a.hidden;
+}
+
 // Partials of a lane-group kernel: W warps, each with 32 / LANES groups that
 // hold the same columns. Groups of a warp are added by a fixed butterfly,
 // then the warps through shared memory in warp order, one vector slot at a
 // time. Slot k covers columns [k * LANES * VEC, (k + 1) * LANES * VEC). All
 // threads of the CTA call this (threads of warps >= W only pass barriers).
-template <typename T, int LANES, int N, int W, bool kRms>
+// Accumulators: 0 = dgamma, 1 = dbeta (LayerNorm), 2 = dbias (kBias).
+template <typename T, int LANES, int N, int W, bool kRms, bool kBias>
 __device__ __forceinline__ void store_group_partials(const BwdArgs& a,
                                                      float (&acc_g)[N][Vec<T>::N],
                                                      float (&acc_b)[N][Vec<T>::N],
+                                                     float (&acc_d)[N][Vec<T>::N],
                                                      float (*red)[LANES * Vec<T>::N]) {
   constexpr int VEC = Vec<T>::N;
   constexpr int SLOT = LANES * VEC;
@@ -198,6 +236,7 @@ __device__ __forceinline__ void store_group_partials(const BwdArgs& a,
   const int warp = threadIdx.x >> 5;
   const int sub = lane / LANES;
   const int l = lane % LANES;
+  const bool rms = kRms || a.rms;
   if (warp < W) {
 #pragma unroll
     for (int o = LANES; o < 32; o <<= 1)
@@ -207,20 +246,21 @@ __device__ __forceinline__ void store_group_partials(const BwdArgs& a,
         for (int e = 0; e < VEC; ++e) {
           acc_g[k][e] += __shfl_xor_sync(0xffffffffu, acc_g[k][e], o);
           if (!kRms) acc_b[k][e] += __shfl_xor_sync(0xffffffffu, acc_b[k][e], o);
+          if (kBias) acc_d[k][e] += __shfl_xor_sync(0xffffffffu, acc_d[k][e], o);
         }
   }
-  const bool rms = kRms || a.rms;
   const int H = a.hidden;
-  const int C = rms ? H : 2 * H;
-  float* ws = a.ws + (int64_t)blockIdx.x * C;
-  const int nacc = rms ? 1 : 2;
-  for (int which = 0; which < nacc; ++which) {
+  float* ws = a.ws + (int64_t)blockIdx.x * a.ws_cols;
+  for (int which = 0; which < 3; ++which) {
+    if (which == 1 && (kRms || rms)) continue;
+    if (which == 2 && !kBias) continue;
+    const int off = partial_offset(a, which);
 #pragma unroll
     for (int k = 0; k < N; ++k) {
       if (warp < W && sub == 0) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e)
-          red[warp][l * VEC + e] = (!kRms && which) ? acc_b[k][e] : acc_g[k][e];
+          red[warp][l * VEC + e] = which == 0 ? acc_g[k][e] : (which == 1 ? acc_b[k][e] : acc_d[k][e]);
       }
       __syncthreads();
       for (int c = threadIdx.x; c < SLOT; c += blockDim.x) {
@@ -229,7 +269,7 @@ __device__ __forceinline__ void store_group_partials(const BwdArgs& a,
           float t = 0.f;
 #pragma unroll
           for (int w = 0; w < W; ++w) t += red[w][c];
-          ws[which * H + col] = t;
+          ws[off + col] = t;
         }
       }
       __syncthreads();
@@ -238,16 +278,17 @@ __device__ __forceinline__ void store_group_partials(const BwdArgs& a,
 }
 
 // Partials of a CTA-per-row kernel: every column belongs to one thread.
-template <typename T, int G, int N, bool kRms>
+template <typename T, int G, int N, bool kRms, bool kBias>
 __device__ __forceinline__ void store_thread_partials(const BwdArgs& a, int t,
                                                       float (&acc_g)[N][Vec<T>::N],
-                                                      float (&acc_b)[N][Vec<T>::N]) {
+                                                      float (&acc_b)[N][Vec<T>::N],
+                                                      float (&acc_d)[N][Vec<T>::N]) {
   constexpr int VEC = Vec<T>::N;
   const bool rms = kRms || a.rms;
   const int H = a.hidden;
   const int V = H / VEC;
-  const int C = rms ? H : 2 * H;
-  float* ws = a.ws + (int64_t)blockIdx.x * C;
+  float* ws = a.ws + (int64_t)blockIdx.x * a.ws_cols;
+  const int off_d = partial_offset(a, 2);
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
@@ -256,6 +297,7 @@ __device__ __forceinline__ void store_thread_partials(const BwdArgs& a, int t,
       for (int e = 0; e < VEC; ++e) {
         ws[v * VEC + e] = acc_g[k][e];
         if (!rms) ws[H + v * VEC + e] = acc_b[k][e];
+        if (kBias) ws[off_d + v * VEC + e] = acc_d[k][e];
       }
     }
   }
@@ -288,7 +330,7 @@ __global__ void __launch_bounds__(kWarpCta) bwd_warp_kernel(const BwdArgs a) {
                                             [](float2 v) { return group_sum2<LANES>(v); },
                                             acc_g, acc_b);
   }
-  store_group_partials<T, LANES, N, W, false>(a, acc_g, acc_b, red);
+  store_group_partials<T, LANES, N, W, false, false>(a, acc_g, acc_b, acc_b, red);
 }
 
 template <typename T, int THREADS, int N>
@@ -306,12 +348,12 @@ __global__ void __launch_bounds__(THREADS) bwd_cta_kernel(const BwdArgs a) {
         a, row, true, threadIdx.x, dy + off, xs + off, mean, rstd,
         [&](float2 v) { return cta_sum2<THREADS>(v, red); }, acc_g, acc_b);
   }
-  store_thread_partials<T, THREADS, N, false>(a, threadIdx.x, acc_g, acc_b);
+  store_thread_partials<T, THREADS, N, false, false>(a, threadIdx.x, acc_g, acc_b, acc_b);
 }
 
 // ---- bulk-copy pipelined kernels ------------------------------------------
 
-template <typename T, int LANES, int N, bool kRms>
+template <typename T, int LANES, int N, bool kRms, bool kBias>
 __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const BwdArgs a,
                                                                          const BulkCfg c) {
   constexpr int RPW = 32 / LANES;
@@ -322,7 +364,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
   const int H = a.hidden;
   const uint32_t in_bytes = (uint32_t)c.tile_rows * H * sizeof(T);
   const Ring ring = make_ring(smem, 2 * in_bytes, c.stages);
-  float* w_s = reinterpret_cast<float*>(ring.empty + c.stages);
+  float* w_s = reinterpret_cast<float*>(ring.after);
   if (threadIdx.x == 0) {
     s_abort = 0;
     s_taken = 0x7fffffffffffffffll;
@@ -334,8 +376,10 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
   const int lane = threadIdx.x & 31;
   const int l = lane % LANES;
   const int local = (threadIdx.x >> 5) * RPW + lane / LANES;   // row within the tile
-  float acc_g[N][Vec<T>::N], acc_b[N][Vec<T>::N];
-  zero_acc<T, N>(acc_g, acc_b);
+  float2 acc_g[N][Vec<T>::N / 2], acc_b[N][Vec<T>::N / 2], acc_d[N][Vec<T>::N / 2];
+  zero_acc2<T, N>(acc_g);
+  zero_acc2<T, N>(acc_b);
+  zero_acc2<T, N>(acc_d);
   // Statistics of this group's row in a tile, loaded one tile ahead.
   auto load_stats = [&](int64_t tile, float& m, float& r) {
     const int64_t row = tile * c.tile_rows + local;
@@ -349,24 +393,27 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
   float nm, nr;
   load_stats(blockIdx.x, nm, nr);
   bool aborted = false;
-  int64_t issued = 0;
   const int64_t taken = run_pipeline<false, T>(
       ring, c, a.rows, H, static_cast<const T*>(a.dy), static_cast<const T*>(a.x_sum), aborted,
-      issued, [&](int64_t tile, unsigned char* slot) {
+      [&](int64_t tile, unsigned char* slot) {
         const float mean = nm, rstd = nr;
         load_stats(tile + gridDim.x, nm, nr);
         const int64_t row = tile * c.tile_rows + local;
         const T* dys = reinterpret_cast<const T*>(slot) + (size_t)local * H;
         const T* xss = reinterpret_cast<const T*>(slot + in_bytes) + (size_t)local * H;
-        bwd_row_smem<T, LANES, N, kRms, true>(a, row, row < a.rows, l, dys, xss, wr, mean, rstd,
-                                        [](float2 v) { return group_sum2<LANES>(v); }, acc_g,
-                                        acc_b);
+        bwd_row_smem<T, LANES, N, kRms, kBias, true>(
+            a, row, row < a.rows, l, dys, xss, wr, mean, rstd,
+            [](float2 v) { return group_sum2<LANES>(v); }, acc_g, acc_b, acc_d);
       });
-  if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;
-  store_group_partials<T, LANES, N, kConsumerWarps, kRms>(a, acc_g, acc_b, red);
+  if (pipeline_finish(ring, aborted, taken, &s_abort, &s_taken)) return;
+  float fg[N][Vec<T>::N], fb[N][Vec<T>::N], fd[N][Vec<T>::N];
+  unpair_acc<T, N>(acc_g, fg);
+  unpair_acc<T, N>(acc_b, fb);
+  unpair_acc<T, N>(acc_d, fd);
+  store_group_partials<T, LANES, N, kConsumerWarps, kRms, kBias>(a, fg, fb, fd, red);
 }
 
-template <typename T, int N, bool kRms>
+template <typename T, int N, bool kRms, bool kBias>
 __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_cta_kernel(const BwdArgs a,
                                                                         const BulkCfg c) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -383,8 +430,10 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_cta_kernel(const Bwd
   const ParamRow<T> wr = {nullptr, static_cast<const T*>(a.gamma), H, a.zero_centered != 0};
   ring_init(ring);
 
-  float acc_g[N][Vec<T>::N], acc_b[N][Vec<T>::N];
-  zero_acc<T, N>(acc_g, acc_b);
+  float2 acc_g[N][Vec<T>::N / 2], acc_b[N][Vec<T>::N / 2], acc_d[N][Vec<T>::N / 2];
+  zero_acc2<T, N>(acc_g);
+  zero_acc2<T, N>(acc_b);
+  zero_acc2<T, N>(acc_d);
   auto load_stats = [&](int64_t row, float& m, float& r) {
     m = 0.f;
     r = 0.f;
@@ -396,27 +445,31 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_cta_kernel(const Bwd
   float nm, nr;
   load_stats(blockIdx.x, nm, nr);
   bool aborted = false;
-  int64_t issued = 0;
   const int64_t taken = run_pipeline<true, T>(
       ring, c, a.rows, H, static_cast<const T*>(a.dy), static_cast<const T*>(a.x_sum), aborted,
-      issued, [&](int64_t row, unsigned char* slot) {
+      [&](int64_t row, unsigned char* slot) {
         const float mean = nm, rstd = nr;
         load_stats(row + gridDim.x, nm, nr);
         const T* dys = reinterpret_cast<const T*>(slot);
         const T* xss = reinterpret_cast<const T*>(slot + in_bytes);
-        bwd_row_smem<T, kBulkThreads, N, kRms, false>(
+        bwd_row_smem<T, kBulkThreads, N, kRms, kBias, false>(
             a, row, true, threadIdx.x, dys, xss, wr, mean, rstd,
-            [&](float2 v) { return cta_sum2<kBulkThreads>(v, red); }, acc_g, acc_b);
+            [&](float2 v) { return cta_sum2<kBulkThreads>(v, red); }, acc_g, acc_b, acc_d);
       });
-  if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;
-  store_thread_partials<T, kBulkThreads, N, kRms>(a, threadIdx.x, acc_g, acc_b);
+  if (pipeline_finish(ring, aborted, taken, &s_abort, &s_taken)) return;
+  float fg[N][Vec<T>::N], fb[N][Vec<T>::N], fd[N][Vec<T>::N];
+  unpair_acc<T, N>(acc_g, fg);
+  unpair_acc<T, N>(acc_b, fb);
+  unpair_acc<T, N>(acc_d, fd);
+  store_thread_partials<T, kBulkThreads, N, kRms, kBias>(a, threadIdx.x, fg, fb, fd);
 }
 
 // ---- scalar kernel ----------------------------------------------------------
 
 // Any hidden size and alignment. Dynamic shared memory: 4 * hidden floats
-// (two per-row staging arrays and the two column accumulators); column j
-// belongs to thread j % kScalarCta throughout, so no barrier guards them.
+// (two per-row staging arrays and the dgamma/dbeta accumulators) plus hidden
+// floats of dbias accumulators when has_dbias; column j belongs to thread
+// j % kScalarCta throughout, so no barrier guards them.
 template <typename T>
 __global__ void __launch_bounds__(kScalarCta) bwd_scalar_kernel(const BwdArgs a) {
   extern __shared__ float sm[];
@@ -426,11 +479,16 @@ __global__ void __launch_bounds__(kScalarCta) bwd_scalar_kernel(const BwdArgs a)
   float* acc_b = sm + H;
   float* sxh = sm + 2 * H;
   float* sg = sm + 3 * H;
+  float* acc_d = sm + 4 * H;   // only with has_dbias
   const T* dy = static_cast<const T*>(a.dy);
   const T* xs = static_cast<const T*>(a.x_sum);
   const T* gamma = static_cast<const T*>(a.gamma);
   T* dx = static_cast<T*>(a.dx);
-  for (int j = threadIdx.x; j < H; j += kScalarCta) { acc_g[j] = 0.f; acc_b[j] = 0.f; }
+  for (int j = threadIdx.x; j < H; j += kScalarCta) {
+    acc_g[j] = 0.f;
+    acc_b[j] = 0.f;
+    if (a.has_dbias) acc_d[j] = 0.f;
+  }
   for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
     const int64_t off = row * (int64_t)H;
     const float rstd = a.rstd[row];
@@ -451,14 +509,18 @@ __global__ void __launch_bounds__(kScalarCta) bwd_scalar_kernel(const BwdArgs a)
     sums = cta_sum2<kScalarCta>(sums, red);
     const float c1 = a.rms ? 0.f : sums.x / (float)H;
     const float c2 = sums.y / (float)H;
-    for (int j = threadIdx.x; j < H; j += kScalarCta)
-      dx[off + j] = from_f<T>(rstd * (sg[j] - c1 - sxh[j] * c2));
+    for (int j = threadIdx.x; j < H; j += kScalarCta) {
+      const float o = rstd * (sg[j] - c1 - sxh[j] * c2);
+      dx[off + j] = from_f<T>(o);
+      if (a.has_dbias) acc_d[j] += o;
+    }
   }
-  const int C = a.rms ? H : 2 * H;
-  float* ws = a.ws + (int64_t)blockIdx.x * C;
+  float* ws = a.ws + (int64_t)blockIdx.x * a.ws_cols;
+  const int off_d = partial_offset(a, 2);
   for (int j = threadIdx.x; j < H; j += kScalarCta) {
     ws[j] = acc_g[j];
     if (!a.rms) ws[H + j] = acc_b[j];
+    if (a.has_dbias) ws[off_d + j] = acc_d[j];
   }
 }
 

@@ -52,12 +52,15 @@ struct BwdArgs {
   const float* mean;     // null for RMSNorm
   const float* rstd;
   void* dx;
-  float* ws;             // [gridDim.x][cols] partials, cols = hidden or 2*hidden
+  float* ws;             // [gridDim.x][ws_cols] partials: dgamma, then dbeta
+                         // (LayerNorm), then dbias (when has_dbias), hidden each
   int64_t rows;
   int hidden;
   float inv_hidden;
   int rms;
   int zero_centered;
+  int has_dbias;         // also accumulate dbias = sum over rows of dx
+  int ws_cols;
 };
 
 // Launch parameters of the pipelined (bulk-copy) kernels.
@@ -149,6 +152,58 @@ template <> __device__ __forceinline__ uint4 pack<f16>(const float* f) {
 // that also lets a NaN win, as torch.amax does.
 __device__ __forceinline__ unsigned abs_bits(float v) {
   return __float_as_uint(v) & 0x7fffffffu;
+}
+
+// ---- fp32 pairs -------------------------------------------------------------
+// sm_100-class GPUs issue two IEEE round-to-nearest fp32 adds, multiplies or
+// fmas in one instruction on a register pair; the row bodies of the pipelined
+// kernels keep their values as float2 pairs to use them.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+
+// Unpack a 16-byte vector of T into Vec<T>::N / 2 fp32 pairs.
+template <typename T> __device__ __forceinline__ void unpack2(const uint4& u, float2* f);
+template <> __device__ __forceinline__ void unpack2<float>(const uint4& u, float2* f) {
+  f[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+  f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+}
+__device__ __forceinline__ float2 bf16x2_to_f2(unsigned w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+template <> __device__ __forceinline__ void unpack2<bf16>(const uint4& u, float2* f) {
+  f[0] = bf16x2_to_f2(u.x); f[1] = bf16x2_to_f2(u.y);
+  f[2] = bf16x2_to_f2(u.z); f[3] = bf16x2_to_f2(u.w);
+}
+__device__ __forceinline__ float2 f16x2_to_f2(unsigned w) {
+  return __half22float2(*reinterpret_cast<__half2*>(&w));
+}
+template <> __device__ __forceinline__ void unpack2<f16>(const uint4& u, float2* f) {
+  f[0] = f16x2_to_f2(u.x); f[1] = f16x2_to_f2(u.y);
+  f[2] = f16x2_to_f2(u.z); f[3] = f16x2_to_f2(u.w);
+}
+
+// Pack fp32 pairs into a 16-byte vector of T (round to nearest even).
+template <typename T> __device__ __forceinline__ uint4 pack2(const float2* f);
+template <> __device__ __forceinline__ uint4 pack2<float>(const float2* f) {
+  return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y),
+                    __float_as_uint(f[1].x), __float_as_uint(f[1].y));
+}
+__device__ __forceinline__ unsigned f2_to_bf16x2(float2 v) {
+  __nv_bfloat162 h = __float22bfloat162_rn(v);
+  return *reinterpret_cast<unsigned*>(&h);
+}
+template <> __device__ __forceinline__ uint4 pack2<bf16>(const float2* f) {
+  return make_uint4(f2_to_bf16x2(f[0]), f2_to_bf16x2(f[1]), f2_to_bf16x2(f[2]),
+                    f2_to_bf16x2(f[3]));
+}
+__device__ __forceinline__ unsigned f2_to_f16x2(float2 v) {
+  __half2 h = __float22half2_rn(v);
+  return *reinterpret_cast<unsigned*>(&h);
+}
+template <> __device__ __forceinline__ uint4 pack2<f16>(const float2* f) {
+  return make_uint4(f2_to_f16x2(f[0]), f2_to_f16x2(f[1]), f2_to_f16x2(f[2]), f2_to_f16x2(f[3]));
 }
 
 // Running amax over stored 16-byte vectors. For 16-bit types the

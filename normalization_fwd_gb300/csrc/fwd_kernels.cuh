@@ -11,9 +11,9 @@
 //
 //  * fwd_bulk_warp_kernel / fwd_bulk_cta_kernel (default for 16-byte aligned
 //    rows): tiles of rows stream into a shared-memory ring by cp.async.bulk
-//    (issued by thread 0 a few tiles ahead) and 8 warps normalize them from
-//    shared memory (a lane group of LANES lanes per row, or all 256 threads
-//    per row for rows longer than 256 vectors).
+//    (every slot in flight, each refilled by the warp that frees it last) and
+//    8 warps normalize them from shared memory (a lane group of LANES lanes
+//    per row, or all 256 threads per row for rows longer than 256 vectors).
 //  * fwd_warp_kernel / fwd_cta_kernel: the same row body with the row loaded
 //    straight into registers (128-bit loads); used when the ring does not fit.
 //  * fwd_scalar_kernel: any hidden size and alignment; element-wise loads,
@@ -221,12 +221,14 @@ __device__ __forceinline__ FwdParams<T> fwd_params(const FwdArgs& a, float* p_s)
 }
 
 // The row body of the pipelined kernels: x and residual rows in shared
-// memory (ring slot), parameters as fp32 in shared memory.
+// memory (ring slot), parameters staged in shared memory (kStaged) or read
+// from global memory. Values are kept as fp32 pairs (packed fp32 math).
 template <typename T, int G, int N, bool kStaged, typename Reduce>
 __device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool row_ok, int t,
                                              const T* xrow, const T* rrow, const FwdParams<T>& p,
                                              Reduce reduce, unsigned& amax_acc, bool write_stats) {
   constexpr int VEC = Vec<T>::N;
+  constexpr int P = VEC / 2;
   const int H = a.hidden;
   const int V = H / VEC;
   T* sum_row = a.out_sum ? static_cast<T*>(a.out_sum) + row * (int64_t)H : nullptr;
@@ -234,70 +236,72 @@ __device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool
 
   // F1: s = (x + bias) + residual in fp32, stored rounded; the statistics
   // see the stored value.
-  float s[N][VEC];
-  float t1 = 0.f;
+  float2 s[N][P];
+  float2 t1 = splat2(0.f);
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) s[k][e] = 0.f;
+    for (int i = 0; i < P; ++i) s[k][i] = splat2(0.f);
     if (row_ok && v < V) {
-      unpack<T>(ld_vec_smem(xrow + v * VEC), s[k]);
+      unpack2<T>(ld_vec_smem(xrow + v * VEC), s[k]);
       if (p.bias.g) {
-        float b[VEC];
-        p.bias.template load<kStaged>(v, b);
+        float2 b[P];
+        p.bias.template load2<kStaged>(v, b);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) s[k][e] += b[e];
+        for (int i = 0; i < P; ++i) s[k][i] = add2(s[k][i], b[i]);
       }
       if (rrow) {
-        float r[VEC];
-        unpack<T>(ld_vec_smem(rrow + v * VEC), r);
+        float2 r[P];
+        unpack2<T>(ld_vec_smem(rrow + v * VEC), r);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) s[k][e] += r[e];
+        for (int i = 0; i < P; ++i) s[k][i] = add2(s[k][i], r[i]);
       }
-      const uint4 packed = pack<T>(s[k]);
+      const uint4 packed = pack2<T>(s[k]);
       if (sum_row) st_vec(sum_row + v * VEC, packed);
-      unpack<T>(packed, s[k]);
+      unpack2<T>(packed, s[k]);
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) t1 += s[k][e];
+      for (int i = 0; i < P; ++i) t1 = add2(t1, s[k][i]);
     }
   }
 
   // F2: mean, then the centred sum of squares (RMSNorm: mean 0).
-  const float mean = a.rms ? 0.f : reduce(t1) / (float)H;
-  float t2 = 0.f;
+  const float mean = a.rms ? 0.f : reduce(t1.x + t1.y) / (float)H;
+  const float2 neg_mean = splat2(-mean);
+  float2 t2 = splat2(0.f);
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     if (row_ok && (k * G + t) < V) {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        s[k][e] -= mean;
-        t2 = fmaf(s[k][e], s[k][e], t2);
+      for (int i = 0; i < P; ++i) {
+        s[k][i] = add2(s[k][i], neg_mean);
+        t2 = fma2(s[k][i], s[k][i], t2);
       }
     }
   }
-  const float rstd = 1.0f / sqrtf(reduce(t2) / (float)H + a.eps);
+  const float rstd = 1.0f / sqrtf(reduce(t2.x + t2.y) / (float)H + a.eps);
   if (row_ok && write_stats) {
     if (a.mean) a.mean[row] = mean;
     if (a.rstd) a.rstd[row] = rstd;
   }
 
   // F3: y = (s - mean) * rstd * w + beta; F4: amax of the stored y.
+  const float2 r2 = splat2(rstd);
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
     if (row_ok && v < V) {
-      float w[VEC], o[VEC];
-      p.w.template load<kStaged>(v, w);
+      float2 w[P], o[P];
+      p.w.template load2<kStaged>(v, w);
       if (p.beta.g) {
-        p.beta.template load<kStaged>(v, o);
+        p.beta.template load2<kStaged>(v, o);
       } else {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) o[e] = 0.f;
+        for (int i = 0; i < P; ++i) o[i] = splat2(0.f);
       }
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) o[e] = fmaf(s[k][e] * rstd, w[e], o[e]);
-      const uint4 packed = pack<T>(o);
+      for (int i = 0; i < P; ++i) o[i] = fma2(mul2(s[k][i], r2), w[i], o[i]);
+      const uint4 packed = pack2<T>(o);
       st_vec(y_row + v * VEC, packed);
       if (a.amax) amax_update<T>(amax_acc, packed);
     }
@@ -320,18 +324,17 @@ __global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 3 : 2) fwd_bulk_warp_ke
     s_abort = 0;
     s_taken = 0x7fffffffffffffffll;
   }
-  const FwdParams<T> p = fwd_params<T>(a, reinterpret_cast<float*>(ring.empty + c.stages));
+  const FwdParams<T> p = fwd_params<T>(a, reinterpret_cast<float*>(ring.after));
   ring_init(ring);
 
   const int lane = threadIdx.x & 31;
   const int l = lane % LANES;
   const int local = (threadIdx.x >> 5) * RPW + lane / LANES;   // row within the tile
   bool aborted = false;
-  int64_t issued = 0;
   unsigned amax_acc = 0;
   const int64_t taken = run_pipeline<false, T>(
       ring, c, a.rows, H, static_cast<const T*>(a.x), static_cast<const T*>(a.residual), aborted,
-      issued, [&](int64_t tile, unsigned char* slot) {
+      [&](int64_t tile, unsigned char* slot) {
         const int64_t row = tile * c.tile_rows + local;
         const T* xs = reinterpret_cast<const T*>(slot) + (size_t)local * H;
         const T* rs = a.residual ? reinterpret_cast<const T*>(slot + in_bytes) + (size_t)local * H
@@ -339,7 +342,7 @@ __global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 3 : 2) fwd_bulk_warp_ke
         fwd_row_smem<T, LANES, N, true>(a, row, row < a.rows, l, xs, rs, p,
                                   [](float v) { return group_sum<LANES>(v); }, amax_acc, l == 0);
       });
-  if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;
+  if (pipeline_finish(ring, aborted, taken, &s_abort, &s_taken)) return;
   if (a.amax) cta_amax_commit(amax_bits<T>(amax_acc), a.amax, red_amax);
 }
 
@@ -363,18 +366,17 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_cta_kernel(const Fwd
   ring_init(ring);
 
   bool aborted = false;
-  int64_t issued = 0;
   unsigned amax_acc = 0;
   const int64_t taken = run_pipeline<true, T>(
       ring, c, a.rows, H, static_cast<const T*>(a.x), static_cast<const T*>(a.residual), aborted,
-      issued, [&](int64_t row, unsigned char* slot) {
+      [&](int64_t row, unsigned char* slot) {
         const T* xs = reinterpret_cast<const T*>(slot);
         const T* rs = a.residual ? reinterpret_cast<const T*>(slot + in_bytes) : nullptr;
         fwd_row_smem<T, kBulkThreads, N, false>(a, row, true, threadIdx.x, xs, rs, p,
                                          [&](float v) { return cta_sum<kBulkThreads>(v, red); },
                                          amax_acc, threadIdx.x == 0);
       });
-  if (pipeline_finish(ring, aborted, issued, taken, &s_abort, &s_taken)) return;
+  if (pipeline_finish(ring, aborted, taken, &s_abort, &s_taken)) return;
   if (a.amax) cta_amax_commit(amax_bits<T>(amax_acc), a.amax, red_amax);
 }
 

@@ -45,10 +45,14 @@ int path_override();
   const void* fwd_reg_table_##NAME(int kind, int group, int n);           \
   const void* bwd_bulk_ln_table_##NAME(int kind, int group, int n);       \
   const void* bwd_bulk_rms_table_##NAME(int kind, int group, int n);      \
+  const void* bwd_bulk_ln_dbias_table_##NAME(int kind, int group, int n); \
+  const void* bwd_bulk_rms_dbias_table_##NAME(int kind, int group, int n); \
   const void* bwd_reg_table_##NAME(int kind, int group, int n);           \
   cudaError_t take_error_fwd_bulk_##NAME(cudaStream_t st, unsigned* out); \
   cudaError_t take_error_bwd_bulk_ln_##NAME(cudaStream_t st, unsigned* out); \
-  cudaError_t take_error_bwd_bulk_rms_##NAME(cudaStream_t st, unsigned* out);
+  cudaError_t take_error_bwd_bulk_rms_##NAME(cudaStream_t st, unsigned* out); \
+  cudaError_t take_error_bwd_bulk_ln_dbias_##NAME(cudaStream_t st, unsigned* out); \
+  cudaError_t take_error_bwd_bulk_rms_dbias_##NAME(cudaStream_t st, unsigned* out);
 NF_DECLARE_TABLES(f32)
 NF_DECLARE_TABLES(bf16)
 NF_DECLARE_TABLES(f16)
@@ -59,14 +63,17 @@ template <typename T>
 cudaError_t fwd_plan(int64_t rows, int hidden, bool vec, bool has_residual, int n_params,
                      Plan* p);
 template <typename T> cudaError_t fwd_launch(const FwdArgs& a, const Plan& p, cudaStream_t st);
-template <typename T> cudaError_t bwd_plan(int64_t rows, int hidden, bool rms, bool vec, Plan* p);
 template <typename T>
-cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, float* dgamma, float* dbeta,
+cudaError_t bwd_plan(int64_t rows, int hidden, bool rms, bool dbias, bool vec, Plan* p);
+template <typename T>
+cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, float* dgamma, float* dbeta, float* dbias,
                        cudaStream_t st);
 
 // Fixed-order sum of the backward's per-CTA partials (finalize.cu).
-cudaError_t launch_bwd_finalize(const float* ws, int P, int C, int H, float* dgamma,
-                                float* dbeta, cudaStream_t st);
+// Columns of a partial row: [0, H) dgamma, then [H, 2H) dbeta when `beta_cols`,
+// then H columns of dbias when dbias is non-null.
+cudaError_t launch_bwd_finalize(const float* ws, int P, int C, int H, bool beta_cols,
+                                float* dgamma, float* dbeta, float* dbias, cudaStream_t st);
 
 }  // namespace nf
 

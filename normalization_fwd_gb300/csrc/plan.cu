@@ -1,8 +1,11 @@
 // Host-side planning and launching: which kernel runs a call, its grid,
 // block and shared memory, and the launch itself. Kernels come from the
 // per-family tables of the kernel translation units (tables.cuh).
+#include <stdlib.h>
+
 #include <algorithm>
 
+#include "bulk.cuh"
 #include "launch.h"
 
 namespace nf {
@@ -55,7 +58,9 @@ template <typename T> struct Tables;
   template <> struct Tables<T> {                                                    \
     static const void* fwd_bulk(int k, int g, int n) { return fwd_bulk_table_##NAME(k, g, n); } \
     static const void* fwd_reg(int k, int g, int n) { return fwd_reg_table_##NAME(k, g, n); }   \
-    static const void* bwd_bulk(int k, int g, int n, bool rms) {                    \
+    static const void* bwd_bulk(int k, int g, int n, bool rms, bool dbias) {        \
+      if (dbias) return rms ? bwd_bulk_rms_dbias_table_##NAME(k, g, n)              \
+                            : bwd_bulk_ln_dbias_table_##NAME(k, g, n);              \
       return rms ? bwd_bulk_rms_table_##NAME(k, g, n) : bwd_bulk_ln_table_##NAME(k, g, n); \
     }                                                                               \
     static const void* bwd_reg(int k, int g, int n) { return bwd_reg_table_##NAME(k, g, n); }   \
@@ -72,6 +77,22 @@ constexpr size_t kRingTarget = 104 * 1024;
 constexpr size_t kRingTargetFwdGroup = 68 * 1024;
 constexpr size_t kMaxDynSmem = 200 * 1024;
 
+// Ring targets may be overridden (in KiB) through NORMFUSE_RING_KB_FWD /
+// NORMFUSE_RING_KB_BWD for tuning; read once.
+inline size_t ring_target_kb_env(const char* name) {
+  const char* e = getenv(name);
+  if (e == nullptr) return 0;
+  const long v = strtol(e, nullptr, 10);
+  return (v >= 16 && v <= 200) ? (size_t)v * 1024 : 0;
+}
+inline size_t ring_target(bool bwd, bool fwd_group) {
+  static const size_t fwd_env = ring_target_kb_env("NORMFUSE_RING_KB_FWD");
+  static const size_t bwd_env = ring_target_kb_env("NORMFUSE_RING_KB_BWD");
+  if (bwd) return bwd_env ? bwd_env : kRingTarget;
+  if (fwd_env) return fwd_env;
+  return fwd_group ? kRingTargetFwdGroup : kRingTarget;
+}
+
 // Fill in a pipelined plan; false when the ring does not fit. `extra`:
 // shared bytes after the ring's barriers (the backward's fp32 weight row).
 inline bool fill_bulk(Plan* p, const Choice& c, int64_t rows, int hidden, size_t esize, int n_in,
@@ -80,7 +101,7 @@ inline bool fill_bulk(Plan* p, const Choice& c, int64_t rows, int hidden, size_t
   const size_t slot = (size_t)n_in * tile_rows * hidden * esize;
   const size_t room = target > extra ? target - extra : 0;
   int stages = (int)std::min<size_t>(8, std::max<size_t>(2, room / slot));
-  size_t smem = (size_t)stages * slot + 2 * stages * sizeof(uint64_t) + extra;
+  size_t smem = (size_t)stages * slot + ring_aux_bytes(stages) + extra;
   if (smem > kMaxDynSmem) return false;
   p->bulk = true;
   p->kind = c.kind;
@@ -96,7 +117,7 @@ inline bool fill_bulk(Plan* p, const Choice& c, int64_t rows, int hidden, size_t
 
 // Fill block, shared memory and the rows one CTA covers per loop step of the
 // register or scalar kernels.
-inline int64_t fill_shape(Plan* p, const Choice& c, int hidden, bool bwd) {
+inline int64_t fill_shape(Plan* p, const Choice& c, int hidden, bool bwd, bool dbias) {
   p->bulk = false;
   p->kind = c.kind;
   p->group = c.group;
@@ -112,7 +133,7 @@ inline int64_t fill_shape(Plan* p, const Choice& c, int hidden, bool bwd) {
     return 1;
   }
   p->block = kScalarCta;
-  p->smem = (size_t)hidden * sizeof(float) * (bwd ? 4 : 1);
+  p->smem = (size_t)hidden * sizeof(float) * (bwd ? (dbias ? 5 : 4) : 1);
   return 1;
 }
 
@@ -138,9 +159,11 @@ inline cudaError_t size_grid(Plan* p, int64_t steps) {
 // n_params: [hidden] parameter rows the pipelined kernels stage in shared
 // memory as fp32.
 template <typename T>
-cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, int n_in,
-                      int n_params, Plan* p) {
+cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bool dbias,
+                      int n_in, int n_params, Plan* p) {
   Choice c = choose(hidden, Vec<T>::N, vec);
+  // The register kernels do not accumulate dbias; the scalar kernel does.
+  if (bwd && dbias && vec && path_override() == kPathRegisters) c = choose(hidden, 1, false);
   const bool want_bulk = vec && path_override() != kPathRegisters;
   if (want_bulk) {
     Choice b = c;
@@ -148,22 +171,22 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, in
     // Lane-group kernels stage the parameter rows in shared memory as fp32;
     // CTA-per-row kernels read them from global memory.
     const size_t extra = b.kind == 0 ? (size_t)n_params * hidden * sizeof(float) : 0;
-    const size_t target = (!bwd && b.kind == 0 && b.n <= 4) ? kRingTargetFwdGroup : kRingTarget;
+    const size_t target = ring_target(bwd, b.kind == 0 && b.n <= 4);
     if (fill_bulk(p, b, rows, hidden, sizeof(T), n_in, extra, target)) {
-      p->fn = bwd ? Tables<T>::bwd_bulk(b.kind, b.group, b.n, rms)
+      p->fn = bwd ? Tables<T>::bwd_bulk(b.kind, b.group, b.n, rms, dbias)
                   : Tables<T>::fwd_bulk(b.kind, b.group, b.n);
       return size_grid(p, p->cfg.num_tiles);
     }
   }
   p->fn = bwd ? Tables<T>::bwd_reg(c.kind, c.group, c.n) : Tables<T>::fwd_reg(c.kind, c.group, c.n);
-  const int64_t rpc = fill_shape(p, c, hidden, bwd);
+  const int64_t rpc = fill_shape(p, c, hidden, bwd, dbias);
   return size_grid(p, (rows + rpc - 1) / rpc);
 }
 
 template <typename T>
 cudaError_t fwd_plan(int64_t rows, int hidden, bool vec, bool has_residual, int n_params,
                      Plan* p) {
-  return make_plan<T>(rows, hidden, vec, false, false, has_residual ? 2 : 1, n_params, p);
+  return make_plan<T>(rows, hidden, vec, false, false, false, has_residual ? 2 : 1, n_params, p);
 }
 
 // Pipelined kernels take (args, BulkCfg); the others take (args) only.
@@ -179,19 +202,20 @@ template <typename T> cudaError_t fwd_launch(const FwdArgs& a, const Plan& p, cu
   return launch_plan(p, const_cast<FwdArgs*>(&a), st);
 }
 
-template <typename T> cudaError_t bwd_plan(int64_t rows, int hidden, bool rms, bool vec, Plan* p) {
-  cudaError_t e = make_plan<T>(rows, hidden, vec, true, rms, 2, 1, p);
-  p->ws_cols = rms ? hidden : 2 * hidden;
+template <typename T>
+cudaError_t bwd_plan(int64_t rows, int hidden, bool rms, bool dbias, bool vec, Plan* p) {
+  cudaError_t e = make_plan<T>(rows, hidden, vec, true, rms, dbias, 2, 1, p);
+  p->ws_cols = hidden * (1 + (rms ? 0 : 1) + (dbias ? 1 : 0));
   return e;
 }
 
 template <typename T>
-cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, float* dgamma, float* dbeta,
+cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, float* dgamma, float* dbeta, float* dbias,
                        cudaStream_t st) {
   cudaError_t e = launch_plan(p, const_cast<BwdArgs*>(&a), st);
   if (e != cudaSuccess) return e;
-  return launch_bwd_finalize(a.ws, p.grid, p.ws_cols, a.hidden, dgamma, a.rms ? nullptr : dbeta,
-                             st);
+  return launch_bwd_finalize(a.ws, p.grid, p.ws_cols, a.hidden, !a.rms, dgamma,
+                             a.rms ? nullptr : dbeta, a.has_dbias ? dbias : nullptr, st);
 }
 
 }  // namespace nf
@@ -199,15 +223,15 @@ cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, float* dgamma, float* db
 template cudaError_t nf::fwd_plan<float>(int64_t, int, bool, bool, int, nf::Plan*);
 template cudaError_t nf::fwd_plan<nf::bf16>(int64_t, int, bool, bool, int, nf::Plan*);
 template cudaError_t nf::fwd_plan<nf::f16>(int64_t, int, bool, bool, int, nf::Plan*);
-template cudaError_t nf::bwd_plan<float>(int64_t, int, bool, bool, nf::Plan*);
-template cudaError_t nf::bwd_plan<nf::bf16>(int64_t, int, bool, bool, nf::Plan*);
-template cudaError_t nf::bwd_plan<nf::f16>(int64_t, int, bool, bool, nf::Plan*);
+template cudaError_t nf::bwd_plan<float>(int64_t, int, bool, bool, bool, nf::Plan*);
+template cudaError_t nf::bwd_plan<nf::bf16>(int64_t, int, bool, bool, bool, nf::Plan*);
+template cudaError_t nf::bwd_plan<nf::f16>(int64_t, int, bool, bool, bool, nf::Plan*);
 template cudaError_t nf::fwd_launch<float>(const nf::FwdArgs&, const nf::Plan&, cudaStream_t);
 template cudaError_t nf::fwd_launch<nf::bf16>(const nf::FwdArgs&, const nf::Plan&, cudaStream_t);
 template cudaError_t nf::fwd_launch<nf::f16>(const nf::FwdArgs&, const nf::Plan&, cudaStream_t);
 template cudaError_t nf::bwd_launch<float>(const nf::BwdArgs&, const nf::Plan&, float*, float*,
-                                           cudaStream_t);
+                                           float*, cudaStream_t);
 template cudaError_t nf::bwd_launch<nf::bf16>(const nf::BwdArgs&, const nf::Plan&, float*, float*,
-                                              cudaStream_t);
+                                              float*, cudaStream_t);
 template cudaError_t nf::bwd_launch<nf::f16>(const nf::BwdArgs&, const nf::Plan&, float*, float*,
-                                             cudaStream_t);
+                                             float*, cudaStream_t);

@@ -27,26 +27,26 @@ namespace nf {
     case 4: return (const void*)KERNEL<T, TH, 4>;  \
     default: return nullptr;                       \
   }
-#define NF_BULK_WARP_CASES_M(KERNEL, T, L, M)      \
-  switch (n) {                                     \
-    case 1: return (const void*)KERNEL<T, L, 1, M>; \
-    case 2: return (const void*)KERNEL<T, L, 2, M>; \
-    case 3: return (const void*)KERNEL<T, L, 3, M>; \
-    case 4: return (const void*)KERNEL<T, L, 4, M>; \
-    case 5: return (const void*)KERNEL<T, L, 5, M>; \
-    case 6: return (const void*)KERNEL<T, L, 6, M>; \
-    case 8: return (const void*)KERNEL<T, L, 8, M>; \
-    default: return nullptr;                       \
+#define NF_BULK_WARP_CASES_M(KERNEL, T, L, M, B)      \
+  switch (n) {                                        \
+    case 1: return (const void*)KERNEL<T, L, 1, M, B>; \
+    case 2: return (const void*)KERNEL<T, L, 2, M, B>; \
+    case 3: return (const void*)KERNEL<T, L, 3, M, B>; \
+    case 4: return (const void*)KERNEL<T, L, 4, M, B>; \
+    case 5: return (const void*)KERNEL<T, L, 5, M, B>; \
+    case 6: return (const void*)KERNEL<T, L, 6, M, B>; \
+    case 8: return (const void*)KERNEL<T, L, 8, M, B>; \
+    default: return nullptr;                          \
   }
-#define NF_BULK_CTA_CASES_M(KERNEL, T, M)          \
-  switch (n) {                                     \
-    case 2: return (const void*)KERNEL<T, 2, M>;   \
-    case 3: return (const void*)KERNEL<T, 3, M>;   \
-    case 4: return (const void*)KERNEL<T, 4, M>;   \
-    case 5: return (const void*)KERNEL<T, 5, M>;   \
-    case 6: return (const void*)KERNEL<T, 6, M>;   \
-    case 8: return (const void*)KERNEL<T, 8, M>;   \
-    default: return nullptr;                       \
+#define NF_BULK_CTA_CASES_M(KERNEL, T, M, B)          \
+  switch (n) {                                        \
+    case 2: return (const void*)KERNEL<T, 2, M, B>;   \
+    case 3: return (const void*)KERNEL<T, 3, M, B>;   \
+    case 4: return (const void*)KERNEL<T, 4, M, B>;   \
+    case 5: return (const void*)KERNEL<T, 5, M, B>;   \
+    case 6: return (const void*)KERNEL<T, 6, M, B>;   \
+    case 8: return (const void*)KERNEL<T, 8, M, B>;   \
+    default: return nullptr;                          \
   }
 #define NF_BULK_CTA_CASES(KERNEL, T)               \
   switch (n) {                                     \
@@ -85,13 +85,14 @@ template <typename T> const void* fwd_reg_table_impl(int kind, int group, int n)
   return nullptr;
 }
 
-template <typename T, bool kRms> const void* bwd_bulk_table_impl(int kind, int group, int n) {
+template <typename T, bool kRms, bool kBias>
+const void* bwd_bulk_table_impl(int kind, int group, int n) {
   if (kind == 0) {
-    if (group == 8) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 8, kRms) }
-    if (group == 16) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 16, kRms) }
-    if (group == 32) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 32, kRms) }
+    if (group == 8) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 8, kRms, kBias) }
+    if (group == 16) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 16, kRms, kBias) }
+    if (group == 32) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 32, kRms, kBias) }
   } else if (kind == 1) {
-    NF_BULK_CTA_CASES_M(bwd_bulk_cta_kernel, T, kRms)
+    NF_BULK_CTA_CASES_M(bwd_bulk_cta_kernel, T, kRms, kBias)
   }
   return nullptr;
 }

@@ -90,9 +90,10 @@ def gpu_fwd(lib, w, inp, *, store_sum=True, stats=True, amax=None, stream=None,
     return result
 
 
-def gpu_bwd(lib, w, dy, x_sum, gamma, mean, rstd, *, need_dbeta=True, workspace=None,
-            stream=None):
-    """Run ln_bwd; inputs are CPU or CUDA tensors. Returns CPU tensors."""
+def gpu_bwd(lib, w, dy, x_sum, gamma, mean, rstd, *, need_dbeta=True, need_dbias=False,
+            workspace=None, stream=None):
+    """Run ln_bwd (ln_bwd_ex with dbias); inputs are CPU or CUDA tensors.
+    Returns CPU tensors."""
     dev = "cuda"
     dt = TORCH_DTYPES[w.dtype]
     R, H = w.rows, w.hidden
@@ -103,9 +104,16 @@ def gpu_bwd(lib, w, dy, x_sum, gamma, mean, rstd, *, need_dbeta=True, workspace=
     outs = {"dx": Guarded((R, H), dt), "dgamma": Guarded((H,), torch.float32)}
     if need_dbeta and not rms:
         outs["dbeta"] = Guarded((H,), torch.float32)
+    if need_dbias:
+        outs["dbias"] = Guarded((H,), torch.float32)
     g = {k: v.t for k, v in outs.items()}
-    lib.ln_bwd(dy, x_sum, gamma, mean, rstd, g["dx"], g["dgamma"], g.get("dbeta"), stream,
-               mode=w.mode, zero_centered_gamma=w.zero_centered_gamma, workspace=workspace)
+    if need_dbias:
+        lib.ln_bwd_ex(dy, x_sum, gamma, mean, rstd, g["dx"], g["dgamma"], g.get("dbeta"),
+                      g["dbias"], stream, mode=w.mode, zero_centered_gamma=w.zero_centered_gamma,
+                      workspace=workspace)
+    else:
+        lib.ln_bwd(dy, x_sum, gamma, mean, rstd, g["dx"], g["dgamma"], g.get("dbeta"), stream,
+                   mode=w.mode, zero_centered_gamma=w.zero_centered_gamma, workspace=workspace)
     torch.cuda.synchronize()
     assert lib.ln_device_error() == 0, "a kernel reported a failed wait"
     result = {k: v.t.cpu() for k, v in outs.items()}

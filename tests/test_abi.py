@@ -35,8 +35,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
-        ["ln_fwd", "ln_bwd", "ln_bwd_workspace_bytes", "ln_status_string", "ln_last_cuda_error",
-         "ln_device_error", "ln_bwd_noalloc"])
+        ["ln_fwd", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes", "ln_status_string",
+         "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -119,6 +119,21 @@ def bwd(lib, dy=X, xs=RES, gamma=G, mean=M, rstd=R, dx=Y, dg=S, db=B, rows=4, hi
 ])
 def test_bwd_rejects_on_host(lib, kw, want):
     assert bwd(lib, **kw) == want
+
+
+def test_bwd_ex_validates_dbias_on_host(lib):
+    def call(dbias, **kw):
+        a = dict(dy=X, xs=RES, gamma=G, mean=M, rstd=R, dx=Y, dg=S, db=B, rows=4, hidden=384,
+                 dtype=1, mode=0, zc=0, ws=A, ws_bytes=1 << 20)
+        a.update(kw)
+        return lib.ln_bwd_ex(a["dy"], a["xs"], a["gamma"], a["mean"], a["rstd"], a["dx"], a["dg"],
+                             a["db"], dbias, None, a["rows"], a["hidden"], a["dtype"], a["mode"],
+                             a["zc"], a["ws"], a["ws_bytes"])
+    DBIAS = 0x7f0000000000 + 11 * 0x10000000
+    assert call(DBIAS + 2) == ALIGN
+    assert call(S + 16) == INVALID          # overlaps dgamma
+    assert call(X + 64) == INVALID          # overlaps dy
+    assert call(DBIAS, dy=None) == NULL
 
 
 def test_rmsnorm_ignores_mean_and_dbeta(lib):
