@@ -5,6 +5,8 @@ Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 library and imports nothing from ``normalization_fwd_gb300``.
 """
 
-from .norm import LAYERNORM, RMSNORM, norm_bwd, norm_fwd, round_to_format
+from .norm import (E4M3_MAX, LAYERNORM, RMSNORM, norm_bwd, norm_fwd, quantize_fp8_e4m3,
+                   round_to_e4m3_satfinite, round_to_format)
 
-__all__ = ["LAYERNORM", "RMSNORM", "norm_fwd", "norm_bwd", "round_to_format"]
+__all__ = ["LAYERNORM", "RMSNORM", "norm_fwd", "norm_bwd", "round_to_format",
+           "round_to_e4m3_satfinite", "quantize_fp8_e4m3", "E4M3_MAX"]

@@ -84,6 +84,42 @@ def round_to_format(v, fmt: str) -> np.ndarray:
     return out
 
 
+E4M3_MAX = 448.0
+
+
+def round_to_e4m3_satfinite(v) -> np.ndarray:
+    """Round float64 values to FP8 E4M3 (1 sign, 4 exponent bits with bias 7,
+    3 mantissa bits; no infinities), nearest even, saturating finite values
+    beyond the largest finite magnitude (448) to +-448; NaN stays NaN.
+
+    E4M3 has normals from 2**-6 and subnormals spaced 2**-9; 1.875 * 2**8
+    would be the next value after 448 but that pattern is NaN, so a value that
+    rounds past 448 saturates to it."""
+    v = np.asarray(v, dtype=np.float64)
+    out = v.copy()
+    finite = np.isfinite(v) & (v != 0.0)
+    vf = v[finite]
+    _, E = np.frexp(vf)
+    e = np.maximum(E - 1, -6)
+    quantum_exp = e - 3
+    r = np.ldexp(np.rint(np.ldexp(vf, -quantum_exp)), quantum_exp)
+    r = np.clip(r, -E4M3_MAX, E4M3_MAX)
+    r = np.where(r == 0.0, np.copysign(0.0, vf), r)
+    out[finite] = r
+    out[np.isinf(v)] = np.copysign(E4M3_MAX, v[np.isinf(v)])
+    return out
+
+
+def quantize_fp8_e4m3(y_stored, scale: float) -> np.ndarray:
+    """The FP8 output of the forward: the stored y times the per-tensor
+    scale, multiplied in fp32 (the precision the kernel takes the decision
+    in), then rounded to E4M3 with saturation. The scale is the caller's
+    (delayed scaling: typically 448 / the amax of an earlier step)."""
+    prod = round_to_format(np.asarray(y_stored, dtype=np.float64) *
+                           float(np.float32(scale)), "f32")
+    return round_to_e4m3_satfinite(prod)
+
+
 def _weight(gamma: np.ndarray, zero_centered_gamma: bool) -> np.ndarray:
     """w = ln_weight, or 1 + ln_weight for zero-centered gamma (Fuser 1660)."""
     gamma = np.asarray(gamma, dtype=np.float64)

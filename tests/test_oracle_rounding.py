@@ -118,3 +118,66 @@ def test_round_f64_is_identity_and_keeps_nan():
     out = round_to_format(v, "f64")
     assert out[0] == v[0] and np.isnan(out[1]) and out[2] == -np.inf
     assert np.isnan(round_to_format(np.array([np.nan]), "bf16")[0])
+
+
+def _all_e4m3():
+    """Every E4M3 code decoded by hand from its bit fields (NaN codes dropped)."""
+    vals, codes = [], []
+    for c in range(256):
+        sign = -1.0 if c & 0x80 else 1.0
+        e = (c >> 3) & 0xF
+        m = c & 0x7
+        if e == 0xF and m == 0x7:
+            continue                      # NaN
+        if e == 0:
+            v = sign * m * 2.0 ** -9      # subnormal
+        else:
+            v = sign * (1 + m / 8.0) * 2.0 ** (e - 7)
+        vals.append(v)
+        codes.append(c)
+    return np.array(codes), np.array(vals)
+
+
+def test_e4m3_matches_exhaustive_nearest_with_saturation():
+    from oracle import round_to_e4m3_satfinite
+    codes, vals = _all_e4m3()
+    assert vals.max() == 448.0 and vals.min() == -448.0
+    rng = np.random.default_rng(5)
+    fv = np.unique(vals)
+    idx = rng.integers(0, len(fv) - 1, size=3000)
+    lo, hi = fv[idx], fv[idx + 1]
+    probe = np.concatenate([(lo + hi) / 2, lo + rng.random(3000) * (hi - lo),
+                            [0.0, -0.0, 448.0, 449.0, 464.0, 470.0, 1e6, -1e6, 2.0 ** -10,
+                             3 * 2.0 ** -10, -2.0 ** -11]])
+    got = round_to_e4m3_satfinite(probe)
+    for x, g in zip(probe, got):
+        if abs(x) >= 448.0:
+            assert g == np.copysign(448.0, x)
+            continue
+        d = np.abs(fv - x)
+        cand = np.nonzero(d == d.min())[0]
+        if len(cand) == 1:
+            want = fv[cand[0]]
+        else:                              # tie: the code with an even mantissa
+            even = [fv[i] for i in cand
+                    if int(codes[vals == fv[i]][0]) & 1 == 0]
+            assert len(even) == 1
+            want = even[0]
+        assert g == want or (g == 0 and want == 0), (x, g, want)
+    assert np.isnan(round_to_e4m3_satfinite(np.array([np.nan]))[0])
+
+
+def test_e4m3_matches_torch_cast_in_range():
+    from oracle import round_to_e4m3_satfinite
+    rng = np.random.default_rng(6)
+    v32 = (rng.standard_normal(20000) * np.exp2(rng.integers(-12, 8, 20000))).astype(np.float32)
+    v32 = v32[np.abs(v32) < 440.0]
+    want = torch.from_numpy(v32).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(round_to_e4m3_satfinite(v32.astype(np.float64)), want)
+
+
+def test_fp8_quantize_multiplies_in_fp32():
+    from oracle import quantize_fp8_e4m3
+    y = np.array([1.0, -0.3125, 3.0, 1e3])
+    out = quantize_fp8_e4m3(y, 2.0)
+    np.testing.assert_array_equal(out, [2.0, -0.625, 6.0, 448.0])
