@@ -111,6 +111,31 @@ ln_status ln_fwd(const void* x, const void* bias, const void* residual,
                  int64_t hidden, ln_dtype dtype);
 
 /*
+ * ln_fwd_ex: ln_fwd plus an FP8 (E4M3) copy of y.
+ *
+ * NVIDIA/Fuser issue 1660 computes the amax of |y| to scale y for an FP8
+ * cast; the pages stop at the amax. This entry point also writes that cast,
+ * with a per-tensor scale the caller provides (delayed scaling: typically
+ * 448 / an amax from an earlier step). Per element:
+ *   y_fp8 = E4M3(round_fp32(y_stored * scale)), round to nearest even,
+ *   finite values beyond +-448 saturate to +-448 (no infinities in E4M3);
+ * y_stored is y rounded to dtype (what y holds), so y_fp8 is the FP8 cast of
+ * the stored y. amax is that of y_stored, as in ln_fwd.
+ *
+ * y_fp8      [rows, hidden] bytes (E4M3 codes), NULL = not written.
+ * fp8_scale  one fp32 on the device, required when y_fp8 is given.
+ * y          may be NULL when y_fp8 is given (only the FP8 copy is written).
+ * Every other argument and the errors are those of ln_fwd; y_fp8 counts as a
+ * tensor pointer for the 16-byte alignment of the vectorised path.
+ */
+ln_status ln_fwd_ex(const void* x, const void* bias, const void* residual,
+                    const void* gamma, const void* beta, float eps, ln_mode mode,
+                    int zero_centered_gamma, void* out_sum, void* y, float* mean,
+                    float* rstd, float* amax, void* y_fp8, const float* fp8_scale,
+                    cudaStream_t stream, int64_t rows, int64_t hidden,
+                    ln_dtype dtype);
+
+/*
  * ln_bwd: dx, dgamma, dbeta of the normalization given dy and the forward's
  * saved sum and statistics.
  *

@@ -22,7 +22,8 @@ from .build import LIB_PATH, build as build_library
 
 __all__ = [
     "LN_F32", "LN_BF16", "LN_F16", "LN_LAYERNORM", "LN_RMSNORM", "NormError",
-    "load_library", "build_library", "ln_fwd", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes",
+    "load_library", "build_library", "ln_fwd", "ln_fwd_ex", "ln_bwd", "ln_bwd_ex",
+    "ln_bwd_workspace_bytes",
     "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc",
     "exported_symbols",
     "fused_norm_fwd", "fused_norm_bwd", "Workspace",
@@ -66,6 +67,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.ln_fwd.argtypes = [vp, vp, vp, vp, vp, f32, ci, ci, vp, vp, vp, vp, vp, vp,
                                i64, i64, ci]
         lib.ln_fwd.restype = ci
+        lib.ln_fwd_ex.argtypes = [vp, vp, vp, vp, vp, f32, ci, ci, vp, vp, vp, vp, vp, vp, vp,
+                                  vp, i64, i64, ci]
+        lib.ln_fwd_ex.restype = ci
         lib.ln_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, ci, ci,
                                vp, sz]
         lib.ln_bwd.restype = ci
@@ -88,8 +92,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
 
 def exported_symbols() -> list[str]:
     """Names of the C entry points this binding wraps."""
-    return ["ln_fwd", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes", "ln_status_string",
-            "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc"]
+    return ["ln_fwd", "ln_fwd_ex", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes",
+            "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc"]
 
 
 def ln_status_string(status: int) -> str:
@@ -168,6 +172,21 @@ def ln_fwd(x, bias, residual, gamma, beta, eps, mode, zero_centered_gamma, out_s
                     hidden, _dtype(x))
     if st:
         raise NormError(st, "ln_fwd")
+
+
+def ln_fwd_ex(x, bias, residual, gamma, beta, eps, mode, zero_centered_gamma, out_sum, y,
+              mean, rstd, amax, y_fp8, fp8_scale, stream=None) -> None:
+    """``ln_fwd`` plus an FP8 E4M3 copy of y: ``y_fp8`` is a uint8 (or
+    torch.float8_e4m3fn) tensor shaped like x, ``fp8_scale`` a one-element fp32
+    CUDA tensor; y may be None when y_fp8 is given."""
+    lib = load_library()
+    rows, hidden = _shape(x)
+    st = lib.ln_fwd_ex(_ptr(x), _ptr(bias), _ptr(residual), _ptr(gamma), _ptr(beta),
+                       float(eps), _mode(mode), int(bool(zero_centered_gamma)), _ptr(out_sum),
+                       _ptr(y), _ptr(mean), _ptr(rstd), _ptr(amax), _ptr(y_fp8),
+                       _ptr(fp8_scale), _stream(stream), rows, hidden, _dtype(x))
+    if st:
+        raise NormError(st, "ln_fwd_ex")
 
 
 def ln_bwd_workspace_bytes(rows: int, hidden: int, dtype, mode) -> int:

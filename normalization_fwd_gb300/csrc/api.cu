@@ -171,6 +171,16 @@ ln_status ln_fwd(const void* x, const void* bias, const void* residual, const vo
                  const void* beta, float eps, ln_mode mode, int zero_centered_gamma,
                  void* out_sum, void* y, float* mean, float* rstd, float* amax,
                  cudaStream_t stream, int64_t rows, int64_t hidden, ln_dtype dtype) {
+  if (rows > 0 && y == nullptr) return LN_ERR_NULL;
+  return ln_fwd_ex(x, bias, residual, gamma, beta, eps, mode, zero_centered_gamma, out_sum, y,
+                   mean, rstd, amax, nullptr, nullptr, stream, rows, hidden, dtype);
+}
+
+ln_status ln_fwd_ex(const void* x, const void* bias, const void* residual, const void* gamma,
+                    const void* beta, float eps, ln_mode mode, int zero_centered_gamma,
+                    void* out_sum, void* y, float* mean, float* rstd, float* amax,
+                    void* y_fp8, const float* fp8_scale, cudaStream_t stream, int64_t rows,
+                    int64_t hidden, ln_dtype dtype) {
   if (dtype != LN_F32 && dtype != LN_BF16 && dtype != LN_F16) return LN_ERR_UNSUPPORTED;
   if (mode != LN_LAYERNORM && mode != LN_RMSNORM) return LN_ERR_UNSUPPORTED;
   if (rows < 0 || hidden < 1) return LN_ERR_SHAPE;
@@ -181,24 +191,29 @@ ln_status ln_fwd(const void* x, const void* bias, const void* residual, const vo
     mean = nullptr;
   }
   if (gamma == nullptr) return LN_ERR_NULL;
-  if (rows > 0 && (x == nullptr || y == nullptr)) return LN_ERR_NULL;
+  if (y_fp8 != nullptr && fp8_scale == nullptr) return LN_ERR_NULL;
+  if (rows > 0 && (x == nullptr || (y == nullptr && y_fp8 == nullptr))) return LN_ERR_NULL;
   const size_t es = elem_size(dtype);
   const void* tensors[] = {x, bias, residual, gamma, beta, out_sum, y};
   for (const void* p : tensors)
     if (!aligned(p, es)) return LN_ERR_ALIGN;
-  if (!aligned(mean, 4) || !aligned(rstd, 4) || !aligned(amax, 4)) return LN_ERR_ALIGN;
+  if (!aligned(mean, 4) || !aligned(rstd, 4) || !aligned(amax, 4) || !aligned(fp8_scale, 4))
+    return LN_ERR_ALIGN;
   bool vec = (hidden * (int64_t)es) % 16 == 0;
   for (const void* p : tensors)
     if (!aligned(p, 16)) vec = false;
+  if (!aligned(y_fp8, 16)) vec = false;
   if (hidden > max_hidden(dtype, vec)) {
     if (!vec || hidden > max_hidden(dtype, false)) return LN_ERR_SHAPE;
     vec = false;
   }
   const size_t mat = (size_t)rows * (size_t)hidden * es, vecb = (size_t)hidden * es;
+  const size_t mat8 = (size_t)rows * (size_t)hidden;
   const Range outs[] = {{out_sum, mat}, {y, mat}, {mean, (size_t)rows * 4},
-                        {rstd, (size_t)rows * 4}, {amax, amax ? 4u : 0u}};
-  const Range ins[] = {{x, mat}, {residual, mat}, {bias, vecb}, {gamma, vecb}, {beta, vecb}};
-  if (any_overlap(outs, 5, ins, 5)) return LN_ERR_INVALID;
+                        {rstd, (size_t)rows * 4}, {amax, amax ? 4u : 0u}, {y_fp8, mat8}};
+  const Range ins[] = {{x, mat}, {residual, mat}, {bias, vecb}, {gamma, vecb}, {beta, vecb},
+                       {fp8_scale, fp8_scale ? 4u : 0u}};
+  if (any_overlap(outs, 6, ins, 6)) return LN_ERR_INVALID;
 
   if (amax) {
     cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
@@ -217,6 +232,8 @@ ln_status ln_fwd(const void* x, const void* bias, const void* residual, const vo
   a.mean = mean;
   a.rstd = rstd;
   a.amax = reinterpret_cast<unsigned*>(amax);
+  a.y_fp8 = static_cast<unsigned char*>(y_fp8);
+  a.fp8_scale = y_fp8 ? fp8_scale : nullptr;
   a.rows = rows;
   a.hidden = (int)hidden;
   a.eps = eps;

@@ -24,6 +24,22 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
 constexpr unsigned kErrWaitTimeout = 1u;
 static __device__ unsigned g_tu_error;
 
+// Read and clear this translation unit's device error word, after `st`.
+static inline cudaError_t take_tu_error(cudaStream_t st, unsigned* out) {
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_tu_error, sizeof(v), 0,
+                                            cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return e;
+  if (v) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_tu_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  }
+  *out |= v;
+  return e;
+}
+
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -91,6 +107,23 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// An L2 policy that evicts the lines it touches first (data read once).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// bulk_load with an L2 cache policy.
+__device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes,
+                                               uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // 16-byte loads from shared memory, always as ld.shared (a generic load of
 // a shared address would take the slower L1TEX path). Volatile, so they stay
 // after the barrier waits (volatile asm keeps its order) and are never merged
@@ -109,6 +142,22 @@ __device__ __forceinline__ float4 ld_f4_smem(const float* p) {
                : "r"(smem_addr(p)));
   return v;
 }
+// The same from a 32-bit shared address (row bases are converted once and
+// the per-slot offsets are constants the assembler folds into the load).
+__device__ __forceinline__ uint4 lds_u4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 lds_f4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a));
+  return v;
+}
 
 // A [hidden] parameter row (gamma with the zero-centered +1 folded in, bias,
 // beta) as fp32, read by 16-byte vector slot v. Staged rows live in shared
@@ -124,6 +173,9 @@ struct ParamRow {
   int hidden;
   bool plus_one;       // add 1 to values read from global (zero-centered gamma)
 
+  // 32-bit shared address of the staged row (valid when s is not null).
+  __device__ __forceinline__ uint32_t saddr() const { return smem_addr(s); }
+
   static __device__ __forceinline__ int staged_index(int i, int hidden) {
     constexpr int VEC = Vec<T>::N;
     if (VEC == 4) return i;
@@ -131,16 +183,16 @@ struct ParamRow {
     return (e < 4 ? 0 : hidden / 2) + v * 4 + (e & 3);
   }
 
-  // The same values as fp32 pairs.
+  // The same values as fp32 pairs; `sa` is saddr() (hoisted by the caller).
   template <bool kStaged>
-  __device__ __forceinline__ void load2(int v, float2* out) const {
+  __device__ __forceinline__ void load2(int v, float2* out, uint32_t sa = 0) const {
     constexpr int VEC = Vec<T>::N;
     if (kStaged) {
-      const float4 a = ld_f4_smem(s + v * 4);
+      const float4 a = lds_f4(sa + v * 16);
       out[0] = make_float2(a.x, a.y);
       out[1] = make_float2(a.z, a.w);
       if (VEC == 8) {
-        const float4 b = ld_f4_smem(s + hidden / 2 + v * 4);
+        const float4 b = lds_f4(sa + hidden * 2 + v * 16);
         out[2] = make_float2(b.x, b.y);
         out[3] = make_float2(b.z, b.w);
       }
@@ -196,13 +248,15 @@ struct Ring {
   uint64_t* empty;
   unsigned* released;     // warps that released the slot in its current round
   long long* issued;      // tiles issued so far (for the drain after an abort)
+  int* abort_now;         // set by a thread whose wait timed out (CTA-wide loops)
   unsigned char* after;   // first byte after the ring
   __device__ unsigned char* slot(int s) const { return base + (size_t)s * slot_bytes; }
 };
 
 // Bytes of the ring's bookkeeping after its slots (host and device agree).
 __host__ __device__ constexpr size_t ring_aux_bytes(int stages) {
-  return ((size_t)stages * (2 * sizeof(uint64_t) + sizeof(unsigned)) + sizeof(long long) + 15) &
+  return ((size_t)stages * (2 * sizeof(uint64_t) + sizeof(unsigned)) + sizeof(long long) +
+          sizeof(int) + 15) &
          ~(size_t)15;
 }
 
@@ -215,6 +269,7 @@ __device__ __forceinline__ Ring make_ring(unsigned char* smem, uint32_t slot_byt
   r.empty = r.full + stages;
   r.issued = reinterpret_cast<long long*>(r.empty + stages);
   r.released = reinterpret_cast<unsigned*>(r.issued + 1);
+  r.abort_now = reinterpret_cast<int*>(r.released + stages);
   r.after = smem + (size_t)stages * slot_bytes + ring_aux_bytes(stages);
   return r;
 }
@@ -228,6 +283,7 @@ __device__ __forceinline__ void ring_init(const Ring& r) {
       r.released[s] = 0;
     }
     *r.issued = 0;
+    *r.abort_now = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -246,7 +302,7 @@ __device__ __forceinline__ void ring_drain(const Ring& r, int64_t taken, int64_t
 // it * gridDim.x): for each input (up to two) the tile's rows are one
 // contiguous bulk copy, the inputs back to back in the slot. Waits (bounded)
 // for the slot to be free; false on timeout. Thread 0 only.
-template <typename T>
+template <typename T, bool kEvictFirst = false>
 __device__ __forceinline__ bool issue_tile(const Ring& ring, const BulkCfg& c, int64_t it,
                                            int64_t rows, int hidden, const T* in0,
                                            const T* in1) {
@@ -260,16 +316,25 @@ __device__ __forceinline__ bool issue_tile(const Ring& ring, const BulkCfg& c, i
   const uint32_t bytes = (uint32_t)n * row_bytes;
   mbar_arrive_expect_tx(&ring.full[s], in1 ? 2 * bytes : bytes);
   unsigned char* dst = ring.slot(s);
-  bulk_load(dst, in0 + r0 * hidden, bytes, &ring.full[s]);
-  if (in1) bulk_load(dst + (size_t)c.tile_rows * row_bytes, in1 + r0 * hidden, bytes, &ring.full[s]);
+  unsigned char* dst1 = dst + (size_t)c.tile_rows * row_bytes;
+  if (kEvictFirst) {
+    const uint64_t pol = l2_evict_first_policy();
+    bulk_load_hint(dst, in0 + r0 * hidden, bytes, &ring.full[s], pol);
+    if (in1) bulk_load_hint(dst1, in1 + r0 * hidden, bytes, &ring.full[s], pol);
+  } else {
+    bulk_load(dst, in0 + r0 * hidden, bytes, &ring.full[s]);
+    if (in1) bulk_load(dst1, in1 + r0 * hidden, bytes, &ring.full[s]);
+  }
   return true;
 }
 
 // The pipeline loop: `body(tile, slot)` for each of the CTA's tiles in order.
-// With kUniform (bodies with CTA-wide barriers) all threads agree on an
-// abort before anyone leaves the loop. Returns the tiles consumed; `aborted`
-// is set when a wait timed out.
-template <bool kUniform, typename T, typename Body>
+// With kUniform (bodies with CTA-wide barriers) a thread whose wait timed out
+// raises a shared flag and still runs the body (on stale but in-bounds
+// shared data), so every thread reaches the body's barriers; after the body
+// all threads see the flag and leave together. Returns the tiles consumed;
+// `aborted` is set when a wait timed out.
+template <bool kUniform, typename T, bool kEvictFirst = false, typename Body>
 __device__ __forceinline__ int64_t run_pipeline(const Ring& ring, const BulkCfg& c, int64_t rows,
                                                 int hidden, const T* in0, const T* in1,
                                                 bool& aborted, Body body) {
@@ -278,7 +343,7 @@ __device__ __forceinline__ int64_t run_pipeline(const Ring& ring, const BulkCfg&
   if (threadIdx.x == 0) {
     int64_t j = 0;
     for (; j < S && j < n_local; ++j) {
-      if (!issue_tile<T>(ring, c, j, rows, hidden, in0, in1)) {
+      if (!issue_tile<T, kEvictFirst>(ring, c, j, rows, hidden, in0, in1)) {
         aborted = true;
         break;
       }
@@ -289,13 +354,18 @@ __device__ __forceinline__ int64_t run_pipeline(const Ring& ring, const BulkCfg&
   int64_t it = 0;
   for (; it < n_local; ++it) {
     const int s = (int)(it % S);
-    int failed = !mbar_wait(&ring.full[s], (uint32_t)((it / S) & 1));
-    if (kUniform) failed = __syncthreads_or(failed);
-    if (failed) {
+    const bool failed = !mbar_wait(&ring.full[s], (uint32_t)((it / S) & 1));
+    if (kUniform) {
+      if (failed) *(volatile int*)ring.abort_now = 1;
+    } else if (failed) {
       aborted = true;
       break;
     }
     body(blockIdx.x + it * gridDim.x, ring.slot(s));
+    if (kUniform && *(volatile int*)ring.abort_now) {   // seen by all after the body's barrier
+      aborted = true;   // this tile is not counted as taken: the drain waits for its copy
+      break;
+    }
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
       mbar_arrive(&ring.empty[s]);
@@ -304,7 +374,7 @@ __device__ __forceinline__ int64_t run_pipeline(const Ring& ring, const BulkCfg&
         atomicExch(&ring.released[s], 0u);
         const int64_t j = it + S;
         if (j < n_local) {
-          if (issue_tile<T>(ring, c, j, rows, hidden, in0, in1)) {
+          if (issue_tile<T, kEvictFirst>(ring, c, j, rows, hidden, in0, in1)) {
             atomicMax(ring.issued, (long long)(j + 1));
           } else {
             aborted = true;

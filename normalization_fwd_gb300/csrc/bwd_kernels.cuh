@@ -119,7 +119,7 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
 // row's fp32 dx into the dbias accumulators.
 template <typename T, int G, int N, bool kRms, bool kBias, bool kStaged, typename Reduce2>
 __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool row_ok, int t,
-                                             const T* dyrow, const T* xsrow, const ParamRow<T>& wr,
+                                             uint32_t dyrow, uint32_t xsrow, const ParamRow<T>& wr,
                                              float mean, float rstd, Reduce2 reduce2,
                                              float2 (&acc_g)[N][Vec<T>::N / 2],
                                              float2 (&acc_b)[N][Vec<T>::N / 2],
@@ -130,15 +130,16 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
   const int V = H / VEC;
   const float2 neg_mean = splat2(-mean);
   const float2 r2 = splat2(rstd);
+  const uint32_t wa = kStaged ? wr.saddr() : 0u;
   float2 sx = splat2(0.f), sy = splat2(0.f);
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
     if (row_ok && v < V) {
       float2 d[P], xv[P], w[P];
-      unpack2<T>(ld_vec_smem(dyrow + v * VEC), d);
-      unpack2<T>(ld_vec_smem(xsrow + v * VEC), xv);
-      wr.template load2<kStaged>(v, w);
+      unpack2<T>(lds_u4(dyrow + v * 16), d);
+      unpack2<T>(lds_u4(xsrow + v * 16), xv);
+      wr.template load2<kStaged>(v, w, wa);
 #pragma unroll
       for (int i = 0; i < P; ++i) {
         const float2 xh = mul2(kRms ? xv[i] : add2(xv[i], neg_mean), r2);
@@ -163,9 +164,9 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
     const int v = k * G + t;
     if (row_ok && v < V) {
       float2 d[P], xv[P], w[P], o[P];
-      unpack2<T>(ld_vec_smem(dyrow + v * VEC), d);
-      unpack2<T>(ld_vec_smem(xsrow + v * VEC), xv);
-      wr.template load2<kStaged>(v, w);
+      unpack2<T>(lds_u4(dyrow + v * 16), d);
+      unpack2<T>(lds_u4(xsrow + v * 16), xv);
+      wr.template load2<kStaged>(v, w, wa);
 #pragma unroll
       for (int i = 0; i < P; ++i) {
         const float2 xm = kRms ? xv[i] : add2(xv[i], neg_mean);
@@ -399,8 +400,8 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
         const float mean = nm, rstd = nr;
         load_stats(tile + gridDim.x, nm, nr);
         const int64_t row = tile * c.tile_rows + local;
-        const T* dys = reinterpret_cast<const T*>(slot) + (size_t)local * H;
-        const T* xss = reinterpret_cast<const T*>(slot + in_bytes) + (size_t)local * H;
+        const uint32_t dys = smem_addr(slot) + (uint32_t)(local * H * sizeof(T));
+        const uint32_t xss = dys + in_bytes;
         bwd_row_smem<T, LANES, N, kRms, kBias, true>(
             a, row, row < a.rows, l, dys, xss, wr, mean, rstd,
             [](float2 v) { return group_sum2<LANES>(v); }, acc_g, acc_b, acc_d);
@@ -414,10 +415,10 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
 }
 
 template <typename T, int N, bool kRms, bool kBias>
-__global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_cta_kernel(const BwdArgs a,
-                                                                        const BulkCfg c) {
+__global__ void __launch_bounds__(kBulkThreads, (kRms && !kBias && N <= 4) ? 3 : 2)
+    bwd_bulk_cta_kernel(const BwdArgs a, const BulkCfg c) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ float2 red[kConsumerWarps];
+  __shared__ float2 red[2][kConsumerWarps];
   __shared__ int s_abort;
   __shared__ long long s_taken;
   const int H = a.hidden;
@@ -445,16 +446,18 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_cta_kernel(const Bwd
   float nm, nr;
   load_stats(blockIdx.x, nm, nr);
   bool aborted = false;
+  int parity = 0;
   const int64_t taken = run_pipeline<true, T>(
       ring, c, a.rows, H, static_cast<const T*>(a.dy), static_cast<const T*>(a.x_sum), aborted,
       [&](int64_t row, unsigned char* slot) {
         const float mean = nm, rstd = nr;
         load_stats(row + gridDim.x, nm, nr);
-        const T* dys = reinterpret_cast<const T*>(slot);
-        const T* xss = reinterpret_cast<const T*>(slot + in_bytes);
+        const uint32_t dys = smem_addr(slot);
+        const uint32_t xss = dys + in_bytes;
         bwd_row_smem<T, kBulkThreads, N, kRms, kBias, false>(
             a, row, true, threadIdx.x, dys, xss, wr, mean, rstd,
-            [&](float2 v) { return cta_sum2<kBulkThreads>(v, red); }, acc_g, acc_b, acc_d);
+            [&](float2 v) { return cta_sum2_db<kBulkThreads>(v, red, parity); }, acc_g, acc_b,
+            acc_d);
       });
   if (pipeline_finish(ring, aborted, taken, &s_abort, &s_taken)) return;
   float fg[N][Vec<T>::N], fb[N][Vec<T>::N], fd[N][Vec<T>::N];

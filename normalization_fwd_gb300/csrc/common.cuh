@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace nf {
@@ -36,6 +37,8 @@ struct FwdArgs {
   float* mean;           // nullable (always null for RMSNorm)
   float* rstd;           // nullable
   unsigned* amax;        // nullable; fp32 bit pattern, zeroed before launch
+  unsigned char* y_fp8;  // nullable; E4M3 codes of y * fp8_scale
+  const float* fp8_scale;  // device scalar, required with y_fp8
   int64_t rows;
   int hidden;
   float eps;
@@ -61,6 +64,14 @@ struct BwdArgs {
   int zero_centered;
   int has_dbias;         // also accumulate dbias = sum over rows of dx
   int ws_cols;
+};
+
+// Arguments of the row softmax kernels.
+struct SmxArgs {
+  const void* x;
+  void* y;               // may equal x (in place); no other overlap
+  int64_t rows;
+  int hidden;
 };
 
 // Launch parameters of the pipelined (bulk-copy) kernels.
@@ -206,6 +217,30 @@ template <> __device__ __forceinline__ uint4 pack2<f16>(const float2* f) {
   return make_uint4(f2_to_f16x2(f[0]), f2_to_f16x2(f[1]), f2_to_f16x2(f[2]), f2_to_f16x2(f[3]));
 }
 
+// FP8 E4M3 codes of VEC fp32 values times `scale` (fp32 product, round to
+// nearest even, finite values saturate to +-448): VEC bytes at `dst`.
+__device__ __forceinline__ unsigned short fp8x2(float2 v, float2 scale) {
+  return __nv_cvt_float2_to_fp8x2(__fmul2_rn(v, scale), __NV_SATFINITE, __NV_E4M3);
+}
+template <int VEC>
+__device__ __forceinline__ void store_fp8(unsigned char* dst, const float2* v, float scale);
+template <>
+__device__ __forceinline__ void store_fp8<8>(unsigned char* dst, const float2* v, float scale) {
+  const float2 s2 = make_float2(scale, scale);
+  const uint2 q = make_uint2((unsigned)fp8x2(v[0], s2) | ((unsigned)fp8x2(v[1], s2) << 16),
+                             (unsigned)fp8x2(v[2], s2) | ((unsigned)fp8x2(v[3], s2) << 16));
+  *reinterpret_cast<uint2*>(dst) = q;
+}
+template <>
+__device__ __forceinline__ void store_fp8<4>(unsigned char* dst, const float2* v, float scale) {
+  const float2 s2 = make_float2(scale, scale);
+  *reinterpret_cast<unsigned*>(dst) = (unsigned)fp8x2(v[0], s2) | ((unsigned)fp8x2(v[1], s2) << 16);
+}
+// One value (scalar kernels).
+__device__ __forceinline__ unsigned char fp8_one(float v, float scale) {
+  return (unsigned char)(fp8x2(make_float2(v, 0.f), make_float2(scale, 1.f)) & 0xffu);
+}
+
 // Running amax over stored 16-byte vectors. For 16-bit types the
 // accumulator holds two halves (|y| bit patterns compared as unsigned 16-bit
 // lanes, which orders non-negative bf16/fp16 values like the values and lets
@@ -256,6 +291,14 @@ template <int LANES> __device__ __forceinline__ float2 group_sum2(float2 v) {
   return v;
 }
 
+// Butterfly max over aligned groups of LANES lanes (fmaxf: a NaN operand
+// loses to a number, so a NaN in a row is caught later by exp(x - m) instead).
+template <int LANES> __device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+  for (int o = LANES / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
 // Sum over the CTA, same fixed order in every thread; returns the total to
 // all threads. `red` holds one float per warp. Two barriers: the second one
 // lets the caller reuse `red` right away.
@@ -279,6 +322,52 @@ template <int THREADS> __device__ __forceinline__ float2 cta_sum2(float2 v, floa
 #pragma unroll
   for (int i = 0; i < W; ++i) { t.x += red[i].x; t.y += red[i].y; }
   __syncthreads();
+  return t;
+}
+
+// The same sums with one barrier: `red` holds two buffers of one entry per
+// warp and `parity` picks the buffer, flipping each call. A warp can write a
+// buffer again only after the barrier of the call in between, which every
+// warp reaches after it has read the buffer, so no second barrier is needed.
+template <int THREADS>
+__device__ __forceinline__ float cta_sum_db(float v, float (*red)[THREADS / 32], int& parity) {
+  constexpr int W = THREADS / 32;
+  v = group_sum<32>(v);
+  if ((threadIdx.x & 31) == 0) red[parity][threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < W; ++i) t += red[parity][i];
+  parity ^= 1;
+  return t;
+}
+template <int THREADS>
+__device__ __forceinline__ float2 cta_sum2_db(float2 v, float2 (*red)[THREADS / 32], int& parity) {
+  constexpr int W = THREADS / 32;
+  v = group_sum2<32>(v);
+  if ((threadIdx.x & 31) == 0) red[parity][threadIdx.x >> 5] = v;
+  __syncthreads();
+  float2 t = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < W; ++i) {
+    t.x += red[parity][i].x;
+    t.y += red[parity][i].y;
+  }
+  parity ^= 1;
+  return t;
+}
+
+// Max over the CTA with one barrier (double buffer and parity as above).
+template <int THREADS>
+__device__ __forceinline__ float cta_max_db(float v, float (*red)[THREADS / 32], int& parity) {
+  constexpr int W = THREADS / 32;
+  v = group_max<32>(v);
+  if ((threadIdx.x & 31) == 0) red[parity][threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = red[parity][0];
+#pragma unroll
+  for (int i = 1; i < W; ++i) t = fmaxf(t, red[parity][i]);
+  parity ^= 1;
   return t;
 }
 

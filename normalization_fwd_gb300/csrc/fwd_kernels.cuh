@@ -141,8 +141,13 @@ __device__ __forceinline__ void fwd_row(const FwdArgs& a, int64_t row, bool row_
         o[e] = fmaf(s[k][e] * rstd, we, b[e]);
       }
       const uint4 packed = pack<T>(o);
-      st_vec(y + v * VEC, packed);
+      if (a.y) st_vec(y + v * VEC, packed);
       if (a.amax) amax_update<T>(amax_acc, packed);
+      if (a.y_fp8) {           // FP8 of the stored (rounded) y
+        float2 yr[VEC / 2];
+        unpack2<T>(packed, yr);
+        store_fp8<VEC>(a.y_fp8 + off + v * VEC, yr, *a.fp8_scale);
+      }
     }
   }
 }
@@ -200,6 +205,7 @@ __global__ void __launch_bounds__(THREADS) fwd_cta_kernel(const FwdArgs a) {
 template <typename T>
 struct FwdParams {
   ParamRow<T> w, bias, beta;
+  float fp8_scale;     // loaded once per CTA when y_fp8 is written
 };
 
 template <typename T>
@@ -208,6 +214,7 @@ __device__ __forceinline__ FwdParams<T> fwd_params(const FwdArgs& a, float* p_s)
   const T* bias = static_cast<const T*>(a.bias);
   const T* beta = static_cast<const T*>(a.beta);
   FwdParams<T> p;
+  p.fp8_scale = a.y_fp8 ? *a.fp8_scale : 0.f;
   p.w = {p_s, static_cast<const T*>(a.gamma), H, a.zero_centered != 0};
   p.bias = {p_s && bias ? p_s + H : nullptr, bias, H, false};
   p.beta = {p_s && beta ? p_s + (bias ? 2 : 1) * H : nullptr, beta, H, false};
@@ -225,14 +232,18 @@ __device__ __forceinline__ FwdParams<T> fwd_params(const FwdArgs& a, float* p_s)
 // from global memory. Values are kept as fp32 pairs (packed fp32 math).
 template <typename T, int G, int N, bool kStaged, typename Reduce>
 __device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool row_ok, int t,
-                                             const T* xrow, const T* rrow, const FwdParams<T>& p,
-                                             Reduce reduce, unsigned& amax_acc, bool write_stats) {
+                                             uint32_t xrow, uint32_t rrow, bool has_res,
+                                             const FwdParams<T>& p, Reduce reduce,
+                                             unsigned& amax_acc, bool write_stats) {
   constexpr int VEC = Vec<T>::N;
   constexpr int P = VEC / 2;
   const int H = a.hidden;
   const int V = H / VEC;
   T* sum_row = a.out_sum ? static_cast<T*>(a.out_sum) + row * (int64_t)H : nullptr;
   T* y_row = static_cast<T*>(a.y) + row * (int64_t)H;
+  const uint32_t wa = kStaged ? p.w.saddr() : 0u;
+  const uint32_t ba = (kStaged && p.beta.g) ? p.beta.saddr() : 0u;
+  const uint32_t bia = (kStaged && p.bias.g) ? p.bias.saddr() : 0u;
 
   // F1: s = (x + bias) + residual in fp32, stored rounded; the statistics
   // see the stored value.
@@ -244,16 +255,16 @@ __device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool
 #pragma unroll
     for (int i = 0; i < P; ++i) s[k][i] = splat2(0.f);
     if (row_ok && v < V) {
-      unpack2<T>(ld_vec_smem(xrow + v * VEC), s[k]);
+      unpack2<T>(lds_u4(xrow + v * 16), s[k]);
       if (p.bias.g) {
         float2 b[P];
-        p.bias.template load2<kStaged>(v, b);
+        p.bias.template load2<kStaged>(v, b, bia);
 #pragma unroll
         for (int i = 0; i < P; ++i) s[k][i] = add2(s[k][i], b[i]);
       }
-      if (rrow) {
+      if (has_res) {
         float2 r[P];
-        unpack2<T>(ld_vec_smem(rrow + v * VEC), r);
+        unpack2<T>(lds_u4(rrow + v * 16), r);
 #pragma unroll
         for (int i = 0; i < P; ++i) s[k][i] = add2(s[k][i], r[i]);
       }
@@ -292,9 +303,9 @@ __device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool
     const int v = k * G + t;
     if (row_ok && v < V) {
       float2 w[P], o[P];
-      p.w.template load2<kStaged>(v, w);
+      p.w.template load2<kStaged>(v, w, wa);
       if (p.beta.g) {
-        p.beta.template load2<kStaged>(v, o);
+        p.beta.template load2<kStaged>(v, o, ba);
       } else {
 #pragma unroll
         for (int i = 0; i < P; ++i) o[i] = splat2(0.f);
@@ -302,8 +313,12 @@ __device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool
 #pragma unroll
       for (int i = 0; i < P; ++i) o[i] = fma2(mul2(s[k][i], r2), w[i], o[i]);
       const uint4 packed = pack2<T>(o);
-      st_vec(y_row + v * VEC, packed);
+      if (a.y) st_vec(y_row + v * VEC, packed);
       if (a.amax) amax_update<T>(amax_acc, packed);
+      if (a.y_fp8) {           // FP8 of the stored (rounded) y
+        unpack2<T>(packed, o);
+        store_fp8<VEC>(a.y_fp8 + row * (int64_t)H + v * VEC, o, p.fp8_scale);
+      }
     }
   }
 }
@@ -336,10 +351,9 @@ __global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 3 : 2) fwd_bulk_warp_ke
       ring, c, a.rows, H, static_cast<const T*>(a.x), static_cast<const T*>(a.residual), aborted,
       [&](int64_t tile, unsigned char* slot) {
         const int64_t row = tile * c.tile_rows + local;
-        const T* xs = reinterpret_cast<const T*>(slot) + (size_t)local * H;
-        const T* rs = a.residual ? reinterpret_cast<const T*>(slot + in_bytes) + (size_t)local * H
-                                 : nullptr;
-        fwd_row_smem<T, LANES, N, true>(a, row, row < a.rows, l, xs, rs, p,
+        const uint32_t xs = smem_addr(slot) + (uint32_t)(local * H * sizeof(T));
+        fwd_row_smem<T, LANES, N, true>(a, row, row < a.rows, l, xs, xs + in_bytes,
+                                        a.residual != nullptr, p,
                                   [](float v) { return group_sum<LANES>(v); }, amax_acc, l == 0);
       });
   if (pipeline_finish(ring, aborted, taken, &s_abort, &s_taken)) return;
@@ -350,7 +364,7 @@ template <typename T, int N>
 __global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_cta_kernel(const FwdArgs a,
                                                                         const BulkCfg c) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ float red[kConsumerWarps];
+  __shared__ float red[2][kConsumerWarps];
   __shared__ unsigned red_amax[kConsumerWarps];
   __shared__ int s_abort;
   __shared__ long long s_taken;
@@ -367,13 +381,14 @@ __global__ void __launch_bounds__(kBulkThreads, 2) fwd_bulk_cta_kernel(const Fwd
 
   bool aborted = false;
   unsigned amax_acc = 0;
+  int parity = 0;
   const int64_t taken = run_pipeline<true, T>(
       ring, c, a.rows, H, static_cast<const T*>(a.x), static_cast<const T*>(a.residual), aborted,
       [&](int64_t row, unsigned char* slot) {
-        const T* xs = reinterpret_cast<const T*>(slot);
-        const T* rs = a.residual ? reinterpret_cast<const T*>(slot + in_bytes) : nullptr;
-        fwd_row_smem<T, kBulkThreads, N, false>(a, row, true, threadIdx.x, xs, rs, p,
-                                         [&](float v) { return cta_sum<kBulkThreads>(v, red); },
+        const uint32_t xs = smem_addr(slot);
+        fwd_row_smem<T, kBulkThreads, N, false>(a, row, true, threadIdx.x, xs, xs + in_bytes,
+                                                a.residual != nullptr, p,
+                                         [&](float v) { return cta_sum_db<kBulkThreads>(v, red, parity); },
                                          amax_acc, threadIdx.x == 0);
       });
   if (pipeline_finish(ring, aborted, taken, &s_abort, &s_taken)) return;
@@ -427,8 +442,9 @@ __global__ void __launch_bounds__(kScalarCta) fwd_scalar_kernel(const FwdArgs a)
       const float w = a.zero_centered ? 1.0f + to_f(gamma[j]) : to_f(gamma[j]);
       const float b = beta ? to_f(beta[j]) : 0.f;
       const T o = from_f<T>(fmaf((srow[j] - mean) * rstd, w, b));
-      y[off + j] = o;
+      if (y) y[off + j] = o;
       amax_u = max(amax_u, abs_bits(to_f(o)));
+      if (a.y_fp8) a.y_fp8[off + j] = fp8_one(to_f(o), *a.fp8_scale);
     }
   }
   if (a.amax) cta_amax_commit(amax_u, a.amax, red_amax);

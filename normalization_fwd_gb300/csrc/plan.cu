@@ -85,12 +85,15 @@ inline size_t ring_target_kb_env(const char* name) {
   const long v = strtol(e, nullptr, 10);
   return (v >= 16 && v <= 200) ? (size_t)v * 1024 : 0;
 }
-inline size_t ring_target(bool bwd, bool fwd_group) {
+// three_ctas: kernels built for three CTAs per SM (the lane-group forward)
+// get the smaller ring. (For the CTA-per-row RMSNorm backward, 2 CTAs with
+// 3 slots measured 167 us at 16384 x 8192 against 176 us for 3 CTAs with 2.)
+inline size_t ring_target(bool bwd, bool three_ctas) {
   static const size_t fwd_env = ring_target_kb_env("NORMFUSE_RING_KB_FWD");
   static const size_t bwd_env = ring_target_kb_env("NORMFUSE_RING_KB_BWD");
-  if (bwd) return bwd_env ? bwd_env : kRingTarget;
-  if (fwd_env) return fwd_env;
-  return fwd_group ? kRingTargetFwdGroup : kRingTarget;
+  if (bwd && bwd_env) return bwd_env;
+  if (!bwd && fwd_env) return fwd_env;
+  return three_ctas ? kRingTargetFwdGroup : kRingTarget;
 }
 
 // Fill in a pipelined plan; false when the ring does not fit. `extra`:
@@ -171,7 +174,8 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
     // Lane-group kernels stage the parameter rows in shared memory as fp32;
     // CTA-per-row kernels read them from global memory.
     const size_t extra = b.kind == 0 ? (size_t)n_params * hidden * sizeof(float) : 0;
-    const size_t target = ring_target(bwd, b.kind == 0 && b.n <= 4);
+    const bool three = !bwd && b.kind == 0 && b.n <= 4;
+    const size_t target = ring_target(bwd, three);
     if (fill_bulk(p, b, rows, hidden, sizeof(T), n_in, extra, target)) {
       p->fn = bwd ? Tables<T>::bwd_bulk(b.kind, b.group, b.n, rms, dbias)
                   : Tables<T>::fwd_bulk(b.kind, b.group, b.n);

@@ -112,20 +112,4 @@ template <typename T> const void* bwd_reg_table_impl(int kind, int group, int n)
   return nullptr;
 }
 
-// Read and clear this translation unit's device error word, after `st`.
-static inline cudaError_t take_tu_error(cudaStream_t st, unsigned* out) {
-  unsigned v = 0;
-  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_tu_error, sizeof(v), 0,
-                                            cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  if (e != cudaSuccess) return e;
-  if (v) {
-    const unsigned zero = 0;
-    e = cudaMemcpyToSymbolAsync(g_tu_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  }
-  *out |= v;
-  return e;
-}
-
 }  // namespace nf

@@ -35,8 +35,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
-        ["ln_fwd", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes", "ln_status_string",
-         "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc"])
+        ["ln_fwd", "ln_fwd_ex", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes",
+         "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -119,6 +119,24 @@ def bwd(lib, dy=X, xs=RES, gamma=G, mean=M, rstd=R, dx=Y, dg=S, db=B, rows=4, hi
 ])
 def test_bwd_rejects_on_host(lib, kw, want):
     assert bwd(lib, **kw) == want
+
+
+def test_fwd_ex_validates_fp8_on_host(lib):
+    F8, SC = 0x7f0000000000 + 12 * 0x10000000, 0x7f0000000000 + 13 * 0x10000000
+
+    def call(y_fp8=F8, scale=SC, **kw):
+        a = dict(x=X, bias=BIAS, residual=RES, gamma=G, beta=B, out_sum=S, y=Y, mean=M, rstd=R,
+                 amax=A, rows=4, hidden=384, dtype=1)
+        a.update(kw)
+        return lib.ln_fwd_ex(a["x"], a["bias"], a["residual"], a["gamma"], a["beta"], 1e-5, 0, 0,
+                             a["out_sum"], a["y"], a["mean"], a["rstd"], a["amax"], y_fp8, scale,
+                             None, a["rows"], a["hidden"], a["dtype"])
+    assert call(scale=None) == NULL            # a scale is required with y_fp8
+    assert call(y_fp8=None, y=None) == NULL    # some output is required
+    assert call(scale=SC + 2) == ALIGN
+    assert call(y_fp8=X + 16) == INVALID       # overlaps x
+    assert call(y_fp8=Y + 128) == INVALID      # overlaps y
+    assert call(y_fp8=M) == INVALID            # overlaps mean
 
 
 def test_bwd_ex_validates_dbias_on_host(lib):
