@@ -8,6 +8,9 @@ so no flush is needed between steps.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--no-e2e] [--no-cpu-baseline] [--no-clocks]
 
+``--workload softmax_bf16_576000x384`` (or ``softmax_bf16_16384x8192``) times
+the row softmax (ln_softmax_fwd) instead, with its own metric line.
+
 Rank 0 prints one JSON line. Under torchrun (N > 1) every rank runs its own
 replica of the workload on its own GPU (the block has no cross-row exchange),
 timing is bracketed by barriers and the max over ranks is reported.
@@ -39,6 +42,13 @@ METRIC = "fwd+bwd rows/s and achieved HBM GB/s vs ~8 TB/s peak at (576000×384) 
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 BENCH_WORKLOADS = {w.name: w for w in (W.BENCH_LN_BF16_576000x384, W.BENCH_RMS_BF16_16384x8192)}
+# The row softmax is measured on its own workloads (its own metric line).
+SOFTMAX_METRIC = "softmax rows/s and achieved HBM GB/s (one read of x, one write of y)"
+SOFTMAX_WORKLOADS = {w.name: w for w in (W.SMX_BF16_576000x384, W.SMX_BF16_16384x8192)}
+
+
+def is_softmax(w) -> bool:
+    return isinstance(w, W.SoftmaxWorkload)
 
 
 # ---------------------------------------------------------------- bytes model
@@ -65,6 +75,11 @@ def bwd_bytes(w) -> int:
     nstats = 2 if w.mode == W.LAYERNORM else 1
     ngrads = 2 if w.mode == W.LAYERNORM else 1
     return 3 * R * H * e + R * 4 * nstats + H * e + H * 4 * ngrads
+
+
+def softmax_bytes(w) -> int:
+    """Minimal HBM bytes of one ln_softmax_fwd: x read once, y written once."""
+    return 2 * w.rows * w.hidden * elem_bytes(w)
 
 
 # ---------------------------------------------------------------- clocks
@@ -207,6 +222,10 @@ class Step:
                        self.dbeta, stream, mode=w.mode, zero_centered_gamma=w.zero_centered_gamma,
                        workspace=self.ws)
 
+    def run(self, stream):
+        self.fwd(stream)
+        self.bwd(stream)
+
     def h2d_tensors(self):
         return [(k, self.inp[k]) for k in ("x", "residual", "bias", "gamma", "beta", "dy")
                 if self.inp[k] is not None]
@@ -216,6 +235,24 @@ class Step:
                ("amax", self.amax), ("dx", self.dx), ("dgamma", self.dgamma),
                ("dbeta", self.dbeta)]
         return [(k, t) for k, t in out if t is not None]
+
+
+class SoftmaxStep:
+    """Device buffers and the C-ABI call of one row softmax step."""
+
+    def __init__(self, nf, w, x_host, device):
+        self.nf, self.w = nf, w
+        self.x = x_host.to(device)
+        self.y = torch.empty_like(self.x)
+
+    def run(self, stream):
+        self.nf.ln_softmax_fwd(self.x, self.y, stream)
+
+    def h2d_tensors(self):
+        return [("x", self.x)]
+
+    def d2h_tensors(self):
+        return [("y", self.y)]
 
 
 def max_over_ranks(value: float, world: int, device=None) -> float:
@@ -254,16 +291,29 @@ def oracle_step(w, inp, rows):
              w.zero_centered_gamma, w.dtype)
 
 
+def oracle_softmax_step(w, x, rows):
+    """One fp64 oracle softmax over the first `rows` rows."""
+    from oracle import softmax_fwd
+    softmax_fwd(W.as_f64(x[:rows]), w.dtype)
+
+
+def oracle_any_step(w, inp, rows):
+    if is_softmax(w):
+        oracle_softmax_step(w, inp, rows)
+    else:
+        oracle_step(w, inp, rows)
+
+
 def time_oracle(w, inp, budget_s: float):
     """rows/s of the oracle on a sample sized to about `budget_s` of CPU work."""
     probe = min(2048, w.rows)
     t0 = time.perf_counter()
-    oracle_step(w, inp, probe)
+    oracle_any_step(w, inp, probe)
     t_probe = time.perf_counter() - t0
     rows = int(min(w.rows, max(probe, probe * budget_s / max(t_probe, 1e-6))))
     rows = min(rows, 131072)
     t0 = time.perf_counter()
-    oracle_step(w, inp, rows)
+    oracle_any_step(w, inp, rows)
     dt = time.perf_counter() - t0
     return rows / dt, rows, dt
 
@@ -273,24 +323,27 @@ def run_reference(args, w, rank):
     """The oracle on host cores, as the reference arm."""
     if rank != 0:
         return
-    inp = W.make_inputs(w, seed=0)
+    smx = is_softmax(w)
+    inp = W.make_softmax_inputs(w, seed=0) if smx else W.make_inputs(w, seed=0)
     budget = 150.0
     probe = min(1024, w.rows)
     t0 = time.perf_counter()
-    oracle_step(w, inp, probe)
+    oracle_any_step(w, inp, probe)
     per_row = (time.perf_counter() - t0) / probe
     steps = args.steps + args.warmup
     rows = max(16, min(w.rows, int(budget / max(steps, 1) / max(per_row, 1e-9))))
     for _ in range(args.warmup):
-        oracle_step(w, inp, rows)
+        oracle_any_step(w, inp, rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(w, inp, rows)
+        oracle_any_step(w, inp, rows)
     el = time.perf_counter() - t0
     value = rows * args.steps / el
-    sample = f"first {rows} of {w.rows} rows per step, fp64 numpy oracle fwd+bwd, 1 thread"
+    what = "softmax" if smx else "fwd+bwd"
+    sample = f"first {rows} of {w.rows} rows per step, fp64 numpy oracle {what}, 1 thread"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "impl": "reference", "metric": SOFTMAX_METRIC if smx else METRIC, "value": value,
+        "unit": "rows/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * el / args.steps * (w.rows / rows), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -304,6 +357,11 @@ def run_reference(args, w, rank):
 
 
 def config_of(w, n):
+    if is_softmax(w):
+        return {"workload": w.name, "rows": w.rows, "hidden": w.hidden, "io_dtype": w.dtype,
+                "x_std": w.x_std, "mask_frac": w.mask_frac,
+                "l2": "no flush: x and y are each larger than the 129 MB L2",
+                "parallelism": "replicas" if n > 1 else "single-gpu"}
     return {"workload": w.name, "rows": w.rows, "hidden": w.hidden, "mode": w.mode,
             "io_dtype": w.dtype, "stats_dtype": "f32", "bias": w.bias_std is not None,
             "residual": w.residual_std is not None, "amax": w.amax, "eps": w.eps,
@@ -401,13 +459,88 @@ def run_ours(args, w, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-def run_e2e(nf, w, inp_host, device, steps):
-    """The same fwd + bwd step end to end from pinned host memory: every step
-    copies its inputs host -> device, runs ln_fwd and ln_bwd, and copies every
+def run_softmax(args, w, rank, world, local_rank):
+    """Time ln_softmax_fwd alone on a softmax workload (its own JSON line)."""
+    import normalization_fwd_gb300 as nf
+    nf.load_library()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    x_host = W.make_softmax_inputs(w, seed=0)
+    step = SoftmaxStep(nf, w, x_host, device)
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step.run(stream)
+    torch.cuda.synchronize(device)
+    K = args.steps
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank) if (rank == 0 and not args.no_clocks) else None
+    if sampler is not None:
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(device)
+    t_host0 = time.time()
+    start.record(stream)
+    for _ in range(K):
+        step.run(stream)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    t_host1 = time.time()
+    barrier()
+    elapsed = max_over_ranks(start.elapsed_time(end), world, device)
+    clocks = None
+    if sampler is not None:
+        time.sleep(0.25)
+        sampler.stop()
+        clocks = sampler.summary(t_host0, t_host1)
+    e2e = None
+    if not args.no_e2e:
+        del step
+        torch.cuda.empty_cache()
+        e2e = run_e2e(nf, w, x_host, device, min(args.e2e_steps, max(K, 1)),
+                      make_step=SoftmaxStep)
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    ms = elapsed / K
+    by = softmax_bytes(w)
+    gbs = by / (ms * 1e-3) / 1e9
+    kernels = {"ln_softmax_fwd": {"us": ms * 1e3, "algorithmic_bytes": by, "GBps": gbs,
+                                  f"frac_of_{peak_kind}": gbs / peak,
+                                  "frac_of_8TBps": gbs / NOMINAL_HBM_GBS,
+                                  "traffic": ncu_traffic(w.name, "ln_softmax_fwd")}}
+    roofline = {"bound": "hbm", "kernel": "ln_softmax_fwd", "achieved": gbs, "peak": peak,
+                "unit": "GB/s", "frac": gbs / peak, "peak_kind": peak_kind,
+                "traffic": kernels["ln_softmax_fwd"]["traffic"]}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        v, rows, secs = time_oracle(w, x_host, budget_s=12.0)
+        cpu = {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {rows} of {w.rows} rows, fp64 numpy oracle softmax, "
+                         f"{secs:.1f} s on 1 host thread"}
+    line = {
+        "metric": SOFTMAX_METRIC, "value": replica_throughput(w.rows, world, ms),
+        "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic", "config": config_of(w, world),
+        "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": K, "clocks": clocks, "impl": "ours",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(nf, w, inp_host, device, steps, make_step=Step):
+    """The same step end to end from pinned host memory: every step copies
+    its inputs host -> device, runs the step's C-ABI calls, and copies every
     output device -> host. Two buffer sets alternate so step i + 1's upload
     (copy stream) overlaps step i's compute (compute stream) and download
     (a third stream); each direction has its own copy engine."""
-    sets = [Step(nf, w, inp_host, device) for _ in range(2)]
+    sets = [make_step(nf, w, inp_host, device) for _ in range(2)]
     h2d = [s.h2d_tensors() for s in sets]
     d2h = [s.d2h_tensors() for s in sets]
     host_in = {k: t.detach().to("cpu").pin_memory() for k, t in h2d[0]}
@@ -427,8 +560,7 @@ def run_e2e(nf, w, inp_host, device, steps):
                 t.copy_(host_in[k], non_blocking=True)
             uploaded[b].record(up)
         comp.wait_event(uploaded[b])
-        sets[b].fwd(comp)
-        sets[b].bwd(comp)
+        sets[b].run(comp)
         computed[b].record(comp)
         down.wait_event(computed[b])
         with torch.cuda.stream(down):
@@ -460,7 +592,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS),
+    ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS) + sorted(SOFTMAX_WORKLOADS),
                     default=W.BENCH_LN_BF16_576000x384.name)
     ap.add_argument("--rows", type=int, default=None,
                     help="override the workload's row count (smaller profiling captures)")
@@ -471,7 +603,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = BENCH_WORKLOADS[args.workload]
+    w = BENCH_WORKLOADS.get(args.workload) or SOFTMAX_WORKLOADS[args.workload]
     if args.rows is not None:
         w = w.with_(rows=args.rows, name=f"{w.name}@rows={args.rows}")
 
@@ -488,7 +620,10 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
     try:
-        run_ours(args, w, rank, world, local_rank)
+        if is_softmax(w):
+            run_softmax(args, w, rank, world, local_rank)
+        else:
+            run_ours(args, w, rank, world, local_rank)
     finally:
         if world > 1:
             torch.distributed.destroy_process_group()

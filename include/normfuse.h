@@ -17,7 +17,8 @@
  *    is 16-byte aligned and hidden * sizeof(dtype) is a multiple of 16, the
  *    128-bit vectorised kernels run; otherwise a scalar kernel handles the
  *    call with the same results.
- *  - Outputs must not overlap inputs or each other.
+ *  - Outputs must not overlap inputs or each other (ln_softmax_fwd alone
+ *    also runs in place).
  *  - Work is enqueued on `stream` (0 = the legacy default stream) and the call
  *    returns without waiting for it. The library calls no allocating CUDA API,
  *    and none that synchronises except ln_device_error().
@@ -175,7 +176,8 @@ ln_status ln_bwd(const void* dy, const void* x_sum, const void* gamma,
                  size_t workspace_bytes);
 
 /*
- * ln_bwd_ex: ln_bwd plus the gradient of the forward's bias.
+ * ln_bwd_ex: ln_bwd plus the gradient of the forward's bias, and a choice
+ * of precision for the parameter gradients.
  *
  * The forward adds `bias` to every row before the norm (NVIDIA/Fuser issue
  * 1660), so dbias = sum over rows of dx, the gradient of the norm's input;
@@ -185,16 +187,23 @@ ln_status ln_bwd(const void* dy, const void* x_sum, const void* gamma,
  * same fixed-order finalize (pytorch/pytorch PR 165370's partial
  * accumulation of the outer reductions).
  *
- * dbias     [hidden] fp32, NULL = not computed (then identical to ln_bwd).
- * Every other argument, the workspace rule and the errors are those of
- * ln_bwd; ln_bwd_workspace_bytes() covers both entry points.
+ * dbias     [hidden] grad_dtype, NULL = not computed.
+ * grad_dtype  the type of dgamma, dbeta and dbias: LN_F32 (as in ln_bwd), or
+ *           LN_BF16 / LN_F16 for the low-precision epilogue PR 165370 names
+ *           (a down cast after the outer reduction): the fixed-order fp64
+ *           total of each column is rounded once, to nearest even, to that
+ *           type. dgamma/dbeta/dbias must then be aligned to its size.
+ * With dbias NULL and grad_dtype LN_F32 this is ln_bwd. Every other
+ * argument, the workspace rule and the errors are those of ln_bwd;
+ * ln_bwd_workspace_bytes() covers both entry points.
  */
 ln_status ln_bwd_ex(const void* dy, const void* x_sum, const void* gamma,
                     const float* mean, const float* rstd, void* dx,
-                    float* dgamma, float* dbeta, float* dbias,
+                    void* dgamma, void* dbeta, void* dbias,
                     cudaStream_t stream, int64_t rows, int64_t hidden,
                     ln_dtype dtype, ln_mode mode, int zero_centered_gamma,
-                    void* workspace, size_t workspace_bytes);
+                    void* workspace, size_t workspace_bytes,
+                    ln_dtype grad_dtype);
 
 /*
  * Bytes of workspace ln_bwd / ln_bwd_ex need for this shape on the current
@@ -239,6 +248,27 @@ ln_status ln_bwd_noalloc(const void* dy, const void* x_sum, const void* gamma,
                          float* dgamma, float* dbeta, cudaStream_t stream,
                          int64_t rows, int64_t hidden, ln_dtype dtype,
                          ln_mode mode, int zero_centered_gamma);
+
+/*
+ * ln_softmax_fwd: row softmax, y[r, :] = exp(x[r, :] - m_r) / s_r with
+ * m_r = max_j x[r, j] and s_r = sum_j exp(x[r, j] - m_r).
+ *
+ * Defined by iree-org/iree issue 9139 (the softmax IR: a max reduction, the
+ * exponential of the shifted row, a sum reduction and a division, fused into
+ * one dispatch). The ln_ prefix is the library's; this call has nothing to do
+ * with a normalization's parameters. Each row is read from HBM once and
+ * written once; the max, exponentials, sum and reciprocal are fp32, and y is
+ * rounded to dtype. A row that is all -inf, or holds a NaN or +inf, gives NaN
+ * in every column, as the definition does; -inf entries of an otherwise
+ * finite row give exactly 0 (masking).
+ *
+ * x, y  [rows, hidden] dtype, device, required when rows > 0. y == x (in
+ *       place) is allowed; any other overlap returns LN_ERR_INVALID.
+ * Shapes, alignment, limits, streams and errors are those of the header's
+ * conventions (no statistics or parameters are involved).
+ */
+ln_status ln_softmax_fwd(const void* x, void* y, cudaStream_t stream, int64_t rows,
+                         int64_t hidden, ln_dtype dtype);
 
 /* Static, human-readable name of a status code. */
 const char* ln_status_string(ln_status status);

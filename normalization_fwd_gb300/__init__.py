@@ -74,7 +74,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                vp, sz]
         lib.ln_bwd.restype = ci
         lib.ln_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, ci, ci,
-                                  vp, sz]
+                                  vp, sz, ci]
         lib.ln_bwd_ex.restype = ci
         lib.ln_bwd_workspace_bytes.argtypes = [i64, i64, ci, ci, ctypes.POINTER(sz)]
         lib.ln_bwd_workspace_bytes.restype = ci
@@ -86,6 +86,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.ln_device_error.restype = ci
         lib.ln_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, ci, ci]
         lib.ln_bwd_noalloc.restype = ci
+        lib.ln_softmax_fwd.argtypes = [vp, vp, vp, i64, i64, ci]
+        lib.ln_softmax_fwd.restype = ci
         _lib = lib
         return lib
 
@@ -93,7 +95,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
 def exported_symbols() -> list[str]:
     """Names of the C entry points this binding wraps."""
     return ["ln_fwd", "ln_fwd_ex", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes",
-            "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc"]
+            "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc",
+            "ln_softmax_fwd"]
 
 
 def ln_status_string(status: int) -> str:
@@ -239,8 +242,10 @@ def ln_bwd_noalloc(dy, x_sum, gamma, mean, rstd, dx, dgamma, dbeta, stream=None,
 
 def ln_bwd_ex(dy, x_sum, gamma, mean, rstd, dx, dgamma, dbeta, dbias, stream=None, *,
               mode="layernorm", zero_centered_gamma=False, workspace=None) -> None:
-    """``ln_bwd`` that also writes ``dbias`` (fp32 [hidden], the column sum of
-    dx: the gradient of the forward's bias); dbias may be None."""
+    """``ln_bwd`` that also writes ``dbias`` ([hidden], the column sum of dx:
+    the gradient of the forward's bias; may be None). dgamma, dbeta and dbias
+    share one dtype, float32, bfloat16 or float16, taken from ``dgamma``: the
+    column totals are rounded once to it."""
     lib = load_library()
     rows, hidden = _shape(dy)
     if workspace is None and rows > 0:
@@ -250,9 +255,29 @@ def ln_bwd_ex(dy, x_sum, gamma, mean, rstd, dx, dgamma, dbeta, dbias, stream=Non
     st = lib.ln_bwd_ex(_ptr(dy), _ptr(x_sum), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),
                        _ptr(dgamma), _ptr(dbeta), _ptr(dbias), _stream(stream), rows, hidden,
                        _dtype(dy), _mode(mode), int(bool(zero_centered_gamma)),
-                       _ptr(workspace), ws_bytes)
+                       _ptr(workspace), ws_bytes, _dtype(dgamma))
     if st:
         raise NormError(st, "ln_bwd_ex")
+
+
+def ln_softmax_fwd(x, y, stream=None) -> None:
+    """Enqueue the softmax over the last dimension of the contiguous CUDA
+    tensor ``x`` into ``y`` (same shape and dtype; ``y`` may be ``x`` itself)."""
+    lib = load_library()
+    rows, hidden = _shape(x)
+    if y is not x and (y.shape != x.shape or y.dtype != x.dtype):
+        raise ValueError("y must have the shape and dtype of x")
+    st = lib.ln_softmax_fwd(_ptr(x), _ptr(y), _stream(stream), rows, hidden, _dtype(x))
+    if st:
+        raise NormError(st, "ln_softmax_fwd")
+
+
+def softmax_fwd(x, *, out=None, stream=None):
+    """Softmax over the last dimension of a contiguous tensor; returns ``y``
+    (allocated with torch unless ``out`` is given)."""
+    y = torch.empty_like(x) if out is None else out
+    ln_softmax_fwd(x, y, stream)
+    return y
 
 
 class Workspace:
@@ -292,19 +317,20 @@ def fused_norm_fwd(x, gamma, beta=None, *, bias=None, residual=None, eps=1e-5,
 
 
 def fused_norm_bwd(dy, x_sum, gamma, mean, rstd, *, mode="layernorm", zero_centered_gamma=False,
-                   need_dbeta=True, need_dbias=False, workspace: Workspace | None = None,
-                   stream=None):
+                   need_dbeta=True, need_dbias=False, grad_dtype=torch.float32,
+                   workspace: Workspace | None = None, stream=None):
     """Allocate the outputs with torch and run ``ln_bwd`` (``ln_bwd_ex`` when
-    ``need_dbias``); returns dx, dgamma, dbeta, dbias."""
+    ``need_dbias`` or a ``grad_dtype`` other than float32); returns dx,
+    dgamma, dbeta, dbias."""
     rows, hidden = _shape(dy)
     rms = _mode(mode) == LN_RMSNORM
     dx = torch.empty_like(dy)
-    dgamma = torch.empty(hidden, dtype=torch.float32, device=dy.device)
-    dbeta = (torch.empty(hidden, dtype=torch.float32, device=dy.device)
-             if (need_dbeta and not rms) else None)
-    dbias = torch.empty(hidden, dtype=torch.float32, device=dy.device) if need_dbias else None
+    g = dict(dtype=grad_dtype, device=dy.device)
+    dgamma = torch.empty(hidden, **g)
+    dbeta = torch.empty(hidden, **g) if (need_dbeta and not rms) else None
+    dbias = torch.empty(hidden, **g) if need_dbias else None
     ws = workspace.get(rows, hidden, dy.dtype, mode) if workspace is not None else None
-    if need_dbias:
+    if need_dbias or grad_dtype != torch.float32:
         ln_bwd_ex(dy, x_sum, gamma, mean, rstd, dx, dgamma, dbeta, dbias, stream, mode=mode,
                   zero_centered_gamma=zero_centered_gamma, workspace=ws)
     else:

@@ -159,7 +159,8 @@ ln_status ln_device_error(cudaStream_t stream, unsigned* flags) {
       take_error_bwd_bulk_rms_f16,      take_error_bwd_bulk_ln_dbias_f32,
       take_error_bwd_bulk_ln_dbias_bf16, take_error_bwd_bulk_ln_dbias_f16,
       take_error_bwd_bulk_rms_dbias_f32, take_error_bwd_bulk_rms_dbias_bf16,
-      take_error_bwd_bulk_rms_dbias_f16};
+      take_error_bwd_bulk_rms_dbias_f16, take_error_softmax_f32,
+      take_error_softmax_bf16,          take_error_softmax_f16};
   for (auto r : readers) {
     cudaError_t e = r(stream, flags);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -260,6 +261,41 @@ static cudaError_t bwd_plan_any(ln_dtype dtype, int64_t rows, int hidden, bool r
   });
 }
 
+ln_status ln_softmax_fwd(const void* x, void* y, cudaStream_t stream, int64_t rows,
+                         int64_t hidden, ln_dtype dtype) {
+  if (dtype != LN_F32 && dtype != LN_BF16 && dtype != LN_F16) return LN_ERR_UNSUPPORTED;
+  if (rows < 0 || hidden < 1) return LN_ERR_SHAPE;
+  if (rows > 0 && (x == nullptr || y == nullptr)) return LN_ERR_NULL;
+  const size_t es = elem_size(dtype);
+  if (!aligned(x, es) || !aligned(y, es)) return LN_ERR_ALIGN;
+  bool vec = (hidden * (int64_t)es) % 16 == 0 && aligned(x, 16) && aligned(y, 16);
+  if (hidden > max_hidden(dtype, vec)) {
+    if (!vec || hidden > max_hidden(dtype, false)) return LN_ERR_SHAPE;
+    vec = false;
+  }
+  // In place (y == x) is allowed; any other overlap is not.
+  const size_t mat = (size_t)rows * (size_t)hidden * es;
+  if (x != y && overlap({x, mat}, {y, mat})) return LN_ERR_INVALID;
+  if (rows == 0) return LN_OK;
+
+  SmxArgs a;
+  a.x = x;
+  a.y = y;
+  a.rows = rows;
+  a.hidden = (int)hidden;
+  cudaError_t e = by_dtype(dtype, [&](auto t) {
+    using T = decltype(t);
+    Plan p;
+    cudaError_t r = softmax_plan<T>(rows, (int)hidden, vec, &p);
+    if (r != cudaSuccess) return r;
+    return softmax_launch(a, p, stream);
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return LN_OK;
+}
+
 ln_status ln_bwd_workspace_bytes(int64_t rows, int64_t hidden, ln_dtype dtype, ln_mode mode,
                                  size_t* bytes) {
   if (bytes == nullptr) return LN_ERR_NULL;
@@ -293,15 +329,17 @@ ln_status ln_bwd(const void* dy, const void* x_sum, const void* gamma, const flo
                  int64_t rows, int64_t hidden, ln_dtype dtype, ln_mode mode,
                  int zero_centered_gamma, void* workspace, size_t workspace_bytes) {
   return ln_bwd_ex(dy, x_sum, gamma, mean, rstd, dx, dgamma, dbeta, nullptr, stream, rows,
-                   hidden, dtype, mode, zero_centered_gamma, workspace, workspace_bytes);
+                   hidden, dtype, mode, zero_centered_gamma, workspace, workspace_bytes, LN_F32);
 }
 
 ln_status ln_bwd_ex(const void* dy, const void* x_sum, const void* gamma, const float* mean,
-                    const float* rstd, void* dx, float* dgamma, float* dbeta, float* dbias,
+                    const float* rstd, void* dx, void* dgamma, void* dbeta, void* dbias,
                     cudaStream_t stream, int64_t rows, int64_t hidden, ln_dtype dtype,
                     ln_mode mode, int zero_centered_gamma, void* workspace,
-                    size_t workspace_bytes) {
+                    size_t workspace_bytes, ln_dtype grad_dtype) {
   if (dtype != LN_F32 && dtype != LN_BF16 && dtype != LN_F16) return LN_ERR_UNSUPPORTED;
+  if (grad_dtype != LN_F32 && grad_dtype != LN_BF16 && grad_dtype != LN_F16)
+    return LN_ERR_UNSUPPORTED;
   if (mode != LN_LAYERNORM && mode != LN_RMSNORM) return LN_ERR_UNSUPPORTED;
   if (rows < 0 || hidden < 1) return LN_ERR_SHAPE;
   const bool rms = mode == LN_RMSNORM;
@@ -317,8 +355,9 @@ ln_status ln_bwd_ex(const void* dy, const void* x_sum, const void* gamma, const 
   const void* tensors[] = {dy, x_sum, gamma, dx};
   for (const void* p : tensors)
     if (!aligned(p, es)) return LN_ERR_ALIGN;
-  if (!aligned(mean, 4) || !aligned(rstd, 4) || !aligned(dgamma, 4) || !aligned(dbeta, 4) ||
-      !aligned(dbias, 4))
+  const size_t gs = elem_size(grad_dtype);
+  if (!aligned(mean, 4) || !aligned(rstd, 4) || !aligned(dgamma, gs) || !aligned(dbeta, gs) ||
+      !aligned(dbias, gs))
     return LN_ERR_ALIGN;
   bool vec = (hidden * (int64_t)es) % 16 == 0;
   for (const void* p : tensors)
@@ -328,7 +367,7 @@ ln_status ln_bwd_ex(const void* dy, const void* x_sum, const void* gamma, const 
     vec = false;
   }
   const size_t mat = (size_t)rows * (size_t)hidden * es;
-  const size_t hb = (size_t)hidden * es, h4 = (size_t)hidden * 4, r4 = (size_t)rows * 4;
+  const size_t hb = (size_t)hidden * es, h4 = (size_t)hidden * gs, r4 = (size_t)rows * 4;
   const Range outs[] = {{dx, mat}, {dgamma, h4}, {dbeta, h4}, {dbias, h4},
                         {workspace, workspace_bytes}};
   const Range ins[] = {{dy, mat}, {x_sum, mat}, {gamma, hb}, {mean, r4}, {rstd, r4}};
@@ -364,7 +403,7 @@ ln_status ln_bwd_ex(const void* dy, const void* x_sum, const void* gamma, const 
   a.ws_cols = p.ws_cols;
   e = by_dtype(dtype, [&](auto t) {
     using T = decltype(t);
-    return bwd_launch<T>(a, p, dgamma, dbeta, dbias, stream);
+    return bwd_launch<T>(a, p, dgamma, dbeta, dbias, (int)grad_dtype, stream);
   });
   if (e != cudaSuccess) return cuda_fail(e);
   return LN_OK;

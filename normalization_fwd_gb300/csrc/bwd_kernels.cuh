@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
 }
 
 template <typename T, int N, bool kRms, bool kBias>
-__global__ void __launch_bounds__(kBulkThreads, (kRms && !kBias && N <= 4) ? 3 : 2)
+__global__ void __launch_bounds__(kBulkThreads, 2)
     bwd_bulk_cta_kernel(const BwdArgs a, const BulkCfg c) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ float2 red[2][kConsumerWarps];

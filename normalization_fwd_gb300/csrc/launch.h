@@ -48,6 +48,8 @@ int path_override();
   const void* bwd_bulk_ln_dbias_table_##NAME(int kind, int group, int n); \
   const void* bwd_bulk_rms_dbias_table_##NAME(int kind, int group, int n); \
   const void* bwd_reg_table_##NAME(int kind, int group, int n);           \
+  const void* softmax_table_##NAME(int kind, int group, int n);           \
+  cudaError_t take_error_softmax_##NAME(cudaStream_t st, unsigned* out);  \
   cudaError_t take_error_fwd_bulk_##NAME(cudaStream_t st, unsigned* out); \
   cudaError_t take_error_bwd_bulk_ln_##NAME(cudaStream_t st, unsigned* out); \
   cudaError_t take_error_bwd_bulk_rms_##NAME(cudaStream_t st, unsigned* out); \
@@ -66,14 +68,20 @@ template <typename T> cudaError_t fwd_launch(const FwdArgs& a, const Plan& p, cu
 template <typename T>
 cudaError_t bwd_plan(int64_t rows, int hidden, bool rms, bool dbias, bool vec, Plan* p);
 template <typename T>
-cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, float* dgamma, float* dbeta, float* dbias,
-                       cudaStream_t st);
+cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, void* dgamma, void* dbeta, void* dbias,
+                       int grad_dtype, cudaStream_t st);
+
+// Row softmax: plan and launch (plan.cu).
+template <typename T> cudaError_t softmax_plan(int64_t rows, int hidden, bool vec, Plan* p);
+cudaError_t softmax_launch(const SmxArgs& a, const Plan& p, cudaStream_t st);
 
 // Fixed-order sum of the backward's per-CTA partials (finalize.cu).
 // Columns of a partial row: [0, H) dgamma, then [H, 2H) dbeta when `beta_cols`,
-// then H columns of dbias when dbias is non-null.
+// then H columns of dbias when dbias is non-null. out_dtype: 0 fp32,
+// 1 bf16, 2 fp16 (the ln_dtype codes) for all three outputs.
 cudaError_t launch_bwd_finalize(const float* ws, int P, int C, int H, bool beta_cols,
-                                float* dgamma, float* dbeta, float* dbias, cudaStream_t st);
+                                void* dgamma, void* dbeta, void* dbias, int out_dtype,
+                                cudaStream_t st);
 
 }  // namespace nf
 

@@ -64,6 +64,7 @@ template <typename T> struct Tables;
       return rms ? bwd_bulk_rms_table_##NAME(k, g, n) : bwd_bulk_ln_table_##NAME(k, g, n); \
     }                                                                               \
     static const void* bwd_reg(int k, int g, int n) { return bwd_reg_table_##NAME(k, g, n); }   \
+    static const void* softmax(int k, int g, int n) { return softmax_table_##NAME(k, g, n); }   \
   };
 NF_TABLES(float, f32)
 NF_TABLES(bf16, bf16)
@@ -214,16 +215,44 @@ cudaError_t bwd_plan(int64_t rows, int hidden, bool rms, bool dbias, bool vec, P
 }
 
 template <typename T>
-cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, float* dgamma, float* dbeta, float* dbias,
-                       cudaStream_t st) {
+cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, void* dgamma, void* dbeta, void* dbias,
+                       int grad_dtype, cudaStream_t st) {
   cudaError_t e = launch_plan(p, const_cast<BwdArgs*>(&a), st);
   if (e != cudaSuccess) return e;
   return launch_bwd_finalize(a.ws, p.grid, p.ws_cols, a.hidden, !a.rms, dgamma,
-                             a.rms ? nullptr : dbeta, a.has_dbias ? dbias : nullptr, st);
+                             a.rms ? nullptr : dbeta, a.has_dbias ? dbias : nullptr, grad_dtype,
+                             st);
+}
+
+// Row softmax: the pipelined kernels for aligned rows (one streamed input,
+// no parameter rows; lane groups of up to 4 vectors run three CTAs per SM),
+// the scalar kernel otherwise.
+template <typename T> cudaError_t softmax_plan(int64_t rows, int hidden, bool vec, Plan* p) {
+  const Choice c = choose(hidden, Vec<T>::N, vec);
+  if (c.kind == 0 || c.kind == 1) {
+    Choice b = c;
+    if (c.kind == 1) b.n = bulk_cta_n(hidden, Vec<T>::N);
+    if (fill_bulk(p, b, rows, hidden, sizeof(T), 1, 0, ring_target(false, b.kind == 0 && b.n <= 4))) {
+      p->fn = Tables<T>::softmax(b.kind, b.group, b.n);
+      return size_grid(p, p->cfg.num_tiles);
+    }
+    return cudaErrorInvalidConfiguration;
+  }
+  if (c.kind != 2) return cudaErrorInvalidConfiguration;
+  p->fn = Tables<T>::softmax(2, 0, 0);
+  fill_shape(p, c, hidden, false, false);
+  return size_grid(p, rows);
+}
+
+cudaError_t softmax_launch(const SmxArgs& a, const Plan& p, cudaStream_t st) {
+  return launch_plan(p, const_cast<SmxArgs*>(&a), st);
 }
 
 }  // namespace nf
 
+template cudaError_t nf::softmax_plan<float>(int64_t, int, bool, nf::Plan*);
+template cudaError_t nf::softmax_plan<nf::bf16>(int64_t, int, bool, nf::Plan*);
+template cudaError_t nf::softmax_plan<nf::f16>(int64_t, int, bool, nf::Plan*);
 template cudaError_t nf::fwd_plan<float>(int64_t, int, bool, bool, int, nf::Plan*);
 template cudaError_t nf::fwd_plan<nf::bf16>(int64_t, int, bool, bool, int, nf::Plan*);
 template cudaError_t nf::fwd_plan<nf::f16>(int64_t, int, bool, bool, int, nf::Plan*);
@@ -233,9 +262,9 @@ template cudaError_t nf::bwd_plan<nf::f16>(int64_t, int, bool, bool, bool, nf::P
 template cudaError_t nf::fwd_launch<float>(const nf::FwdArgs&, const nf::Plan&, cudaStream_t);
 template cudaError_t nf::fwd_launch<nf::bf16>(const nf::FwdArgs&, const nf::Plan&, cudaStream_t);
 template cudaError_t nf::fwd_launch<nf::f16>(const nf::FwdArgs&, const nf::Plan&, cudaStream_t);
-template cudaError_t nf::bwd_launch<float>(const nf::BwdArgs&, const nf::Plan&, float*, float*,
-                                           float*, cudaStream_t);
-template cudaError_t nf::bwd_launch<nf::bf16>(const nf::BwdArgs&, const nf::Plan&, float*, float*,
-                                              float*, cudaStream_t);
-template cudaError_t nf::bwd_launch<nf::f16>(const nf::BwdArgs&, const nf::Plan&, float*, float*,
-                                             float*, cudaStream_t);
+template cudaError_t nf::bwd_launch<float>(const nf::BwdArgs&, const nf::Plan&, void*, void*,
+                                           void*, int, cudaStream_t);
+template cudaError_t nf::bwd_launch<nf::bf16>(const nf::BwdArgs&, const nf::Plan&, void*, void*,
+                                           void*, int, cudaStream_t);
+template cudaError_t nf::bwd_launch<nf::f16>(const nf::BwdArgs&, const nf::Plan&, void*, void*,
+                                           void*, int, cudaStream_t);

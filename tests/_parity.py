@@ -91,9 +91,9 @@ def gpu_fwd(lib, w, inp, *, store_sum=True, stats=True, amax=None, stream=None,
 
 
 def gpu_bwd(lib, w, dy, x_sum, gamma, mean, rstd, *, need_dbeta=True, need_dbias=False,
-            workspace=None, stream=None):
-    """Run ln_bwd (ln_bwd_ex with dbias); inputs are CPU or CUDA tensors.
-    Returns CPU tensors."""
+            grad_dtype=torch.float32, workspace=None, stream=None):
+    """Run ln_bwd (ln_bwd_ex with dbias or a low-precision grad_dtype); inputs
+    are CPU or CUDA tensors. Returns CPU tensors."""
     dev = "cuda"
     dt = TORCH_DTYPES[w.dtype]
     R, H = w.rows, w.hidden
@@ -101,13 +101,13 @@ def gpu_bwd(lib, w, dy, x_sum, gamma, mean, rstd, *, need_dbeta=True, need_dbias
     dy, x_sum, gamma = dy.to(dev), x_sum.to(dev), gamma.to(dev)
     mean = mean.to(dev) if (mean is not None and not rms) else None
     rstd = rstd.to(dev)
-    outs = {"dx": Guarded((R, H), dt), "dgamma": Guarded((H,), torch.float32)}
+    outs = {"dx": Guarded((R, H), dt), "dgamma": Guarded((H,), grad_dtype)}
     if need_dbeta and not rms:
-        outs["dbeta"] = Guarded((H,), torch.float32)
+        outs["dbeta"] = Guarded((H,), grad_dtype)
     if need_dbias:
-        outs["dbias"] = Guarded((H,), torch.float32)
+        outs["dbias"] = Guarded((H,), grad_dtype)
     g = {k: v.t for k, v in outs.items()}
-    if need_dbias:
+    if need_dbias or grad_dtype != torch.float32:
         lib.ln_bwd_ex(dy, x_sum, gamma, mean, rstd, g["dx"], g["dgamma"], g.get("dbeta"),
                       g["dbias"], stream, mode=w.mode, zero_centered_gamma=w.zero_centered_gamma,
                       workspace=workspace)

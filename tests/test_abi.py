@@ -36,7 +36,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["ln_fwd", "ln_fwd_ex", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes",
-         "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc"])
+         "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc",
+         "ln_softmax_fwd"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -146,12 +147,36 @@ def test_bwd_ex_validates_dbias_on_host(lib):
         a.update(kw)
         return lib.ln_bwd_ex(a["dy"], a["xs"], a["gamma"], a["mean"], a["rstd"], a["dx"], a["dg"],
                              a["db"], dbias, None, a["rows"], a["hidden"], a["dtype"], a["mode"],
-                             a["zc"], a["ws"], a["ws_bytes"])
+                             a["zc"], a["ws"], a["ws_bytes"], a.get("gdt", 0))
     DBIAS = 0x7f0000000000 + 11 * 0x10000000
     assert call(DBIAS + 2) == ALIGN
     assert call(S + 16) == INVALID          # overlaps dgamma
     assert call(X + 64) == INVALID          # overlaps dy
     assert call(DBIAS, dy=None) == NULL
+    assert call(DBIAS, gdt=3) == UNSUPPORTED       # grad_dtype must be f32, bf16 or f16
+    assert call(DBIAS, gdt=1, dg=S + 1) == ALIGN    # bf16 grads need 2-byte alignment
+    assert call(DBIAS, gdt=0, dg=S + 2) == ALIGN
+    assert call(DBIAS, gdt=1, db=S + 512) == INVALID   # bf16 dgamma [384] is 768 bytes
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(x=None), NULL),
+    (dict(y=None), NULL),
+    (dict(dtype=5), UNSUPPORTED),
+    (dict(rows=-1), SHAPE),
+    (dict(hidden=0), SHAPE),
+    (dict(hidden=16385), SHAPE),
+    (dict(hidden=8200, dtype=0), SHAPE),           # fp32: 8192 max
+    (dict(x=X + 2, hidden=9000), SHAPE),           # unaligned rows: scalar path, 8192 max
+    (dict(x=X + 1), ALIGN),
+    (dict(y=Y + 2, dtype=0), ALIGN),
+    (dict(y=X + 128), INVALID),                    # partial overlap (in place is y == x)
+    (dict(x=Y + 768), INVALID),
+])
+def test_softmax_rejects_on_host(lib, kw, want):
+    a = dict(x=X, y=Y, rows=4, hidden=384, dtype=1)
+    a.update(kw)
+    assert lib.ln_softmax_fwd(a["x"], a["y"], None, a["rows"], a["hidden"], a["dtype"]) == want
 
 
 def test_rmsnorm_ignores_mean_and_dbeta(lib):

@@ -7,6 +7,7 @@ in the last bits: the dbias kernel can run a different number of CTAs per SM,
 hence a different row partition of the partial sums).
 """
 
+import numpy as np
 import pytest
 import torch
 
@@ -50,6 +51,44 @@ def test_dbias_matches_oracle(cuda_lib, dtype, rows, hidden, mode):
     check_rel_l2(as_f64(ex["dgamma"]), bref["dgamma"], 1e-4, "dgamma")
     if mode == W.LAYERNORM:
         check_rel_l2(as_f64(ex["dbeta"]), bref["dbeta"], 1e-4, "dbeta")
+
+
+@pytest.mark.parametrize("gdt", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("mode", [W.LAYERNORM, W.RMSNORM])
+@pytest.mark.parametrize("dtype,rows,hidden", [("bf16", 20001, 384), ("bf16", 601, 8192),
+                                               ("f32", 3001, 768), ("bf16", 777, 1001)])
+def test_low_precision_parameter_gradients(cuda_lib, dtype, rows, hidden, mode, gdt):
+    # The down cast after the outer reduction (PR 165370's epilogue): each
+    # column total is rounded once to bf16 / fp16. Every value is within one
+    # unit of the oracle's total rounded to that type, and equals the fp32
+    # result of the same partials rounded to it unless that was a double
+    # rounding (the fp64 total lying within an fp32 ulp of a tie).
+    from oracle import round_to_format
+    from _parity import ulp
+    fmt = "bf16" if gdt == torch.bfloat16 else "f16"
+    w = wl(dtype, rows, hidden, mode)
+    inp = make_inputs(w, seed=13)
+    ref = oracle_fwd(w, inp)
+    dt = W.TORCH_DTYPES[w.dtype]
+    x_sum = torch.from_numpy(ref["sum"]).to(dt)
+    mean = None if ref["mean"] is None else torch.from_numpy(ref["mean"]).float()
+    rstd = torch.from_numpy(ref["rstd"]).float()
+    bref = oracle_bwd_rows(w, inp["dy"], x_sum, inp["gamma"], mean, rstd, slice(None))
+    lo = gpu_bwd(cuda_lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd, need_dbias=True,
+                 grad_dtype=gdt)
+    hi = gpu_bwd(cuda_lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd, need_dbias=True)
+    assert lo["guards_ok"]
+    names = ["dgamma", "dbias"] + (["dbeta"] if mode == W.LAYERNORM else [])
+    for k in names:
+        got = as_f64(lo[k])
+        want = round_to_format(bref[k], fmt)
+        # the ulp floor of reading G: a column total that cancels to ~0 is
+        # measured on the scale of the vector (2^-8 of its largest entry)
+        mag = np.maximum(abs(bref[k]), np.ldexp(abs(bref[k]).max(), -8))
+        d = abs(got - want) / ulp(mag, fmt)
+        assert d.max() <= 1.0, (k, float(d.max()))
+        same = (got == round_to_format(as_f64(hi[k]), fmt)).mean()
+        assert same >= 0.999, (k, same)
 
 
 def test_dbias_on_empty_rows_is_zero(cuda_lib):

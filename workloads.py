@@ -139,6 +139,55 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
     return out
 
 
+# ---- row softmax ------------------------------------------------------------
+# The softmax IR of iree-org/iree issue 9139 is a 6 x 3 fp32 toy with an
+# elided constant, so no shape or distribution comes from the pages. The
+# softmax workloads reuse the normalization shapes (rows of 384 and 8192
+# elements, a 1280-wide fp16 case) with attention-logit-like inputs,
+# x = x_std * N(0, 1), and optionally a fraction of positions masked to -inf.
+
+@dataclass(frozen=True)
+class SoftmaxWorkload:
+    name: str
+    dtype: str
+    rows: int
+    hidden: int
+    x_std: float = 2.0
+    mask_frac: float = 0.0        # positions set to -inf (distinct, uniform)
+    masked_rows: int = 0          # whole rows set to -inf (the first ones drawn)
+
+    def with_(self, **kw) -> "SoftmaxWorkload":
+        return replace(self, **kw)
+
+
+SMX_F32_4096x384 = SoftmaxWorkload(name="softmax_f32_4096x384", dtype="f32", rows=4096,
+                                   hidden=384)
+SMX_F16_8192x1280_MASKED = SoftmaxWorkload(name="softmax_f16_8192x1280_masked", dtype="f16",
+                                           rows=8192, hidden=1280, mask_frac=0.25,
+                                           masked_rows=3)
+SMX_BF16_576000x384 = SoftmaxWorkload(name="softmax_bf16_576000x384", dtype="bf16",
+                                      rows=576000, hidden=384)
+SMX_BF16_16384x8192 = SoftmaxWorkload(name="softmax_bf16_16384x8192", dtype="bf16",
+                                      rows=16384, hidden=8192)
+
+SOFTMAX_WORKLOADS = {w.name: w for w in (SMX_F32_4096x384, SMX_F16_8192x1280_MASKED,
+                                         SMX_BF16_576000x384, SMX_BF16_16384x8192)}
+
+
+def make_softmax_inputs(w: SoftmaxWorkload, seed: int = 0) -> torch.Tensor:
+    """x for a softmax workload: draws in the order x, masked positions,
+    masked rows; float64 -> float32 -> dtype as for the normalization."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    R, H = w.rows, w.hidden
+    x = w.x_std * rng.standard_normal((R, H))
+    if w.mask_frac > 0.0 and R * H > 0:
+        k = int(round(w.mask_frac * R * H))
+        x.reshape(-1)[rng.choice(R * H, size=k, replace=False)] = -np.inf
+    if w.masked_rows > 0 and R > 0:
+        x[rng.choice(R, size=min(R, w.masked_rows), replace=False)] = -np.inf
+    return to_dtype(x, w.dtype)
+
+
 def as_f64(t) -> np.ndarray | None:
     """Decode a CPU tensor of any of the I/O dtypes to a float64 numpy array."""
     if t is None:
