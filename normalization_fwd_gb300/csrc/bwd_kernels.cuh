@@ -112,14 +112,17 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
 }
 
 // The row body of the pipelined kernels: dy and x_sum rows in shared memory,
-// w = gamma (+1) staged in shared memory (kStaged) or read from global. Both
-// passes read shared memory, so only the accumulators stay in registers
-// across the reduction. Values are fp32 pairs (packed fp32 math). kRms drops
+// w = gamma (+1) staged in shared memory (kStaged), read from global, or
+// (kWReg) held in registers: a thread covers the same columns in every row,
+// so `wreg` is loaded once per kernel. Both passes read shared memory, so only
+// the accumulators (and wreg) stay in registers across the reduction. Values are fp32 pairs (packed fp32 math). kRms drops
 // the mean, c1 and the dbeta accumulators at compile time; kBias adds the
 // row's fp32 dx into the dbias accumulators.
-template <typename T, int G, int N, bool kRms, bool kBias, bool kStaged, typename Reduce2>
+template <typename T, int G, int N, bool kRms, bool kBias, bool kStaged, bool kWReg,
+          typename Reduce2>
 __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool row_ok, int t,
                                              uint32_t dyrow, uint32_t xsrow, const ParamRow<T>& wr,
+                                             const float2 (&wreg)[N][Vec<T>::N / 2],
                                              float mean, float rstd, Reduce2 reduce2,
                                              float2 (&acc_g)[N][Vec<T>::N / 2],
                                              float2 (&acc_b)[N][Vec<T>::N / 2],
@@ -139,7 +142,12 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
       float2 d[P], xv[P], w[P];
       unpack2<T>(lds_u4(dyrow + v * 16), d);
       unpack2<T>(lds_u4(xsrow + v * 16), xv);
-      wr.template load2<kStaged>(v, w, wa);
+      if (kWReg) {
+#pragma unroll
+        for (int i = 0; i < P; ++i) w[i] = wreg[k][i];
+      } else {
+        wr.template load2<kStaged>(v, w, wa);
+      }
 #pragma unroll
       for (int i = 0; i < P; ++i) {
         const float2 xh = mul2(kRms ? xv[i] : add2(xv[i], neg_mean), r2);
@@ -166,7 +174,12 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
       float2 d[P], xv[P], w[P], o[P];
       unpack2<T>(lds_u4(dyrow + v * 16), d);
       unpack2<T>(lds_u4(xsrow + v * 16), xv);
-      wr.template load2<kStaged>(v, w, wa);
+      if (kWReg) {
+#pragma unroll
+        for (int i = 0; i < P; ++i) w[i] = wreg[k][i];
+      } else {
+        wr.template load2<kStaged>(v, w, wa);
+      }
 #pragma unroll
       for (int i = 0; i < P; ++i) {
         const float2 xm = kRms ? xv[i] : add2(xv[i], neg_mean);
@@ -377,6 +390,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
   const int lane = threadIdx.x & 31;
   const int l = lane % LANES;
   const int local = (threadIdx.x >> 5) * RPW + lane / LANES;   // row within the tile
+  float2 wreg[N][Vec<T>::N / 2];   // unused: w is staged in shared memory
   float2 acc_g[N][Vec<T>::N / 2], acc_b[N][Vec<T>::N / 2], acc_d[N][Vec<T>::N / 2];
   zero_acc2<T, N>(acc_g);
   zero_acc2<T, N>(acc_b);
@@ -402,8 +416,8 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
         const int64_t row = tile * c.tile_rows + local;
         const uint32_t dys = smem_addr(slot) + (uint32_t)(local * H * sizeof(T));
         const uint32_t xss = dys + in_bytes;
-        bwd_row_smem<T, LANES, N, kRms, kBias, true>(
-            a, row, row < a.rows, l, dys, xss, wr, mean, rstd,
+        bwd_row_smem<T, LANES, N, kRms, kBias, true, false>(
+            a, row, row < a.rows, l, dys, xss, wr, wreg, mean, rstd,
             [](float2 v) { return group_sum2<LANES>(v); }, acc_g, acc_b, acc_d);
       });
   if (pipeline_finish(ring, aborted, taken, &s_abort, &s_taken)) return;
@@ -413,6 +427,11 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
   unpair_acc<T, N>(acc_d, fd);
   store_group_partials<T, LANES, N, kConsumerWarps, kRms, kBias>(a, fg, fb, fd, red);
 }
+
+// Whether the CTA-per-row backward keeps w in registers: its accumulators
+// take N * VEC floats per reduction (dgamma; dbeta for LayerNorm; dbias).
+template <typename T, int N, bool kRms, bool kBias>
+constexpr bool kWRegCta = N * Vec<T>::N * (1 + (kRms ? 0 : 1) + (kBias ? 1 : 0)) <= 32;
 
 template <typename T, int N, bool kRms, bool kBias>
 __global__ void __launch_bounds__(kBulkThreads, 2)
@@ -429,6 +448,16 @@ __global__ void __launch_bounds__(kBulkThreads, 2)
     s_taken = 0x7fffffffffffffffll;
   }
   const ParamRow<T> wr = {nullptr, static_cast<const T*>(a.gamma), H, a.zero_centered != 0};
+  // w in registers when the accumulators leave room for it.
+  constexpr bool kWReg = kWRegCta<T, N, kRms, kBias>;
+  float2 wreg[N][Vec<T>::N / 2];
+  if (kWReg) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int v = k * kBulkThreads + threadIdx.x;
+      if (v < H / Vec<T>::N) wr.template load2<false>(v, wreg[k]);
+    }
+  }
   ring_init(ring);
 
   float2 acc_g[N][Vec<T>::N / 2], acc_b[N][Vec<T>::N / 2], acc_d[N][Vec<T>::N / 2];
@@ -454,8 +483,8 @@ __global__ void __launch_bounds__(kBulkThreads, 2)
         load_stats(row + gridDim.x, nm, nr);
         const uint32_t dys = smem_addr(slot);
         const uint32_t xss = dys + in_bytes;
-        bwd_row_smem<T, kBulkThreads, N, kRms, kBias, false>(
-            a, row, true, threadIdx.x, dys, xss, wr, mean, rstd,
+        bwd_row_smem<T, kBulkThreads, N, kRms, kBias, false, kWReg>(
+            a, row, true, threadIdx.x, dys, xss, wr, wreg, mean, rstd,
             [&](float2 v) { return cta_sum2_db<kBulkThreads>(v, red, parity); }, acc_g, acc_b,
             acc_d);
       });

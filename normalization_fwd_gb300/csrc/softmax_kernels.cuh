@@ -14,8 +14,9 @@
 //  * smx_scalar_kernel: any hidden size and alignment; element-wise loads,
 //    the row staged in shared memory as fp32.
 //
-// Arithmetic: fp32 throughout. m = max (fmaxf), e = expf(x - m), s = sum of
-// e, y = e * (1/s) with a correctly rounded reciprocal. A row whose entries
+// Arithmetic: fp32 throughout. m = max, e = exp2f((x - m) * log2 e) (one fma
+// and one exp2f per element), s = sum of e, y = e * (1/s) with a correctly
+// rounded reciprocal. A row whose entries
 // are all -inf, or that holds a NaN or +inf, comes out as NaN, as the
 // definition gives.
 #pragma once
@@ -27,9 +28,61 @@
 
 namespace nf {
 
-// One row from shared memory. `G` threads share the row, this one is `t`;
-// `xrow` is the shared-memory address of the row. `rmax` / `rsum` reduce a
-// float over the G threads.
+// exp(v) = 2^(v * log2(e)): the exponential of the shifted row is taken as
+// exp2f(fma(x, log2e, -m * log2e)). The rounding of m * log2e multiplies every
+// e_j of the row by the same factor, which the division by their sum removes.
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Running max over a row's 16-byte vectors. For bf16/fp16 the max is taken
+// on the packed pairs (exact: no rounding is involved) and widened at the end.
+template <typename T> struct RowMax;
+template <> struct RowMax<float> {
+  float m = -INFINITY;
+  __device__ __forceinline__ void add(const uint4& u) {
+    m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(u.x), __uint_as_float(u.y)),
+                       fmaxf(__uint_as_float(u.z), __uint_as_float(u.w))));
+  }
+  __device__ __forceinline__ float value() const { return m; }
+};
+template <> struct RowMax<bf16> {
+  __nv_bfloat162 m = __nv_bfloat162(__ushort_as_bfloat16(0xff80u), __ushort_as_bfloat16(0xff80u));
+  static __device__ __forceinline__ __nv_bfloat162 h(unsigned w) {
+    return *reinterpret_cast<__nv_bfloat162*>(&w);
+  }
+  __device__ __forceinline__ void add(const uint4& u) {
+    m = __hmax2(m, __hmax2(__hmax2(h(u.x), h(u.y)), __hmax2(h(u.z), h(u.w))));
+  }
+  __device__ __forceinline__ float value() const {
+    return fmaxf(__bfloat162float(m.x), __bfloat162float(m.y));
+  }
+};
+template <> struct RowMax<f16> {
+  __half2 m = __half2(__ushort_as_half(0xfc00u), __ushort_as_half(0xfc00u));
+  static __device__ __forceinline__ __half2 h(unsigned w) { return *reinterpret_cast<__half2*>(&w); }
+  __device__ __forceinline__ void add(const uint4& u) {
+    m = __hmax2(m, __hmax2(__hmax2(h(u.x), h(u.y)), __hmax2(h(u.z), h(u.w))));
+  }
+  __device__ __forceinline__ float value() const {
+    return fmaxf(__half2float(m.x), __half2float(m.y));
+  }
+};
+
+// e = 2^(x * log2e + nml) for one vector, added into acc; nml = -shift * log2e.
+template <typename T>
+__device__ __forceinline__ void exp_vec(const uint4& u, float nml, float2* e, float2& acc) {
+  constexpr int P = Vec<T>::N / 2;
+  unpack2<T>(u, e);
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    const float2 t = fma2(e[p], splat2(kLog2e), splat2(nml));
+    e[p].x = exp2f(t.x);
+    e[p].y = exp2f(t.y);
+    acc = add2(acc, e[p]);
+  }
+}
+
+// Lane-group rows: `G` lanes share the row, this one is `t`; `xrow` is the
+// row's shared-memory address. Reductions: max over the row, then the sum.
 template <typename T, int G, int N, typename RMax, typename RSum>
 __device__ __forceinline__ void smx_row_smem(const SmxArgs& a, int64_t row, bool row_ok, int t,
                                              uint32_t xrow, RMax rmax, RSum rsum) {
@@ -38,30 +91,23 @@ __device__ __forceinline__ void smx_row_smem(const SmxArgs& a, int64_t row, bool
   const int V = a.hidden / VEC;
   T* y_row = static_cast<T*>(a.y) + row * (int64_t)a.hidden;
 
-  float2 v[N][P];
-  float m = -INFINITY;
+  uint4 raw[N];
+  RowMax<T> rm;
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     const int i = k * G + t;
     if (row_ok && i < V) {
-      unpack2<T>(lds_u4(xrow + i * 16), v[k]);
-#pragma unroll
-      for (int p = 0; p < P; ++p) m = fmaxf(m, fmaxf(v[k][p].x, v[k][p].y));
+      raw[k] = lds_u4(xrow + i * 16);
+      rm.add(raw[k]);
     }
   }
-  m = rmax(m);
+  const float nml = -rmax(rm.value()) * kLog2e;
 
+  float2 e[N][P];
   float2 acc = splat2(0.f);
 #pragma unroll
   for (int k = 0; k < N; ++k) {
-    if (row_ok && (k * G + t) < V) {
-#pragma unroll
-      for (int p = 0; p < P; ++p) {
-        v[k][p].x = expf(v[k][p].x - m);
-        v[k][p].y = expf(v[k][p].y - m);
-        acc = add2(acc, v[k][p]);
-      }
-    }
+    if (row_ok && (k * G + t) < V) exp_vec<T>(raw[k], nml, e[k], acc);
   }
   const float2 inv = splat2(__frcp_rn(rsum(acc.x + acc.y)));
 
@@ -71,7 +117,67 @@ __device__ __forceinline__ void smx_row_smem(const SmxArgs& a, int64_t row, bool
     if (row_ok && i < V) {
       float2 o[P];
 #pragma unroll
-      for (int p = 0; p < P; ++p) o[p] = mul2(v[k][p], inv);
+      for (int p = 0; p < P; ++p) o[p] = mul2(e[k][p], inv);
+      st_vec(y_row + i * VEC, pack2<T>(o));
+    }
+  }
+}
+
+// CTA rows (all 256 threads on one row), with one barrier per row: each warp
+// takes the exponentials against its own max m_w and sums them to s_w; the
+// warps' (m_w, s_w) pairs meet in shared memory, where every warp forms the
+// row max M and s = sum_w s_w * exp(m_w - M); thread scale exp(m_w - M) / s
+// (all in log2 units: L = m * log2 e).
+// This is the online normalizer of Milakov and Gimelshein ("Online normalizer
+// calculation for softmax", 2018) applied across the eight warps. A warp
+// whose entries are all -inf shifts by 0 instead (its e are 0 either way)
+// and contributes 0; a row that is all -inf stays NaN.
+template <typename T, int N>
+__device__ __forceinline__ void smx_row_cta(const SmxArgs& a, int64_t row, uint32_t xrow,
+                                            float2 (*red)[kConsumerWarps], int& parity) {
+  constexpr int VEC = Vec<T>::N;
+  constexpr int P = VEC / 2;
+  const int V = a.hidden / VEC;
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  T* y_row = static_cast<T*>(a.y) + row * (int64_t)a.hidden;
+
+  uint4 raw[N];
+  RowMax<T> rm;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int i = k * kBulkThreads + t;
+    if (i < V) {
+      raw[k] = lds_u4(xrow + i * 16);
+      rm.add(raw[k]);
+    }
+  }
+  // Lw: this warp's shift in log2 units, rounded once. The warps exchange Lw
+  // itself, so the factor 2^(Lw - L) that moves a warp's e onto the row max
+  // carries exactly the rounding its exponentials were taken with.
+  const float Lw = group_max<32>(rm.value()) * kLog2e;
+  float2 e[N][P];
+  float2 acc = splat2(0.f);
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    if (k * kBulkThreads + t < V) exp_vec<T>(raw[k], Lw == -INFINITY ? 0.f : -Lw, e[k], acc);
+  }
+  const float sw = group_sum<32>(acc.x + acc.y);
+  if (lane == 0) red[parity][t >> 5] = make_float2(Lw, sw);
+  __syncthreads();
+  const float2 q = red[parity][lane & (kConsumerWarps - 1)];
+  parity ^= 1;
+  const float L = group_max<kConsumerWarps>(q.x);
+  const float S = group_sum<kConsumerWarps>(q.y * exp2f(q.x - L));
+  const float2 f = splat2(exp2f(Lw - L) * __frcp_rn(S));
+
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int i = k * kBulkThreads + t;
+    if (i < V) {
+      float2 o[P];
+#pragma unroll
+      for (int p = 0; p < P; ++p) o[p] = mul2(e[k][p], f);
       st_vec(y_row + i * VEC, pack2<T>(o));
     }
   }
@@ -112,7 +218,7 @@ template <typename T, int N>
 __global__ void __launch_bounds__(kBulkThreads, 2) smx_bulk_cta_kernel(const SmxArgs a,
                                                                         const BulkCfg c) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ float red[2][kConsumerWarps];
+  __shared__ float2 red[2][kConsumerWarps];
   __shared__ int s_abort;
   __shared__ long long s_taken;
   const int H = a.hidden;
@@ -128,10 +234,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) smx_bulk_cta_kernel(const Smx
   const int64_t taken = run_pipeline<true, T>(
       ring, c, a.rows, H, static_cast<const T*>(a.x), static_cast<const T*>(nullptr), aborted,
       [&](int64_t row, unsigned char* slot) {
-        smx_row_smem<T, kBulkThreads, N>(
-            a, row, true, threadIdx.x, smem_addr(slot),
-            [&](float v) { return cta_max_db<kBulkThreads>(v, red, parity); },
-            [&](float v) { return cta_sum_db<kBulkThreads>(v, red, parity); });
+        smx_row_cta<T, N>(a, row, smem_addr(slot), red, parity);
       });
   pipeline_finish(ring, aborted, taken, &s_abort, &s_taken);
 }
@@ -154,10 +257,10 @@ __global__ void __launch_bounds__(kScalarCta) smx_scalar_kernel(const SmxArgs a)
       srow[j] = v;
       m = fmaxf(m, v);
     }
-    m = cta_max_db<kScalarCta>(m, red, parity);
+    const float nml = -cta_max_db<kScalarCta>(m, red, parity) * kLog2e;
     float s = 0.f;
     for (int j = threadIdx.x; j < H; j += kScalarCta) {
-      const float e = expf(srow[j] - m);
+      const float e = exp2f(fmaf(srow[j], kLog2e, nml));
       srow[j] = e;
       s += e;
     }
