@@ -85,12 +85,30 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
+// try_wait with a suspend-time hint: the warp is parked (issuing nothing and
+// polling no shared memory) until the phase completes or about `hint_ns`
+// nanoseconds have passed.
+constexpr uint32_t kSuspendHintNs = 1000000u;
+__device__ __forceinline__ bool mbar_test_suspend(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return done != 0;
+}
+
 // Wait for the phase of `bar` with the given parity to complete; false when
-// it has not completed within kWaitLimitNs.
+// it has not completed within kWaitLimitNs. Waiting warps sleep in the
+// hinted try_wait instead of spinning, so they take no issue slots and no
+// shared-memory bandwidth from the warps that work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (!mbar_test(bar, parity)) {
+  while (!mbar_test_suspend(bar, parity)) {
     if (global_ns() - t0 > kWaitLimitNs) return false;
   }
   return true;

@@ -77,6 +77,7 @@ NF_TABLES(f16, f16)
 constexpr size_t kRingTarget = 104 * 1024;
 constexpr size_t kRingTargetFwdGroup = 68 * 1024;
 constexpr size_t kMaxDynSmem = 200 * 1024;
+constexpr size_t kRingTargetSmx = 48 * 1024;
 
 // Ring targets may be overridden (in KiB) through NORMFUSE_RING_KB_FWD /
 // NORMFUSE_RING_KB_BWD for tuning; read once.
@@ -224,15 +225,20 @@ cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, void* dgamma, void* dbet
                              st);
 }
 
-// Row softmax: the pipelined kernels for aligned rows (one streamed input,
-// no parameter rows; lane groups of up to 4 vectors run three CTAs per SM),
-// the scalar kernel otherwise.
+// Row softmax: the pipelined kernels for aligned rows (one streamed input, no
+// parameter rows), the scalar kernel otherwise. Softmax kernels of up to 4
+// vectors per thread are built for three or four CTAs per SM and take a
+// 48 KiB ring: at 16384 x 8192 bf16, 3 CTAs x 3 slots ran 90 us against
+// 98 us for 2 CTAs x 6 slots; at 576000 x 384 the two were within 2 %.
+// Wider rows (more registers, two CTAs per SM) keep the 104 KiB ring.
 template <typename T> cudaError_t softmax_plan(int64_t rows, int hidden, bool vec, Plan* p) {
   const Choice c = choose(hidden, Vec<T>::N, vec);
   if (c.kind == 0 || c.kind == 1) {
     Choice b = c;
     if (c.kind == 1) b.n = bulk_cta_n(hidden, Vec<T>::N);
-    if (fill_bulk(p, b, rows, hidden, sizeof(T), 1, 0, ring_target(false, b.kind == 0 && b.n <= 4))) {
+    static const size_t env = ring_target_kb_env("NORMFUSE_RING_KB_SMX");
+    const size_t target = env ? env : (b.n <= 4 ? kRingTargetSmx : kRingTarget);
+    if (fill_bulk(p, b, rows, hidden, sizeof(T), 1, 0, target)) {
       p->fn = Tables<T>::softmax(b.kind, b.group, b.n);
       return size_grid(p, p->cfg.num_tiles);
     }

@@ -184,7 +184,7 @@ __device__ __forceinline__ void smx_row_cta(const SmxArgs& a, int64_t row, uint3
 }
 
 template <typename T, int LANES, int N>
-__global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 3 : 2) smx_bulk_warp_kernel(const SmxArgs a,
+__global__ void __launch_bounds__(kBulkThreads, N <= 3 ? 4 : (N == 4 ? 3 : 2)) smx_bulk_warp_kernel(const SmxArgs a,
                                                                          const BulkCfg c) {
   constexpr int RPW = 32 / LANES;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 3 : 2) smx_bulk_warp_ke
 }
 
 template <typename T, int N>
-__global__ void __launch_bounds__(kBulkThreads, 2) smx_bulk_cta_kernel(const SmxArgs a,
+__global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 3 : 2) smx_bulk_cta_kernel(const SmxArgs a,
                                                                         const BulkCfg c) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ float2 red[2][kConsumerWarps];

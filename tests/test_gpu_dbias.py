@@ -1,10 +1,10 @@
 """GPU parity of the bias gradient (ln_bwd_ex): dbias = sum over rows of dx,
 the third column reduction fused into the backward's persistent kernel.
 
-Checked against the oracle's dbias (fp32 rules: relative L2 <= 1e-4), and
-dx must be bitwise that of ln_bwd on the same inputs (dgamma/dbeta may differ
-in the last bits: the dbias kernel can run a different number of CTAs per SM,
-hence a different row partition of the partial sums).
+Checked against the oracle's dbias (fp32 rules: relative L2 <= 1e-4); dx,
+dgamma and dbeta against the oracle with the usual tolerances. (With dbias a
+shape can run on another kernel family than ln_bwd does, e.g. CTA-per-row
+where ln_bwd uses lane groups, so dx need not be bitwise that of ln_bwd.)
 """
 
 import numpy as np
@@ -12,7 +12,8 @@ import pytest
 import torch
 
 import workloads as W
-from _parity import check_rel_l2, gpu_bwd, oracle_bwd_rows, oracle_fwd
+from _parity import (check_elementwise, check_rel_l2, dx_row_scale, gpu_bwd, oracle_bwd_rows,
+                     oracle_fwd)
 from workloads import Workload, as_f64, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -43,11 +44,11 @@ def test_dbias_matches_oracle(cuda_lib, dtype, rows, hidden, mode):
     rstd = torch.from_numpy(ref["rstd"]).float()
     bref = oracle_bwd_rows(w, inp["dy"], x_sum, inp["gamma"], mean, rstd, slice(None))
     ex = gpu_bwd(cuda_lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd, need_dbias=True)
-    plain = gpu_bwd(cuda_lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd)
     assert ex["guards_ok"]
     check_rel_l2(as_f64(ex["dbias"]), bref["dbias"], 1e-4, "dbias")
-    bits = torch.int16 if ex["dx"].element_size() == 2 else torch.int32
-    assert torch.equal(ex["dx"].view(bits), plain["dx"].view(bits))
+    check_elementwise(as_f64(ex["dx"]), bref["dx_exact"], dtype, "dx",
+                      scale_rows=dx_row_scale(as_f64(inp["dy"]), as_f64(inp["gamma"]),
+                                              as_f64(rstd), w.zero_centered_gamma))
     check_rel_l2(as_f64(ex["dgamma"]), bref["dgamma"], 1e-4, "dgamma")
     if mode == W.LAYERNORM:
         check_rel_l2(as_f64(ex["dbeta"]), bref["dbeta"], 1e-4, "dbeta")
