@@ -102,6 +102,39 @@ int device_sm_count(int* sms) {
   return (int)cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
 }
 
+struct SmemEntry {
+  const void* fn;
+  int device;
+  size_t allowed;     // dynamic bytes the kernel is opted in to
+  size_t static_bytes;
+};
+std::vector<SmemEntry>& smem_cache() {
+  static std::vector<SmemEntry> v;
+  return v;
+}
+
+int allow_dyn_smem(const void* fn, size_t smem) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  SmemEntry* ent = nullptr;
+  for (SmemEntry& s : smem_cache())
+    if (s.fn == fn && s.device == dev) ent = &s;
+  if (ent == nullptr) {
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, fn);
+    if (e != cudaSuccess) return (int)e;
+    smem_cache().push_back({fn, dev, 0, attr.sharedSizeBytes});
+    ent = &smem_cache().back();
+  }
+  if (smem <= ent->allowed || smem + ent->static_bytes <= 48 * 1024) return (int)cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return (int)e;
+  ent->allowed = smem;
+  return (int)cudaSuccess;
+}
+
 int resident_blocks(const void* fn, int block, size_t smem, int* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -317,6 +317,48 @@ __device__ __forceinline__ void store_thread_partials(const BwdArgs& a, int t,
   }
 }
 
+// Partials of a row-group kernel: 256 / G groups of G threads (G = 64 or
+// 128), thread t of every group holding the same columns (vectors k * G + t).
+// The groups are added through shared memory in group order, one vector slot
+// (G * VEC columns) at a time. All threads of the CTA call this.
+template <typename T, int G, int N, bool kRms, bool kBias>
+__device__ __forceinline__ void store_rowgroup_partials(const BwdArgs& a,
+                                                        float (&acc_g)[N][Vec<T>::N],
+                                                        float (&acc_b)[N][Vec<T>::N],
+                                                        float (&acc_d)[N][Vec<T>::N],
+                                                        float (*red)[G * Vec<T>::N]) {
+  constexpr int VEC = Vec<T>::N;
+  constexpr int SLOT = G * VEC;
+  constexpr int NG = kBulkThreads / G;
+  const int grp = threadIdx.x / G;
+  const int t = threadIdx.x % G;
+  const bool rms = kRms || a.rms;
+  const int H = a.hidden;
+  float* ws = a.ws + (int64_t)blockIdx.x * a.ws_cols;
+  for (int which = 0; which < 3; ++which) {
+    if (which == 1 && rms) continue;
+    if (which == 2 && !kBias) continue;
+    const int off = partial_offset(a, which);
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e)
+        red[grp][t * VEC + e] = which == 0 ? acc_g[k][e] : (which == 1 ? acc_b[k][e] : acc_d[k][e]);
+      __syncthreads();
+      for (int c = threadIdx.x; c < SLOT; c += kBulkThreads) {
+        const int col = k * SLOT + c;
+        if (col < H) {
+          float s = 0.f;
+#pragma unroll
+          for (int g = 0; g < NG; ++g) s += red[g][c];
+          ws[off + col] = s;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
 // ---- register kernels ------------------------------------------------------
 
 template <typename T, int LANES, int N>
@@ -432,6 +474,93 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
 // take N * VEC floats per reduction (dgamma; dbeta for LayerNorm; dbias).
 template <typename T, int N, bool kRms, bool kBias>
 constexpr bool kWRegCta = N * Vec<T>::N * (1 + (kRms ? 0 : 1) + (kBias ? 1 : 0)) <= 32;
+
+// Rows of two or four warps (G = 64 or 128 threads per row; 256 / G rows
+// per tile): for widths whose lane-group accumulators would not fit in
+// registers (LayerNorm from 6 vectors per lane, with dbias from 4), without
+// the one-row-per-CTA-step latency of the CTA-per-row kernel. The row sums
+// are added across the group's warps through shared memory behind a named
+// barrier of the group's threads; w is staged in shared memory as fp32.
+// Bodies synchronise within groups, so the loop runs in the uniform mode
+// (a thread whose wait timed out still runs the body; its group leaves
+// together after it, and every other group at its own next check).
+template <typename T, int G, int N, bool kRms, bool kBias>
+__global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_group_kernel(const BwdArgs a,
+                                                                          const BulkCfg c) {
+  static_assert(G == 64 || G == 128, "row groups of two or four warps");
+  constexpr int WPR = G / 32;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ float red[kBulkThreads / G][G * Vec<T>::N];
+  __shared__ float2 xch[2][kConsumerWarps];
+  __shared__ int s_abort;
+  __shared__ long long s_taken;
+  const int H = a.hidden;
+  const uint32_t in_bytes = (uint32_t)c.tile_rows * H * sizeof(T);
+  const Ring ring = make_ring(smem, 2 * in_bytes, c.stages);
+  float* w_s = reinterpret_cast<float*>(ring.after);
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    s_taken = 0x7fffffffffffffffll;
+  }
+  const ParamRow<T> wr = {w_s, static_cast<const T*>(a.gamma), H, a.zero_centered != 0};
+  stage_param_row<T>(wr.g, H, wr.plus_one, w_s);
+  ring_init(ring);
+
+  const int local = threadIdx.x / G;   // row within the tile
+  const int t = threadIdx.x % G;
+  const int warp = threadIdx.x >> 5;
+  float2 wreg[N][Vec<T>::N / 2];   // unused: w is staged in shared memory
+  float2 acc_g[N][Vec<T>::N / 2], acc_b[N][Vec<T>::N / 2], acc_d[N][Vec<T>::N / 2];
+  zero_acc2<T, N>(acc_g);
+  zero_acc2<T, N>(acc_b);
+  zero_acc2<T, N>(acc_d);
+  auto load_stats = [&](int64_t tile, float& m, float& r) {
+    const int64_t row = tile * c.tile_rows + local;
+    m = 0.f;
+    r = 0.f;
+    if (tile < c.num_tiles && row < a.rows) {
+      r = a.rstd[row];
+      if (!a.rms) m = a.mean[row];
+    }
+  };
+  // Sum of a float2 over the group: warp butterfly, then the group's warps
+  // in order through a double-buffered exchange (one barrier per call).
+  int parity = 0;
+  auto row_sum = [&](float2 v) {
+    v = group_sum2<32>(v);
+    if ((threadIdx.x & 31) == 0) xch[parity][warp] = v;
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + local), "r"(G) : "memory");
+    float2 s = xch[parity][local * WPR];
+#pragma unroll
+    for (int i = 1; i < WPR; ++i) {
+      s.x += xch[parity][local * WPR + i].x;
+      s.y += xch[parity][local * WPR + i].y;
+    }
+    parity ^= 1;
+    return s;
+  };
+  float nm, nr;
+  load_stats(blockIdx.x, nm, nr);
+  bool aborted = false;
+  const int64_t taken = run_pipeline<true, T>(
+      ring, c, a.rows, H, static_cast<const T*>(a.dy), static_cast<const T*>(a.x_sum), aborted,
+      [&](int64_t tile, unsigned char* slot) {
+        const float mean = nm, rstd = nr;
+        load_stats(tile + gridDim.x, nm, nr);
+        const int64_t row = tile * c.tile_rows + local;
+        const uint32_t dys = smem_addr(slot) + (uint32_t)(local * H * sizeof(T));
+        const uint32_t xss = dys + in_bytes;
+        bwd_row_smem<T, G, N, kRms, kBias, true, false>(a, row, row < a.rows, t, dys, xss, wr,
+                                                        wreg, mean, rstd, row_sum, acc_g,
+                                                        acc_b, acc_d);
+      });
+  if (pipeline_finish(ring, aborted, taken, &s_abort, &s_taken)) return;
+  float fg[N][Vec<T>::N], fb[N][Vec<T>::N], fd[N][Vec<T>::N];
+  unpair_acc<T, N>(acc_g, fg);
+  unpair_acc<T, N>(acc_b, fb);
+  unpair_acc<T, N>(acc_d, fd);
+  store_rowgroup_partials<T, G, N, kRms, kBias>(a, fg, fb, fd, red);
+}
 
 template <typename T, int N, bool kRms, bool kBias>
 __global__ void __launch_bounds__(kBulkThreads, 2)

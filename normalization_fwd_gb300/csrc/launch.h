@@ -18,7 +18,7 @@ constexpr int kMaxHiddenScalar = 8192;    // scalar kernels (shared-memory stage
 struct Plan {
   const void* fn = nullptr;
   bool bulk = false;   // pipelined kernel taking (args, BulkCfg)
-  int kind = -1;       // 0 lane group per row, 1 CTA per row, 2 scalar
+  int kind = -1;       // 0 lane group per row, 1 CTA per row, 2 scalar, 3 row group (backward)
   int group = 0;       // threads sharing a row
   int n = 0;           // 16-byte vectors per thread per row
   int block = 0;
@@ -31,6 +31,9 @@ struct Plan {
 // Per-device facts, cached (api.cu).
 int device_sm_count(int* sms);                                  // returns cudaError_t
 int resident_blocks(const void* fn, int block, size_t smem, int* out);  // returns cudaError_t
+// Opt `fn` in to `smem` bytes of dynamic shared memory when that plus its
+// static shared memory passes the default 48 KiB (cached per kernel).
+int allow_dyn_smem(const void* fn, size_t smem);  // returns cudaError_t
 
 // Kernel family override from the NORMFUSE_PATH environment variable
 // ("registers" selects the register kernels for aligned rows), read once.

@@ -43,6 +43,28 @@ inline Choice choose(int hidden, int vec_elems, bool vec) {
   return {-1, 0, 0};
 }
 
+// Accumulator floats per thread a pipelined backward may keep without
+// spilling (ptxas, 2 CTAs per SM: LayerNorm lane groups spill from 6 vectors
+// of 8 per lane, LayerNorm with dbias from 4).
+constexpr int kMaxAccFloats = 80;
+
+// A backward lane group whose accumulators (n * VEC floats per reduction:
+// dgamma; dbeta for LayerNorm; dbias) would not fit moves to a row group of
+// 64 or 128 threads (kind 3), the smallest that fits.
+inline Choice bwd_choice(const Choice& c, int hidden, int vec_elems, bool rms, bool dbias) {
+  if (c.kind != 0) return c;
+  const int n_acc = 1 + (rms ? 0 : 1) + (dbias ? 1 : 0);
+  if (c.n * vec_elems * n_acc <= kMaxAccFloats) return c;
+  const int V = hidden / vec_elems;
+  for (int g : {64, 128}) {
+    int n = (V + g - 1) / g;
+    if (n == 7) n = 8;
+    if (n < 2) n = 2;
+    if (n * vec_elems * n_acc <= kMaxAccFloats) return {3, g, n};
+  }
+  return c;
+}
+
 // Vectors per consumer thread when the 256 consumers of a pipelined CTA
 // share one row (rows of more than 256 vectors).
 inline int bulk_cta_n(int hidden, int vec_elems) {
@@ -102,7 +124,8 @@ inline size_t ring_target(bool bwd, bool three_ctas) {
 // shared bytes after the ring's barriers (the backward's fp32 weight row).
 inline bool fill_bulk(Plan* p, const Choice& c, int64_t rows, int hidden, size_t esize, int n_in,
                       size_t extra, size_t target) {
-  const int tile_rows = c.kind == 0 ? kConsumerWarps * (32 / c.group) : 1;
+  const int tile_rows = c.kind == 0 ? kConsumerWarps * (32 / c.group)
+                                    : (c.kind == 3 ? kBulkThreads / c.group : 1);
   const size_t slot = (size_t)n_in * tile_rows * hidden * esize;
   const size_t room = target > extra ? target - extra : 0;
   int stages = (int)std::min<size_t>(8, std::max<size_t>(2, room / slot));
@@ -110,7 +133,7 @@ inline bool fill_bulk(Plan* p, const Choice& c, int64_t rows, int hidden, size_t
   if (smem > kMaxDynSmem) return false;
   p->bulk = true;
   p->kind = c.kind;
-  p->group = c.kind == 0 ? c.group : kBulkThreads;
+  p->group = (c.kind == 0 || c.kind == 3) ? c.group : kBulkThreads;
   p->n = c.n;
   p->block = kBulkThreads;
   p->smem = smem;
@@ -145,13 +168,10 @@ inline int64_t fill_shape(Plan* p, const Choice& c, int hidden, bool bwd, bool d
 // Persistent grid: every CTA resident at once, never more CTAs than row steps.
 inline cudaError_t size_grid(Plan* p, int64_t steps) {
   if (p->fn == nullptr) return cudaErrorInvalidValue;
-  if (p->smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(p->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)p->smem);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = (cudaError_t)allow_dyn_smem(p->fn, p->smem);
+  if (e != cudaSuccess) return e;
   int sms = 0, per_sm = 0;
-  cudaError_t e = (cudaError_t)device_sm_count(&sms);
+  e = (cudaError_t)device_sm_count(&sms);
   if (e != cudaSuccess) return e;
   e = (cudaError_t)resident_blocks(p->fn, p->block, p->smem, &per_sm);
   if (e != cudaSuccess) return e;
@@ -171,11 +191,11 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
   if (bwd && dbias && vec && path_override() == kPathRegisters) c = choose(hidden, 1, false);
   const bool want_bulk = vec && path_override() != kPathRegisters;
   if (want_bulk) {
-    Choice b = c;
+    Choice b = bwd ? bwd_choice(c, hidden, Vec<T>::N, rms, dbias) : c;
     if (c.kind == 1) b.n = bulk_cta_n(hidden, Vec<T>::N);
-    // Lane-group kernels stage the parameter rows in shared memory as fp32;
-    // CTA-per-row kernels read them from global memory.
-    const size_t extra = b.kind == 0 ? (size_t)n_params * hidden * sizeof(float) : 0;
+    // Lane-group and row-group kernels stage the parameter rows in shared
+    // memory as fp32; CTA-per-row kernels read them from global memory.
+    const size_t extra = (b.kind == 0 || b.kind == 3) ? (size_t)n_params * hidden * sizeof(float) : 0;
     const bool three = !bwd && b.kind == 0 && b.n <= 4;
     const size_t target = ring_target(bwd, three);
     if (fill_bulk(p, b, rows, hidden, sizeof(T), n_in, extra, target)) {

@@ -48,6 +48,16 @@ namespace nf {
     case 8: return (const void*)KERNEL<T, 8, M, B>;   \
     default: return nullptr;                          \
   }
+#define NF_BULK_GROUP_CASES_M(KERNEL, T, G, M, B)     \
+  switch (n) {                                        \
+    case 2: return (const void*)KERNEL<T, G, 2, M, B>; \
+    case 3: return (const void*)KERNEL<T, G, 3, M, B>; \
+    case 4: return (const void*)KERNEL<T, G, 4, M, B>; \
+    case 5: return (const void*)KERNEL<T, G, 5, M, B>; \
+    case 6: return (const void*)KERNEL<T, G, 6, M, B>; \
+    case 8: return (const void*)KERNEL<T, G, 8, M, B>; \
+    default: return nullptr;                          \
+  }
 #define NF_BULK_CTA_CASES(KERNEL, T)               \
   switch (n) {                                     \
     case 2: return (const void*)KERNEL<T, 2>;      \
@@ -93,6 +103,9 @@ const void* bwd_bulk_table_impl(int kind, int group, int n) {
     if (group == 32) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 32, kRms, kBias) }
   } else if (kind == 1) {
     NF_BULK_CTA_CASES_M(bwd_bulk_cta_kernel, T, kRms, kBias)
+  } else if (kind == 3) {
+    if (group == 64) { NF_BULK_GROUP_CASES_M(bwd_bulk_group_kernel, T, 64, kRms, kBias) }
+    if (group == 128) { NF_BULK_GROUP_CASES_M(bwd_bulk_group_kernel, T, 128, kRms, kBias) }
   }
   return nullptr;
 }
