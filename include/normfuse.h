@@ -152,7 +152,8 @@ ln_status ln_fwd_ex(const void* x, const void* bias, const void* residual,
  * dx is also the gradient of the residual and of x through the identity add.
  * dgamma and dbeta are bitwise reproducible from run to run on the same GPU
  * model: the row-to-CTA assignment depends only on the SM count and the
- * finalize adds the partials in a fixed order (in fp64).
+ * finalize adds the partials in a fixed order (compensated fp32 sums, exact
+ * up to the rounding of the compensation term, rounded once at the end).
  *
  * dy, x_sum [rows, hidden] dtype, required (x_sum is the forward's out_sum,
  *           or x itself when the forward had neither bias nor residual).
@@ -190,9 +191,9 @@ ln_status ln_bwd(const void* dy, const void* x_sum, const void* gamma,
  * dbias     [hidden] grad_dtype, NULL = not computed.
  * grad_dtype  the type of dgamma, dbeta and dbias: LN_F32 (as in ln_bwd), or
  *           LN_BF16 / LN_F16 for the low-precision epilogue PR 165370 names
- *           (a down cast after the outer reduction): the fixed-order fp64
- *           total of each column is rounded once, to nearest even, to that
- *           type. dgamma/dbeta/dbias must then be aligned to its size.
+ *           (a down cast after the outer reduction): the fixed-order
+ *           compensated total of each column is rounded once, to nearest
+ *           even, to that type. dgamma/dbeta/dbias must then be aligned to its size.
  * With dbias NULL and grad_dtype LN_F32 this is ln_bwd. Every other
  * argument, the workspace rule and the errors are those of ln_bwd;
  * ln_bwd_workspace_bytes() covers both entry points.

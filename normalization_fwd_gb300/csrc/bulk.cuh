@@ -404,6 +404,14 @@ __device__ __forceinline__ int64_t run_pipeline(const Ring& ring, const BulkCfg&
   return it;
 }
 
+// Programmatic dependent launch: let the grid launched after this one on
+// the stream (the backward's finalize) be scheduled once every CTA of this
+// grid has called this; the dependent still waits (griddepcontrol.wait) for
+// this grid to complete and its writes to be visible before it reads them.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // End of a pipelined kernel, all threads: record an abort in the error word,
 // and on abort let thread 0 drain the copies still in flight. Returns true
 // when the kernel aborted (the caller then skips its epilogue).

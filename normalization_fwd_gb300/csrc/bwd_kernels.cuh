@@ -11,8 +11,8 @@
 // kernel adds the partials of all CTAs in a fixed order.
 //
 // The row -> CTA assignment is a grid-stride loop over a grid sized from the
-// SM count, so the partials, and the finalize's fixed-order fp64 sum over
-// them, are the same on every run.
+// SM count, so the partials, and the finalize's fixed-order compensated sum
+// over them, are the same on every run.
 //
 //  * bwd_bulk_warp_kernel / bwd_bulk_cta_kernel (default for 16-byte aligned
 //    rows): dy and x_sum tiles stream into a shared-memory ring by
@@ -462,6 +462,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
             a, row, row < a.rows, l, dys, xss, wr, wreg, mean, rstd,
             [](float2 v) { return group_sum2<LANES>(v); }, acc_g, acc_b, acc_d);
       });
+  allow_dependent_launch();
   if (pipeline_finish(ring, aborted, taken, &s_abort, &s_taken)) return;
   float fg[N][Vec<T>::N], fb[N][Vec<T>::N], fd[N][Vec<T>::N];
   unpair_acc<T, N>(acc_g, fg);
@@ -554,6 +555,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_group_kernel(const B
                                                         wreg, mean, rstd, row_sum, acc_g,
                                                         acc_b, acc_d);
       });
+  allow_dependent_launch();
   if (pipeline_finish(ring, aborted, taken, &s_abort, &s_taken)) return;
   float fg[N][Vec<T>::N], fb[N][Vec<T>::N], fd[N][Vec<T>::N];
   unpair_acc<T, N>(acc_g, fg);
@@ -617,6 +619,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2)
             [&](float2 v) { return cta_sum2_db<kBulkThreads>(v, red, parity); }, acc_g, acc_b,
             acc_d);
       });
+  allow_dependent_launch();
   if (pipeline_finish(ring, aborted, taken, &s_abort, &s_taken)) return;
   float fg[N][Vec<T>::N], fb[N][Vec<T>::N], fd[N][Vec<T>::N];
   unpair_acc<T, N>(acc_g, fg);

@@ -5,44 +5,66 @@
 
 namespace nf {
 
-constexpr int kFinCols = 8;      // columns per block: one 32-byte sector of a partial row
-constexpr int kFinSlices = 128;  // partial rows are dealt round-robin to this many slices
+constexpr int kFinCols = 32;    // columns per block: one 128-byte line of a partial row
+constexpr int kFinSlices = 32;  // partial rows are dealt round-robin to this many slices
+
+// Error-free sum of two floats (Knuth's TwoSum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bp = s - a;
+  e = (a - (s - bp)) + (b - bp);
+}
+
+// (s, c) += x, carrying the rounding error of every add in c (compensated
+// summation): the pair holds the exact running sum up to the rounding of c.
+__device__ __forceinline__ void comp_add(float& s, float& c, float x) {
+  float e;
+  two_sum(s, x, s, e);
+  c += e;
+}
 
 // dgamma[j] = sum_p ws[p][j] (and likewise dbeta, dbias from their column
-// ranges) over the P CTA partials, in a fixed order that depends only on P:
-// partial row p goes to slice p % 128; each slice is summed in increasing p;
-// then slices 32q .. 32q + 31 are summed in increasing order for q = 0..3, and
-// the four results in increasing q. All sums are fp64.
+// ranges) over the P CTA partials, in an order that depends only on P:
+// partial row p goes to slice p % 32, each slice is summed in increasing p,
+// and the 32 slices are combined by a fixed pairwise tree (slice y with
+// y + 16, then y + 8, ...). Sums are compensated fp32 pairs; the column
+// total s + c is formed once in fp64 and rounded once to the output type
+// (out_dtype 0 fp32, 1 bf16, 2 fp16). fp64 arithmetic is slow on this part,
+// so it is used for that single add only.
 //
-// The totals are written as fp32, or (out_dtype 1 / 2) rounded once from
-// fp64 to bf16 / fp16: the low-precision epilogue of the outer reductions.
-//
-// Block (8, 128): thread (x, y) owns column blockIdx.x * 8 + x and slice y,
-// so one warp reads four partial rows of 8 consecutive columns (four full
-// 32-byte sectors) and every thread has only ceil(P / 128) loads to wait for.
+// Block (32, 32): thread (x, y) owns column blockIdx.x * 32 + x and slice y,
+// so a warp reads 128 contiguous bytes of one partial row and every thread
+// waits for only ceil(P / 32) independent loads.
 __global__ void __launch_bounds__(kFinCols* kFinSlices)
     bwd_finalize_kernel(const float* __restrict__ ws, int P, int C, int H, int beta_cols,
                         void* dgamma, void* dbeta, void* dbias, int out_dtype) {
-  __shared__ double part[kFinSlices][kFinCols];
-  __shared__ double quarter[4][kFinCols];
+  __shared__ float ps[kFinSlices][kFinCols + 1];
+  __shared__ float pc[kFinSlices][kFinCols + 1];
+  // Launched as a programmatic dependent of the backward kernel: wait until
+  // that grid has completed and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int x = threadIdx.x, y = threadIdx.y;
   const int c = blockIdx.x * kFinCols + x;
-  double acc = 0.0;
+  float s = 0.f, e = 0.f;
   if (c < C) {
-#pragma unroll 4
-    for (int p = y; p < P; p += kFinSlices) acc += (double)ws[(int64_t)p * C + c];
-  }
-  part[y][x] = acc;
-  __syncthreads();
-  if (y < 4) {
-    double t = 0.0;
 #pragma unroll 8
-    for (int i = 0; i < 32; ++i) t += part[32 * y + i][x];
-    quarter[y][x] = t;
+    for (int p = y; p < P; p += kFinSlices) comp_add(s, e, ws[(int64_t)p * C + c]);
   }
+  ps[y][x] = s;
+  pc[y][x] = e;
   __syncthreads();
+#pragma unroll
+  for (int half = kFinSlices / 2; half > 0; half >>= 1) {
+    if (y < half) {
+      float t, r;
+      two_sum(ps[y][x], ps[y + half][x], t, r);
+      ps[y][x] = t;
+      pc[y][x] = pc[y][x] + pc[y + half][x] + r;
+    }
+    __syncthreads();
+  }
   if (y == 0 && c < C) {
-    const double t = ((quarter[0][x] + quarter[1][x]) + quarter[2][x]) + quarter[3][x];
+    const double t = (double)ps[0][x] + (double)pc[0][x];   // exact
     void* out = nullptr;
     int j = 0;
     if (c < H) {
@@ -70,9 +92,21 @@ __global__ void __launch_bounds__(kFinCols* kFinSlices)
 cudaError_t launch_bwd_finalize(const float* ws, int P, int C, int H, bool beta_cols,
                                 void* dgamma, void* dbeta, void* dbias, int out_dtype,
                                 cudaStream_t st) {
-  bwd_finalize_kernel<<<(C + kFinCols - 1) / kFinCols, dim3(kFinCols, kFinSlices), 0, st>>>(
-      ws, P, C, H, beta_cols ? 1 : 0, dgamma, dbeta, dbias, out_dtype);
-  return cudaGetLastError();
+  // Programmatic stream serialization: the finalize may be scheduled while
+  // the backward kernel drains; griddepcontrol.wait above orders its reads.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((C + kFinCols - 1) / kFinCols);
+  cfg.blockDim = dim3(kFinCols, kFinSlices);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int bc = beta_cols ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, bwd_finalize_kernel, ws, P, C, H, bc, dgamma, dbeta, dbias,
+                            out_dtype);
 }
 
 }  // namespace nf
