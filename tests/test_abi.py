@@ -212,3 +212,18 @@ def test_binding_fails_loudly_without_library(tmp_path):
             mod.load_library(missing)
     finally:
         mod._lib = saved
+
+
+def test_cuda_errors_propagate_as_status_without_a_device(lib):
+    # Where no CUDA device is usable, the calls that only query the device
+    # (no launch, no pointer dereference) must return LN_ERR_CUDA and leave
+    # the CUDA error code readable, never abort.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is visible: covered by the GPU tests")
+    out = ctypes.c_size_t(0)
+    assert lib.ln_bwd_workspace_bytes(1024, 384, 1, 0, ctypes.byref(out)) == CUDA
+    assert lib.ln_last_cuda_error() != 0
+    flags = ctypes.c_uint(7)
+    assert lib.ln_device_error(None, ctypes.byref(flags)) == CUDA
+    assert nf.ln_status_string(CUDA).startswith("LN_ERR_CUDA")
