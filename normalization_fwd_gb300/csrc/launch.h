@@ -18,7 +18,8 @@ constexpr int kMaxHiddenScalar = 8192;    // scalar kernels (shared-memory stage
 struct Plan {
   const void* fn = nullptr;
   bool bulk = false;   // pipelined kernel taking (args, BulkCfg)
-  int kind = -1;       // 0 lane group per row, 1 CTA per row, 2 scalar, 3 row group (backward)
+  int kind = -1;       // 0 lane group per row, 1 CTA per row, 2 scalar, 3 row group (backward),
+                       // 4 lane group from registers, one CTA per row tile (softmax)
   int group = 0;       // threads sharing a row
   int n = 0;           // 16-byte vectors per thread per row
   int block = 0;

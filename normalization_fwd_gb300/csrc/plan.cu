@@ -2,6 +2,7 @@
 // block and shared memory, and the launch itself. Kernels come from the
 // per-family tables of the kernel translation units (tables.cuh).
 #include <stdlib.h>
+#include <string.h>
 
 #include <algorithm>
 
@@ -253,6 +254,43 @@ cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, void* dgamma, void* dbet
 // Wider rows (more registers, two CTAs per SM) keep the 104 KiB ring.
 template <typename T> cudaError_t softmax_plan(int64_t rows, int hidden, bool vec, Plan* p) {
   const Choice c = choose(hidden, Vec<T>::N, vec);
+  static const int smx_path = [] {
+    const char* e = getenv("NORMFUSE_SMX_PATH");   // "ring": the pipelined kernels
+    return (e && strcmp(e, "ring") == 0) ? 1 : 0;
+  }();
+  if (smx_path == 0 && c.kind == 1) {
+    // Rows of more than 256 vectors: one CTA per row from registers.
+    p->bulk = false;
+    p->kind = 5;
+    p->group = kBulkThreads;
+    p->n = bulk_cta_n(hidden, Vec<T>::N);
+    p->block = kBulkThreads;
+    p->smem = 0;
+    p->fn = Tables<T>::softmax(5, kBulkThreads, p->n);
+    cudaError_t e = size_grid(p, 1);
+    if (e != cudaSuccess) return e;
+    if (rows > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    p->grid = (int)rows;
+    return cudaSuccess;
+  }
+  if (smx_path == 0 && c.kind == 0) {
+    // Lane groups of up to 4 vectors: rows straight into registers, one CTA
+    // per 8 * (32 / lanes) rows, as many CTAs as the rows need.
+    p->bulk = false;
+    p->kind = 4;
+    p->group = c.group;
+    p->n = c.n;
+    p->block = kBulkThreads;
+    p->smem = 0;
+    p->fn = Tables<T>::softmax(4, c.group, c.n);
+    cudaError_t e = size_grid(p, 1);   // occupancy check and attributes
+    if (e != cudaSuccess) return e;
+    const int64_t rpc = (int64_t)kConsumerWarps * (32 / c.group);
+    const int64_t ctas = (rows + rpc - 1) / rpc;
+    if (ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    p->grid = (int)ctas;
+    return cudaSuccess;
+  }
   if (c.kind == 0 || c.kind == 1) {
     Choice b = c;
     if (c.kind == 1) b.n = bulk_cta_n(hidden, Vec<T>::N);
