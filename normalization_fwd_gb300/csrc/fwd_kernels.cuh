@@ -227,13 +227,14 @@ __device__ __forceinline__ FwdParams<T> fwd_params(const FwdArgs& a, float* p_s)
   return p;
 }
 
-// The row body of the pipelined kernels: x and residual rows in shared
-// memory (ring slot), parameters staged in shared memory (kStaged) or read
-// from global memory. Values are kept as fp32 pairs (packed fp32 math).
+// The row body: `xr` / `rr` hold the thread's 16-byte vectors k * G + t of
+// the x and residual rows (those below V; rr only with a residual),
+// parameters staged in shared memory (kStaged) or read from global memory.
+// Values are kept as fp32 pairs (packed fp32 math).
 template <typename T, int G, int N, bool kStaged, typename Reduce>
-__device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool row_ok, int t,
-                                             uint32_t xrow, uint32_t rrow, bool has_res,
-                                             const FwdParams<T>& p, Reduce reduce,
+__device__ __forceinline__ void fwd_row_regs(const FwdArgs& a, int64_t row, bool row_ok, int t,
+                                             const uint4 (&xr)[N], const uint4 (&rr)[N],
+                                             bool has_res, const FwdParams<T>& p, Reduce reduce,
                                              unsigned& amax_acc, bool write_stats) {
   constexpr int VEC = Vec<T>::N;
   constexpr int P = VEC / 2;
@@ -255,7 +256,7 @@ __device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool
 #pragma unroll
     for (int i = 0; i < P; ++i) s[k][i] = splat2(0.f);
     if (row_ok && v < V) {
-      unpack2<T>(lds_u4(xrow + v * 16), s[k]);
+      unpack2<T>(xr[k], s[k]);
       if (p.bias.g) {
         float2 b[P];
         p.bias.template load2<kStaged>(v, b, bia);
@@ -264,7 +265,7 @@ __device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool
       }
       if (has_res) {
         float2 r[P];
-        unpack2<T>(lds_u4(rrow + v * 16), r);
+        unpack2<T>(rr[k], r);
 #pragma unroll
         for (int i = 0; i < P; ++i) s[k][i] = add2(s[k][i], r[i]);
       }
@@ -319,6 +320,69 @@ __device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool
         unpack2<T>(packed, o);
         store_fp8<VEC>(a.y_fp8 + row * (int64_t)H + v * VEC, o, p.fp8_scale);
       }
+    }
+  }
+}
+
+// The same row with its vectors read from shared memory (the ring slot).
+template <typename T, int G, int N, bool kStaged, typename Reduce>
+__device__ __forceinline__ void fwd_row_smem(const FwdArgs& a, int64_t row, bool row_ok, int t,
+                                             uint32_t xrow, uint32_t rrow, bool has_res,
+                                             const FwdParams<T>& p, Reduce reduce,
+                                             unsigned& amax_acc, bool write_stats) {
+  const int V = a.hidden / Vec<T>::N;
+  uint4 xr[N], rr[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int v = k * G + t;
+    if (row_ok && v < V) {
+      xr[k] = lds_u4(xrow + v * 16);
+      if (has_res) rr[k] = lds_u4(rrow + v * 16);
+    }
+  }
+  fwd_row_regs<T, G, N, kStaged>(a, row, row_ok, t, xr, rr, has_res, p, reduce, amax_acc,
+                                 write_stats);
+}
+
+// One CTA per tile of 8 * (32 / LANES) rows, as many CTAs as tiles: rows go
+// straight from global memory into registers (no ring) and the CTA scheduler
+// keeps loads in flight as CTAs end and start. Parameters come from global
+// memory (L1/L2-resident). amax: a CTA issues its atomicMax only when its
+// maximum beats the value already there.
+template <typename T, int LANES, int N>
+__global__ void __launch_bounds__(kBulkThreads, N <= 3 ? 4 : 2) fwd_tile_kernel(const FwdArgs a) {
+  constexpr int RPW = 32 / LANES;
+  constexpr int VEC = Vec<T>::N;
+  __shared__ unsigned red_amax[kConsumerWarps];
+  const int lane = threadIdx.x & 31;
+  const int l = lane % LANES;
+  const int64_t row =
+      ((int64_t)blockIdx.x * kConsumerWarps + (threadIdx.x >> 5)) * RPW + lane / LANES;
+  const bool row_ok = row < a.rows;
+  const int H = a.hidden;
+  const int V = H / VEC;
+  const T* x = static_cast<const T*>(a.x) + row * (int64_t)H;
+  const T* res = a.residual ? static_cast<const T*>(a.residual) + row * (int64_t)H : nullptr;
+  uint4 xr[N], rr[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int v = k * LANES + l;
+    if (row_ok && v < V) {
+      xr[k] = ld_vec(x + v * VEC);
+      if (res) rr[k] = ld_vec(res + v * VEC);
+    }
+  }
+  const FwdParams<T> p = fwd_params<T>(a, nullptr);
+  unsigned amax_acc = 0;
+  fwd_row_regs<T, LANES, N, false>(a, row, row_ok, l, xr, rr, res != nullptr, p,
+                                   [](float v) { return group_sum<LANES>(v); }, amax_acc, l == 0);
+  if (a.amax) {
+    unsigned m = __reduce_max_sync(0xffffffffu, amax_bits<T>(amax_acc));
+    if (lane == 0) red_amax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int i = 1; i < kConsumerWarps; ++i) m = max(m, red_amax[i]);
+      if (m > *(volatile unsigned*)a.amax) atomicMax(a.amax, m);
     }
   }
 }

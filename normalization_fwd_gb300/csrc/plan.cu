@@ -184,10 +184,36 @@ inline cudaError_t size_grid(Plan* p, int64_t steps) {
 // Plan shared by both directions. n_in: streamed [rows, hidden] inputs;
 // n_params: [hidden] parameter rows the pipelined kernels stage in shared
 // memory as fp32.
+// Forward lane groups: one CTA per row tile from registers (kind 4, the
+// default) or the bulk-copy ring (NORMFUSE_FWD_PATH=ring).
+inline bool fwd_tile_path() {
+  static const bool v = [] {
+    const char* e = getenv("NORMFUSE_FWD_PATH");
+    return !(e && strcmp(e, "ring") == 0);
+  }();
+  return v;
+}
+
 template <typename T>
 cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bool dbias,
                       int n_in, int n_params, Plan* p) {
   Choice c = choose(hidden, Vec<T>::N, vec);
+  if (!bwd && vec && c.kind == 0 && path_override() != kPathRegisters && fwd_tile_path()) {
+    p->bulk = false;
+    p->kind = 4;
+    p->group = c.group;
+    p->n = c.n;
+    p->block = kBulkThreads;
+    p->smem = 0;
+    p->fn = Tables<T>::fwd_bulk(4, c.group, c.n);
+    cudaError_t e = size_grid(p, 1);   // occupancy check and attributes
+    if (e != cudaSuccess) return e;
+    const int64_t rpc = (int64_t)kConsumerWarps * (32 / c.group);
+    const int64_t ctas = (rows + rpc - 1) / rpc;
+    if (ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    p->grid = (int)ctas;
+    return cudaSuccess;
+  }
   // The register kernels do not accumulate dbias; the scalar kernel does.
   if (bwd && dbias && vec && path_override() == kPathRegisters) c = choose(hidden, 1, false);
   const bool want_bulk = vec && path_override() != kPathRegisters;
