@@ -387,6 +387,46 @@ __global__ void __launch_bounds__(kBulkThreads, N <= 3 ? 4 : 2) fwd_tile_kernel(
   }
 }
 
+// Rows of more than 256 vectors from registers: one CTA per row, as many
+// CTAs as rows; the row sums go through the CTA (double-buffered, one
+// barrier each).
+template <typename T, int N>
+__global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 3 : 2) fwd_tile_cta_kernel(const FwdArgs a) {
+  constexpr int VEC = Vec<T>::N;
+  __shared__ float red[2][kConsumerWarps];
+  __shared__ unsigned red_amax[kConsumerWarps];
+  const int64_t row = blockIdx.x;
+  const int H = a.hidden;
+  const int V = H / VEC;
+  const T* x = static_cast<const T*>(a.x) + row * (int64_t)H;
+  const T* res = a.residual ? static_cast<const T*>(a.residual) + row * (int64_t)H : nullptr;
+  uint4 xr[N], rr[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int v = k * kBulkThreads + threadIdx.x;
+    if (v < V) {
+      xr[k] = ld_vec(x + v * VEC);
+      if (res) rr[k] = ld_vec(res + v * VEC);
+    }
+  }
+  const FwdParams<T> p = fwd_params<T>(a, nullptr);
+  unsigned amax_acc = 0;
+  int parity = 0;
+  fwd_row_regs<T, kBulkThreads, N, false>(
+      a, row, true, threadIdx.x, xr, rr, res != nullptr, p,
+      [&](float v) { return cta_sum_db<kBulkThreads>(v, red, parity); }, amax_acc,
+      threadIdx.x == 0);
+  if (a.amax) {
+    unsigned m = __reduce_max_sync(0xffffffffu, amax_bits<T>(amax_acc));
+    if ((threadIdx.x & 31) == 0) red_amax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int i = 1; i < kConsumerWarps; ++i) m = max(m, red_amax[i]);
+      if (m > *(volatile unsigned*)a.amax) atomicMax(a.amax, m);
+    }
+  }
+}
+
 template <typename T, int LANES, int N>
 __global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 3 : 2) fwd_bulk_warp_kernel(const FwdArgs a,
                                                                          const BulkCfg c) {

@@ -184,8 +184,9 @@ inline cudaError_t size_grid(Plan* p, int64_t steps) {
 // Plan shared by both directions. n_in: streamed [rows, hidden] inputs;
 // n_params: [hidden] parameter rows the pipelined kernels stage in shared
 // memory as fp32.
-// Forward lane groups: one CTA per row tile from registers (kind 4, the
-// default) or the bulk-copy ring (NORMFUSE_FWD_PATH=ring).
+// Forward: rows straight into registers with one CTA per row tile (kind 4,
+// lane groups) or per row (kind 5, rows of more than 256 vectors), the
+// default; NORMFUSE_FWD_PATH=ring selects the bulk-copy ring kernels.
 inline bool fwd_tile_path() {
   static const bool v = [] {
     const char* e = getenv("NORMFUSE_FWD_PATH");
@@ -198,6 +199,20 @@ template <typename T>
 cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bool dbias,
                       int n_in, int n_params, Plan* p) {
   Choice c = choose(hidden, Vec<T>::N, vec);
+  if (!bwd && vec && c.kind == 1 && path_override() != kPathRegisters && fwd_tile_path()) {
+    p->bulk = false;
+    p->kind = 5;
+    p->group = kBulkThreads;
+    p->n = bulk_cta_n(hidden, Vec<T>::N);
+    p->block = kBulkThreads;
+    p->smem = 0;
+    p->fn = Tables<T>::fwd_bulk(5, kBulkThreads, p->n);
+    cudaError_t e = size_grid(p, 1);
+    if (e != cudaSuccess) return e;
+    if (rows > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    p->grid = (int)rows;
+    return cudaSuccess;
+  }
   if (!bwd && vec && c.kind == 0 && path_override() != kPathRegisters && fwd_tile_path()) {
     p->bulk = false;
     p->kind = 4;

@@ -74,6 +74,8 @@ template <typename T> const void* fwd_bulk_table_impl(int kind, int group, int n
     if (group == 8) { NF_WARP_CASES(fwd_bulk_warp_kernel, T, 8) }
     if (group == 16) { NF_WARP_CASES(fwd_bulk_warp_kernel, T, 16) }
     if (group == 32) { NF_WARP_CASES(fwd_bulk_warp_kernel, T, 32) }
+  } else if (kind == 5) {
+    NF_BULK_CTA_CASES(fwd_tile_cta_kernel, T)
   } else if (kind == 4) {
     if (group == 8) { NF_WARP_CASES(fwd_tile_kernel, T, 8) }
     if (group == 16) { NF_WARP_CASES(fwd_tile_kernel, T, 16) }
