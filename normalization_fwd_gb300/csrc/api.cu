@@ -342,13 +342,13 @@ ln_status ln_bwd_workspace_bytes(int64_t rows, int64_t hidden, ln_dtype dtype, l
                             hidden <= max_hidden(dtype, true);
   if (!vec_possible && hidden > max_hidden(dtype, false)) return LN_ERR_SHAPE;
   size_t need = 0;
-  for (int v = 0; v < 2; ++v) {
-    const bool vec = v == 1;
+  for (int v = 0; v < 4; ++v) {
+    const bool vec = (v & 1) != 0;
+    const bool dbias = (v & 2) != 0;   // ln_bwd_ex's layout, so one query serves both calls
     if (vec && !vec_possible) continue;
     if (!vec && hidden > max_hidden(dtype, false)) continue;
-    // Sized for the largest layout (with dbias), so it serves ln_bwd_ex too.
     Plan p;
-    cudaError_t e = bwd_plan_any(dtype, rows, (int)hidden, rms, true, vec, &p);
+    cudaError_t e = bwd_plan_any(dtype, rows, (int)hidden, rms, dbias, vec, &p);
     if (e != cudaSuccess) return cuda_fail(e);
     const size_t b = (size_t)p.grid * (size_t)p.ws_cols * sizeof(float);
     if (b > need) need = b;

@@ -229,9 +229,16 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
     p->grid = (int)ctas;
     return cudaSuccess;
   }
-  // The register kernels do not accumulate dbias; the scalar kernel does.
-  if (bwd && dbias && vec && path_override() == kPathRegisters) c = choose(hidden, 1, false);
-  const bool want_bulk = vec && path_override() != kPathRegisters;
+  bool want_bulk = vec && path_override() != kPathRegisters;
+  // The register kernels do not accumulate dbias: in register mode a dbias
+  // call takes the scalar kernel when the row fits it, else the pipelined one.
+  if (bwd && dbias && vec && !want_bulk) {
+    if (hidden <= kMaxHiddenScalar) {
+      c = choose(hidden, 1, false);
+    } else {
+      want_bulk = true;
+    }
+  }
   if (want_bulk) {
     Choice b = bwd ? bwd_choice(c, hidden, Vec<T>::N, rms, dbias) : c;
     if (c.kind == 1) b.n = bulk_cta_n(hidden, Vec<T>::N);
