@@ -1,0 +1,44 @@
+"""bench.py's algorithmic byte model (the denominator of every roofline
+fraction) against byte counts written out tensor by tensor: each input read
+once, each output written once (workspace partials not counted)."""
+
+import bench
+import workloads as W
+
+
+def test_forward_bytes():
+    R, H = 576000, 384
+    # x, residual in; sum, y out (bf16); mean, rstd (fp32); gamma, beta, bias (bf16); amax
+    want = 2 * R * H * 2 + 2 * R * H * 2 + 2 * R * 4 + 3 * H * 2 + 4
+    assert want == 1_774_082_308
+    assert bench.fwd_bytes(W.BENCH_LN_BF16_576000x384) == want
+    R, H = 32768, 768     # the zero-centered fused add + LN + amax workload
+    assert bench.fwd_bytes(W.FWD_AMAX_BF16_32768x768) == 4 * R * H * 2 + 2 * R * 4 + 3 * H * 2 + 4
+    R, H = 16384, 8192    # RMSNorm: x, residual in; sum, y out; rstd; gamma
+    assert bench.fwd_bytes(W.RMS_BF16_16384x8192) == 4 * R * H * 2 + R * 4 + H * 2
+    assert bench.fwd_bytes(W.BENCH_RMS_BF16_16384x8192) == 4 * R * H * 2 + R * 4 + H * 2 + 4
+    R, H = 4096, 384      # fp32 LN with bias and residual, no amax
+    assert bench.fwd_bytes(W.LN_F32_4096x384) == 4 * R * H * 4 + 2 * R * 4 + 3 * H * 4
+
+
+def test_backward_bytes():
+    R, H = 576000, 384
+    # dy, x_sum in, dx out (bf16); mean, rstd in; gamma in; dgamma, dbeta out (fp32)
+    want = 3 * R * H * 2 + 2 * R * 4 + H * 2 + 2 * H * 4
+    assert want == 1_331_715_840
+    assert bench.bwd_bytes(W.BWD_BF16_576000x384_LN) == want
+    assert bench.bwd_bytes(W.BWD_BF16_576000x384_RMS) == 3 * R * H * 2 + R * 4 + H * 2 + H * 4
+    R, H = 16384, 8192
+    assert bench.bwd_bytes(W.RMS_BF16_16384x8192) == 3 * R * H * 2 + R * 4 + H * 2 + H * 4
+    for h, w in W.UNET_F16.items():
+        assert bench.bwd_bytes(w) == 3 * 8192 * h * 2 + 2 * 8192 * 4 + h * 2 + 2 * h * 4
+
+
+def test_softmax_bytes():
+    assert bench.softmax_bytes(W.SMX_BF16_576000x384) == 576000 * 384 * 2 * 2
+    assert bench.softmax_bytes(W.SMX_BF16_16384x8192) == 16384 * 8192 * 2 * 2
+
+
+def test_replica_throughput_counts_every_rank():
+    # whole-job rows/s: every replica's rows over the slowest rank's step time
+    assert bench.replica_throughput(1000, 4, 2.0) == 4 * 1000 / 2e-3
