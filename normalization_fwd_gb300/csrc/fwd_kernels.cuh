@@ -5,17 +5,20 @@
 //
 // Every kernel keeps a row on chip between the statistics and the normalize
 // step, so each input element is read from HBM once and each output written
-// once. Row loops are grid-stride loops over a grid sized to the CTAs that
-// are resident at once (persistent kernels), so the amax partial is
-// committed once per CTA.
+// once; the amax partial is committed once per CTA.
 //
-//  * fwd_bulk_warp_kernel / fwd_bulk_cta_kernel (default for 16-byte aligned
-//    rows): tiles of rows stream into a shared-memory ring by cp.async.bulk
-//    (every slot in flight, each refilled by the warp that frees it last) and
-//    8 warps normalize them from shared memory (a lane group of LANES lanes
-//    per row, or all 256 threads per row for rows longer than 256 vectors).
-//  * fwd_warp_kernel / fwd_cta_kernel: the same row body with the row loaded
-//    straight into registers (128-bit loads); used when the ring does not fit.
+//  * fwd_tile_kernel / fwd_tile_cta_kernel (default for 16-byte aligned
+//    rows): one CTA per tile of rows (a lane group of LANES lanes per row) or
+//    per row (rows of more than 256 vectors), as many CTAs as that takes;
+//    rows go straight from global memory into registers and the CTA
+//    scheduler keeps loads in flight as CTAs end and start.
+//  * fwd_bulk_warp_kernel / fwd_bulk_cta_kernel (NORMFUSE_FWD_PATH=ring):
+//    persistent CTAs; tiles of rows stream into a shared-memory ring by
+//    cp.async.bulk (every slot in flight, each refilled by the warp that
+//    frees it last) and 8 warps normalize them from shared memory.
+//  * fwd_warp_kernel / fwd_cta_kernel: persistent grid-stride loops with the
+//    row loaded straight into registers (NORMFUSE_PATH=registers, or when
+//    the ring does not fit).
 //  * fwd_scalar_kernel: any hidden size and alignment; element-wise loads,
 //    the row staged in shared memory.
 #pragma once

@@ -6,19 +6,21 @@
 // whole row stays on chip between the reductions, so each element is read
 // from HBM once and written once.
 //
-//  * smx_bulk_warp_kernel / smx_bulk_cta_kernel (16-byte aligned rows): tiles
-//    of rows stream into a shared-memory ring by cp.async.bulk (the ring and
-//    refill scheme of the normalization kernels) and 8 warps work on them
-//    from shared memory: a lane group of LANES lanes per row, or all 256
+//  * smx_reg_kernel / smx_reg_cta_kernel (default for 16-byte aligned rows):
+//    one CTA per tile of rows (lane groups) or per row, rows straight from
+//    global memory into registers.
+//  * smx_bulk_warp_kernel / smx_bulk_cta_kernel (NORMFUSE_SMX_PATH=ring):
+//    tiles of rows stream into a shared-memory ring by cp.async.bulk (the
+//    ring and refill scheme of the normalization kernels) and 8 warps work on
+//    them from shared memory: a lane group of LANES lanes per row, or all 256
 //    threads per row for rows of more than 256 vectors.
 //  * smx_scalar_kernel: any hidden size and alignment; element-wise loads,
 //    the row staged in shared memory as fp32.
 //
 // Arithmetic: fp32 throughout. m = max, e = exp2f((x - m) * log2 e) (one fma
 // and one exp2f per element), s = sum of e, y = e * (1/s) with a correctly
-// rounded reciprocal. A row whose entries
-// are all -inf, or that holds a NaN or +inf, comes out as NaN, as the
-// definition gives.
+// rounded reciprocal. A row whose entries are all -inf, or that holds a NaN
+// or +inf, comes out as NaN, as the definition gives.
 #pragma once
 
 #include <math.h>
