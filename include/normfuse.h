@@ -237,7 +237,9 @@ ln_status ln_bwd_workspace_bytes(int64_t rows, int64_t hidden, ln_dtype dtype,
  * - Limit: shapes whose partials need more than LN_NOALLOC_SCRATCH_BYTES
  *   (ln_bwd_workspace_bytes() reports the need) return LN_ERR_SCRATCH_LIMIT
  *   before anything is enqueued. At 2 CTAs per SM on 152 SMs that is about
- *   hidden <= 6800 for LayerNorm and hidden <= 13700 for RMSNorm.
+ *   hidden <= 6800 for LayerNorm and hidden <= 13700 for RMSNorm (rows of
+ *   2049 to 8192 bf16 elements whose backward runs from registers at 3 CTAs
+ *   per SM, up to 4096 for LayerNorm, also fit).
  * - Every call on a device shares the one array and nothing in it needs to
  *   start at zero (each call overwrites the partials it reads). Calls whose
  *   execution overlaps on the GPU (different streams, or different host

@@ -14,12 +14,17 @@
 // SM count, so the partials, and the finalize's fixed-order compensated sum
 // over them, are the same on every run.
 //
-//  * bwd_bulk_warp_kernel / bwd_bulk_cta_kernel (default for 16-byte aligned
-//    rows): dy and x_sum tiles stream into a shared-memory ring by
+//  * bwd_row_cta_kernel (default for rows of more than 256 vectors whose
+//    accumulators take at most 32 floats per thread): the row straight from
+//    global memory into registers, a CTA per row, three CTAs per SM.
+//  * bwd_bulk_warp_kernel / bwd_bulk_group_kernel / bwd_bulk_cta_kernel
+//    (the other 16-byte aligned rows; all of them with NORMFUSE_BWD_PATH=ring):
+//    dy and x_sum tiles stream into a shared-memory ring by
 //    cp.async.bulk; the row is read from shared memory twice (sums, then dx)
 //    instead of being held in registers, and w = gamma (+1) sits in shared
 //    memory as fp32.
-//  * bwd_warp_kernel / bwd_cta_kernel: the row held in registers.
+//  * bwd_warp_kernel / bwd_cta_kernel: the row held in registers
+//    (NORMFUSE_PATH=registers).
 //  * bwd_scalar_kernel: any hidden size and alignment.
 #pragma once
 
@@ -626,6 +631,121 @@ __global__ void __launch_bounds__(kBulkThreads, 2)
   unpair_acc<T, N>(acc_b, fb);
   unpair_acc<T, N>(acc_d, fd);
   store_thread_partials<T, kBulkThreads, N, kRms, kBias>(a, threadIdx.x, fg, fb, fd);
+}
+
+// ---- register backward, one CTA per row ------------------------------------
+
+// An empty asm statement that claims to rewrite N 16-byte vectors held in
+// registers, so the compiler re-unpacks them where they are used instead of
+// keeping the fp32 values live across the row sum (twice the registers).
+template <int N>
+__device__ __forceinline__ void vec_fence(uint4 (&q)[N]) {
+#pragma unroll
+  for (int k = 0; k < N; ++k)
+    asm volatile("" : "+r"(q[k].x), "+r"(q[k].y), "+r"(q[k].z), "+r"(q[k].w));
+}
+
+// Rows of more than 256 vectors, straight from global memory into registers
+// (N 16-byte vectors per thread, 256 threads per row): the CTAs of one wave
+// step through the rows (row blockIdx.x + k * gridDim.x), so the partial row
+// of CTA b sums a fixed set of rows and the sums depend only on the grid.
+// gamma is read through L1 in both passes (it is the same for every row),
+// the row sums go through a double-buffered CTA exchange with one barrier,
+// and each thread owns the same columns in every row, so its dgamma / dbeta
+// / dbias sums stay in registers until the end.
+template <typename T, int N, bool kRms, bool kBias>
+__global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdArgs a) {
+  constexpr int VEC = Vec<T>::N;
+  constexpr int P = VEC / 2;
+  __shared__ float2 red[2][kConsumerWarps];
+  const int t = threadIdx.x;
+  const int H = a.hidden;
+  const int V = H / VEC;
+  const T* gamma = static_cast<const T*>(a.gamma);
+  const T* dy = static_cast<const T*>(a.dy);
+  const T* xs = static_cast<const T*>(a.x_sum);
+  T* dx = static_cast<T*>(a.dx);
+  const bool plus_one = a.zero_centered != 0;
+  auto w_of = [&](int v, float2 (&w)[P]) {
+    unpack2<T>(ld_vec_param(gamma + v * VEC), w);
+    if (plus_one) {
+#pragma unroll
+      for (int i = 0; i < P; ++i) w[i] = add2(w[i], splat2(1.f));
+    }
+  };
+  float2 acc_g[N][P], acc_b[N][P], acc_d[N][P];
+  zero_acc2<T, N>(acc_g);
+  zero_acc2<T, N>(acc_b);
+  zero_acc2<T, N>(acc_d);
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+    const int64_t off = row * (int64_t)H;
+    uint4 dr[N], xr[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int v = k * kBulkThreads + t;
+      if (v < V) {
+        dr[k] = ld_vec(dy + off + v * VEC);
+        xr[k] = ld_vec(xs + off + v * VEC);
+      }
+    }
+    const float rstd = a.rstd[row];
+    const float mean = kRms ? 0.f : a.mean[row];
+    const float2 neg_mean = splat2(-mean);
+    const float2 r2 = splat2(rstd);
+    float2 sx = splat2(0.f), sy = splat2(0.f);
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int v = k * kBulkThreads + t;
+      if (v < V) {
+        float2 d[P], xv[P], w[P];
+        unpack2<T>(dr[k], d);
+        unpack2<T>(xr[k], xv);
+        w_of(v, w);
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+          const float2 xh = mul2(kRms ? xv[i] : add2(xv[i], neg_mean), r2);
+          const float2 g = mul2(d[i], w[i]);
+          if (!kRms) sx = add2(sx, g);
+          sy = fma2(g, xh, sy);
+          acc_g[k][i] = fma2(d[i], xh, acc_g[k][i]);
+          if (!kRms) acc_b[k][i] = add2(acc_b[k][i], d[i]);
+        }
+      }
+    }
+    const float2 sums =
+        cta_sum2_db<kBulkThreads>(make_float2(sx.x + sx.y, sy.x + sy.y), red, parity);
+    // dx = rstd * (g - c1 - xhat * c2) = (x - mean) * b2 + (g * rstd + a1)
+    const float c2 = sums.y / (float)H;
+    const float2 a1 = splat2(kRms ? 0.f : -rstd * (sums.x / (float)H));
+    const float2 b2 = splat2(-rstd * rstd * c2);
+    vec_fence<N>(dr);
+    vec_fence<N>(xr);
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int v = k * kBulkThreads + t;
+      if (v < V) {
+        float2 d[P], xv[P], w[P], o[P];
+        unpack2<T>(dr[k], d);
+        unpack2<T>(xr[k], xv);
+        w_of(v, w);
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+          const float2 xm = kRms ? xv[i] : add2(xv[i], neg_mean);
+          const float2 gr = kRms ? mul2(mul2(d[i], w[i]), r2) : fma2(mul2(d[i], w[i]), r2, a1);
+          o[i] = fma2(xm, b2, gr);
+          if (kBias) acc_d[k][i] = add2(acc_d[k][i], o[i]);
+        }
+        st_vec(dx + off + v * VEC, pack2<T>(o));
+      }
+    }
+  }
+  allow_dependent_launch();
+  float fg[N][VEC], fb[N][VEC], fd[N][VEC];
+  unpair_acc<T, N>(acc_g, fg);
+  unpair_acc<T, N>(acc_b, fb);
+  unpair_acc<T, N>(acc_d, fd);
+  store_thread_partials<T, kBulkThreads, N, kRms, kBias>(a, t, fg, fb, fd);
 }
 
 // ---- scalar kernel ----------------------------------------------------------

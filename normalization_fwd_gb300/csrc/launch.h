@@ -19,7 +19,9 @@ struct Plan {
   const void* fn = nullptr;
   bool bulk = false;   // pipelined kernel taking (args, BulkCfg)
   int kind = -1;       // 0 lane group per row, 1 CTA per row, 2 scalar, 3 row group (backward),
-                       // 4 lane group from registers, one CTA per row tile (softmax)
+                       // 4 lane group from registers, one CTA per row tile,
+                       // 5 CTA per row from registers (forward and softmax: one
+                       // CTA per row; backward: a persistent grid over the rows)
   int group = 0;       // threads sharing a row
   int n = 0;           // 16-byte vectors per thread per row
   int block = 0;

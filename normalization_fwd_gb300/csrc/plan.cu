@@ -195,10 +195,40 @@ inline bool fwd_tile_path() {
   return v;
 }
 
+// Backward rows of more than 256 vectors run from registers with a CTA per
+// row (kind 5) when its accumulators (n * VEC floats per reduction: dgamma;
+// dbeta for LayerNorm; dbias) take at most 32 floats per thread, so the
+// kernel keeps three CTAs per SM without spilling; NORMFUSE_BWD_PATH=ring
+// keeps the pipelined kernel for them. (At 16384 x 8192 bf16 RMSNorm the
+// register kernel ran 128 us against 148 us for the ring.)
+inline bool bwd_reg_cta_path() {
+  static const bool v = [] {
+    const char* e = getenv("NORMFUSE_BWD_PATH");
+    return !(e && strcmp(e, "ring") == 0);
+  }();
+  return v;
+}
+inline bool bwd_row_cta_fits(int n, int vec_elems, bool rms, bool dbias) {
+  return n <= 4 && n * vec_elems * (1 + (rms ? 0 : 1) + (dbias ? 1 : 0)) <= 32;
+}
+
 template <typename T>
 cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bool dbias,
                       int n_in, int n_params, Plan* p) {
   Choice c = choose(hidden, Vec<T>::N, vec);
+  if (bwd && vec && c.kind == 1 && path_override() != kPathRegisters && bwd_reg_cta_path()) {
+    const int n = bulk_cta_n(hidden, Vec<T>::N);
+    if (bwd_row_cta_fits(n, Vec<T>::N, rms, dbias)) {
+      p->bulk = false;
+      p->kind = 5;
+      p->group = kBulkThreads;
+      p->n = n;
+      p->block = kBulkThreads;
+      p->smem = 0;
+      p->fn = Tables<T>::bwd_bulk(5, kBulkThreads, n, rms, dbias);
+      return size_grid(p, rows);
+    }
+  }
   if (!bwd && vec && c.kind == 1 && path_override() != kPathRegisters && fwd_tile_path()) {
     p->bulk = false;
     p->kind = 5;

@@ -112,6 +112,13 @@ const void* bwd_bulk_table_impl(int kind, int group, int n) {
   } else if (kind == 3) {
     if (group == 64) { NF_BULK_GROUP_CASES_M(bwd_bulk_group_kernel, T, 64, kRms, kBias) }
     if (group == 128) { NF_BULK_GROUP_CASES_M(bwd_bulk_group_kernel, T, 128, kRms, kBias) }
+  } else if (kind == 5) {
+    switch (n) {
+      case 2: return (const void*)bwd_row_cta_kernel<T, 2, kRms, kBias>;
+      case 3: return (const void*)bwd_row_cta_kernel<T, 3, kRms, kBias>;
+      case 4: return (const void*)bwd_row_cta_kernel<T, 4, kRms, kBias>;
+      default: return nullptr;
+    }
   }
   return nullptr;
 }

@@ -1,8 +1,10 @@
 """The kernel families that are not the default for a shape stay correct:
 the parity files run again in child processes with the path switches set
 (read once per process): NORMFUSE_FWD_PATH=ring (the pipelined forward
-kernels), NORMFUSE_SMX_PATH=ring (the pipelined softmax kernels) and
-NORMFUSE_PATH=registers (the register kernels, both directions)."""
+kernels), NORMFUSE_SMX_PATH=ring (the pipelined softmax kernels),
+NORMFUSE_BWD_PATH=ring (the pipelined backward kernels also for the wide
+rows that default to the register CTA-per-row backward) and
+NORMFUSE_PATH=registers (the older register kernels, both directions)."""
 
 import os
 import subprocess
@@ -18,8 +20,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 @pytest.mark.parametrize("env,files", [
     ({"NORMFUSE_FWD_PATH": "ring"}, ["tests/test_gpu_edges.py", "tests/test_gpu_fp8.py"]),
     ({"NORMFUSE_SMX_PATH": "ring"}, ["tests/test_gpu_softmax.py"]),
+    ({"NORMFUSE_BWD_PATH": "ring"}, ["tests/test_gpu_edges.py", "tests/test_gpu_dbias.py"]),
     ({"NORMFUSE_PATH": "registers"}, ["tests/test_gpu_edges.py"]),
-], ids=["fwd-ring", "softmax-ring", "registers"])
+], ids=["fwd-ring", "softmax-ring", "bwd-ring", "registers"])
 def test_parity_on_alternate_paths(cuda_lib, env, files):
     e = dict(os.environ)
     e.update(env)

@@ -59,7 +59,7 @@ def fwd_bwd_parity(lib, w, seed=0, x_override=None, **fwd_kw):
 # Hidden sizes that reach every family: warp exact fits (LANES x N), warp
 # with masked lanes, CTA per row (exact and masked), and the scalar kernel
 # (row width not a multiple of 16 bytes).
-HIDDEN_16BIT = [8, 56, 64, 128, 200, 256, 320, 384, 640, 768, 1000, 1024, 1280, 2048,
+HIDDEN_16BIT = [8, 56, 64, 128, 136, 200, 256, 320, 384, 512, 640, 768, 1000, 1024, 1280, 2048,
                 2056, 3000, 4096, 8192, 16384,          # vector paths
                 1, 2, 3, 7, 100, 1001, 4100]            # scalar path
 HIDDEN_F32 = [4, 28, 64, 96, 384, 500, 768, 1024, 1028, 2048, 4096, 8192,
