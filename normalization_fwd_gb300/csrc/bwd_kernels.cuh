@@ -15,8 +15,9 @@
 // over them, are the same on every run.
 //
 //  * bwd_row_cta_kernel (default for rows of more than 256 vectors whose
-//    accumulators take at most 32 floats per thread): the row straight from
-//    global memory into registers, a CTA per row, three CTAs per SM.
+//    accumulators and row fit in registers at three CTAs per SM: bf16/fp16
+//    RMSNorm up to 8192, LayerNorm up to 4096): the row straight from global
+//    memory into registers, a CTA per row.
 //  * bwd_bulk_warp_kernel / bwd_bulk_group_kernel / bwd_bulk_cta_kernel
 //    (the other 16-byte aligned rows; all of them with NORMFUSE_BWD_PATH=ring):
 //    dy and x_sum tiles stream into a shared-memory ring by
@@ -645,19 +646,15 @@ __device__ __forceinline__ void vec_fence(uint4 (&q)[N]) {
     asm volatile("" : "+r"(q[k].x), "+r"(q[k].y), "+r"(q[k].z), "+r"(q[k].w));
 }
 
-// Rows of more than 256 vectors, straight from global memory into registers
-// (N 16-byte vectors per thread, 256 threads per row): the CTAs of one wave
-// step through the rows (row blockIdx.x + k * gridDim.x), so the partial row
-// of CTA b sums a fixed set of rows and the sums depend only on the grid.
-// gamma is read through L1 in both passes (it is the same for every row),
-// the row sums go through a double-buffered CTA exchange with one barrier,
-// and each thread owns the same columns in every row, so its dgamma / dbeta
-// / dbias sums stay in registers until the end.
-template <typename T, int N, bool kRms, bool kBias>
-__global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdArgs a) {
+// The row loop of bwd_row_cta_kernel; kZc adds 1 to gamma (zero-centered
+// gamma) at compile time, so the loop carries no per-element branch.
+template <typename T, int N, bool kRms, bool kBias, bool kZc>
+__device__ __forceinline__ void row_cta_rows(const BwdArgs& a, float2 (*red)[kConsumerWarps],
+                                             float2 (&acc_g)[N][Vec<T>::N / 2],
+                                             float2 (&acc_b)[N][Vec<T>::N / 2],
+                                             float2 (&acc_d)[N][Vec<T>::N / 2]) {
   constexpr int VEC = Vec<T>::N;
   constexpr int P = VEC / 2;
-  __shared__ float2 red[2][kConsumerWarps];
   const int t = threadIdx.x;
   const int H = a.hidden;
   const int V = H / VEC;
@@ -665,18 +662,6 @@ __global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdA
   const T* dy = static_cast<const T*>(a.dy);
   const T* xs = static_cast<const T*>(a.x_sum);
   T* dx = static_cast<T*>(a.dx);
-  const bool plus_one = a.zero_centered != 0;
-  auto w_of = [&](int v, float2 (&w)[P]) {
-    unpack2<T>(ld_vec_param(gamma + v * VEC), w);
-    if (plus_one) {
-#pragma unroll
-      for (int i = 0; i < P; ++i) w[i] = add2(w[i], splat2(1.f));
-    }
-  };
-  float2 acc_g[N][P], acc_b[N][P], acc_d[N][P];
-  zero_acc2<T, N>(acc_g);
-  zero_acc2<T, N>(acc_b);
-  zero_acc2<T, N>(acc_d);
   int parity = 0;
   for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
     const int64_t off = row * (int64_t)H;
@@ -701,9 +686,10 @@ __global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdA
         float2 d[P], xv[P], w[P];
         unpack2<T>(dr[k], d);
         unpack2<T>(xr[k], xv);
-        w_of(v, w);
+        unpack2<T>(ld_vec_param(gamma + v * VEC), w);
 #pragma unroll
         for (int i = 0; i < P; ++i) {
+          if (kZc) w[i] = add2(w[i], splat2(1.f));
           const float2 xh = mul2(kRms ? xv[i] : add2(xv[i], neg_mean), r2);
           const float2 g = mul2(d[i], w[i]);
           if (!kRms) sx = add2(sx, g);
@@ -713,8 +699,8 @@ __global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdA
         }
       }
     }
-    const float2 sums =
-        cta_sum2_db<kBulkThreads>(make_float2(sx.x + sx.y, sy.x + sy.y), red, parity);
+    const float2 sums = cta_sum2_db<kBulkThreads>(
+        make_float2(kRms ? 0.f : sx.x + sx.y, sy.x + sy.y), red, parity);
     // dx = rstd * (g - c1 - xhat * c2) = (x - mean) * b2 + (g * rstd + a1)
     const float c2 = sums.y / (float)H;
     const float2 a1 = splat2(kRms ? 0.f : -rstd * (sums.x / (float)H));
@@ -728,24 +714,65 @@ __global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdA
         float2 d[P], xv[P], w[P], o[P];
         unpack2<T>(dr[k], d);
         unpack2<T>(xr[k], xv);
-        w_of(v, w);
+        unpack2<T>(ld_vec_param(gamma + v * VEC), w);
 #pragma unroll
         for (int i = 0; i < P; ++i) {
-          const float2 xm = kRms ? xv[i] : add2(xv[i], neg_mean);
-          const float2 gr = kRms ? mul2(mul2(d[i], w[i]), r2) : fma2(mul2(d[i], w[i]), r2, a1);
-          o[i] = fma2(xm, b2, gr);
+          if (kZc) w[i] = add2(w[i], splat2(1.f));
+          const float2 gr = kRms ? mul2(mul2(d[i], w[i]), r2)
+                                 : fma2(mul2(d[i], w[i]), r2, a1);
+          o[i] = fma2(kRms ? xv[i] : add2(xv[i], neg_mean), b2, gr);
           if (kBias) acc_d[k][i] = add2(acc_d[k][i], o[i]);
         }
         st_vec(dx + off + v * VEC, pack2<T>(o));
       }
     }
   }
+}
+
+// Rows of more than 256 vectors, straight from global memory into registers
+// (N 16-byte vectors per thread, 256 threads per row): the CTAs of one wave
+// step through the rows (row blockIdx.x + k * gridDim.x), so the partial row
+// of CTA b sums a fixed set of rows and the sums depend only on the grid.
+// gamma is read through L1 in both passes (it is the same for every row),
+// the row sums go through a double-buffered CTA exchange with one barrier,
+// and each thread owns the same columns in every row, so its dgamma / dbeta
+// / dbias sums stay in registers until the end.
+template <typename T, int N, bool kRms, bool kBias>
+__global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdArgs a) {
+  constexpr int VEC = Vec<T>::N;
+  constexpr int P = VEC / 2;
+  __shared__ float2 red[2][kConsumerWarps];
+  float2 acc_g[N][P], acc_b[N][P], acc_d[N][P];
+  zero_acc2<T, N>(acc_g);
+  zero_acc2<T, N>(acc_b);
+  zero_acc2<T, N>(acc_d);
+  if (a.zero_centered) {
+    row_cta_rows<T, N, kRms, kBias, true>(a, red, acc_g, acc_b, acc_d);
+  } else {
+    row_cta_rows<T, N, kRms, kBias, false>(a, red, acc_g, acc_b, acc_d);
+  }
   allow_dependent_launch();
-  float fg[N][VEC], fb[N][VEC], fd[N][VEC];
-  unpair_acc<T, N>(acc_g, fg);
-  unpair_acc<T, N>(acc_b, fb);
-  unpair_acc<T, N>(acc_d, fd);
-  store_thread_partials<T, kBulkThreads, N, kRms, kBias>(a, t, fg, fb, fd);
+  // Partials: every column belongs to one thread; fp32 pairs go out as
+  // 16-byte stores (dgamma at 0, dbeta at H, dbias after them).
+  const int H = a.hidden;
+  const int V = H / VEC;
+  float* ws = a.ws + (int64_t)blockIdx.x * a.ws_cols;
+  auto put = [&](const float2 (&acc)[N][P], int off) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int v = k * kBulkThreads + threadIdx.x;
+      if (v < V) {
+        float4* q = reinterpret_cast<float4*>(ws + off + v * VEC);
+#pragma unroll
+        for (int i = 0; i < P / 2; ++i)
+          q[i] = make_float4(acc[k][2 * i].x, acc[k][2 * i].y, acc[k][2 * i + 1].x,
+                             acc[k][2 * i + 1].y);
+      }
+    }
+  };
+  put(acc_g, 0);
+  if (!kRms) put(acc_b, H);
+  if (kBias) put(acc_d, kRms ? H : 2 * H);
 }
 
 // ---- scalar kernel ----------------------------------------------------------

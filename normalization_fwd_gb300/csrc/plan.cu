@@ -197,10 +197,10 @@ inline bool fwd_tile_path() {
 
 // Backward rows of more than 256 vectors run from registers with a CTA per
 // row (kind 5) when its accumulators (n * VEC floats per reduction: dgamma;
-// dbeta for LayerNorm; dbias) take at most 32 floats per thread, so the
-// kernel keeps three CTAs per SM without spilling; NORMFUSE_BWD_PATH=ring
-// keeps the pipelined kernel for them. (At 16384 x 8192 bf16 RMSNorm the
-// register kernel ran 128 us against 148 us for the ring.)
+// dbeta for LayerNorm; dbias) and the row's two inputs (8n registers) fit in
+// 64 registers' worth (56 for LayerNorm, which also keeps the mean and a
+// second row sum live), so the kernel keeps three CTAs per SM without
+// spilling; NORMFUSE_BWD_PATH=ring keeps the pipelined kernel for them.
 inline bool bwd_reg_cta_path() {
   static const bool v = [] {
     const char* e = getenv("NORMFUSE_BWD_PATH");
@@ -209,7 +209,8 @@ inline bool bwd_reg_cta_path() {
   return v;
 }
 inline bool bwd_row_cta_fits(int n, int vec_elems, bool rms, bool dbias) {
-  return n <= 4 && n * vec_elems * (1 + (rms ? 0 : 1) + (dbias ? 1 : 0)) <= 32;
+  const int acc = n * vec_elems * (1 + (rms ? 0 : 1) + (dbias ? 1 : 0));
+  return n <= 4 && acc + 8 * n <= (rms ? 64 : 56);
 }
 
 template <typename T>
