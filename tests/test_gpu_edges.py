@@ -60,7 +60,7 @@ def fwd_bwd_parity(lib, w, seed=0, x_override=None, **fwd_kw):
 # with masked lanes, CTA per row (exact and masked), and the scalar kernel
 # (row width not a multiple of 16 bytes).
 HIDDEN_16BIT = [8, 56, 64, 128, 136, 200, 256, 320, 384, 512, 640, 768, 1000, 1024, 1280, 2048,
-                2056, 3000, 4096, 8192, 16384,          # vector paths
+                2056, 3000, 3072, 4096, 8192, 16384,    # vector paths
                 1, 2, 3, 7, 100, 1001, 4100]            # scalar path
 HIDDEN_F32 = [4, 28, 64, 96, 384, 500, 768, 1024, 1028, 2048, 4096, 8192,
               1, 3, 7, 99, 1001]
@@ -138,16 +138,24 @@ def test_unaligned_pointers_use_scalar_path(cuda_lib, dtype):
     fwd_bwd_parity(cuda_lib, w, seed=2, x_override=x_shifted)
 
 
-def test_backward_is_deterministic(cuda_lib):
-    w = wl("bf16", 50001, 384, W.LAYERNORM)
+@pytest.mark.parametrize("rows,hidden,mode,zc", [
+    (50001, 384, W.LAYERNORM, False),     # pipelined lane-group backward
+    (3001, 8192, W.RMSNORM, False),       # register CTA-per-row backward
+    (2001, 3072, W.LAYERNORM, True),      # the same with zero-centered gamma
+], ids=["ln384", "rms8192", "ln3072zc"])
+def test_backward_is_deterministic(cuda_lib, rows, hidden, mode, zc):
+    w = wl("bf16", rows, hidden, mode, zero_centered_gamma=zc)
     inp = make_inputs(w, seed=3)
     ref = oracle_fwd(w, inp)
     x_sum = torch.from_numpy(ref["sum"]).to(torch.bfloat16)
-    mean = torch.from_numpy(ref["mean"]).float()
+    mean = None if ref["mean"] is None else torch.from_numpy(ref["mean"]).float()
     rstd = torch.from_numpy(ref["rstd"]).float()
     a = gpu_bwd(cuda_lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd)
     b = gpu_bwd(cuda_lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd)
+    assert a["guards_ok"] and b["guards_ok"]
     for k in ("dx", "dgamma", "dbeta"):
+        if a.get(k) is None:
+            continue
         bits = torch.int16 if a[k].element_size() == 2 else torch.int32
         assert torch.equal(a[k].view(bits), b[k].view(bits)), k
 
