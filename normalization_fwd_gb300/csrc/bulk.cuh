@@ -146,13 +146,6 @@ __device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint3
 // a shared address would take the slower L1TEX path). Volatile, so they stay
 // after the barrier waits (volatile asm keeps its order) and are never merged
 // with an earlier load of the same address.
-__device__ __forceinline__ uint4 ld_vec_smem(const void* p) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(smem_addr(p)));
-  return v;
-}
 __device__ __forceinline__ float4 ld_f4_smem(const float* p) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"

@@ -35,11 +35,11 @@
 
 namespace nf {
 
-// One row for the vector kernels: dx of the row, and the row added into
-// acc_g (dy * xhat) and acc_b (dy). G threads share the row, this one is `t`.
-// With kReread the second pass loads dy and x_sum again (cheap from shared
-// memory) rather than keeping xhat and g in registers across the reduction.
-template <typename T, int G, int N, typename Src, bool kReread, typename Reduce2>
+// One row of the grid-stride register kernels (NORMFUSE_PATH=registers): dx
+// of the row, and the row added into acc_g (dy * xhat) and acc_b (dy). G
+// threads share the row, this one is `t`; xhat and g stay in registers
+// across the row sums.
+template <typename T, int G, int N, typename Reduce2>
 __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_ok, int t,
                                         const T* dyrow, const T* xsrow, float mean, float rstd,
                                         Reduce2 reduce2, float (&acc_g)[N][Vec<T>::N],
@@ -54,18 +54,17 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
     if (row_ok && v < V) {
-      dr[k] = Src::load(dyrow + v * VEC);
-      xr[k] = Src::load(xsrow + v * VEC);
+      dr[k] = ld_vec(dyrow + v * VEC);
+      xr[k] = ld_vec(xsrow + v * VEC);
     }
   }
 
   // xhat, g = dy * w, the two row sums, and the outer-reduction partials.
-  float xh[kReread ? 1 : N][VEC], g[kReread ? 1 : N][VEC];
+  float xh[N][VEC], g[N][VEC];
   float2 sums = make_float2(0.f, 0.f);
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
-    const int kk = kReread ? 0 : k;
     if (row_ok && v < V) {
       float d[VEC], xv[VEC], w[VEC];
       unpack<T>(dr[k], d);
@@ -74,11 +73,11 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         const float we = a.zero_centered ? 1.0f + w[e] : w[e];
-        xh[kk][e] = (xv[e] - mean) * rstd;
-        g[kk][e] = d[e] * we;
-        sums.x += g[kk][e];
-        sums.y = fmaf(g[kk][e], xh[kk][e], sums.y);
-        acc_g[k][e] = fmaf(d[e], xh[kk][e], acc_g[k][e]);
+        xh[k][e] = (xv[e] - mean) * rstd;
+        g[k][e] = d[e] * we;
+        sums.x += g[k][e];
+        sums.y = fmaf(g[k][e], xh[k][e], sums.y);
+        acc_g[k][e] = fmaf(d[e], xh[k][e], acc_g[k][e]);
         acc_b[k][e] += d[e];
       }
     }
@@ -86,9 +85,6 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
   sums = reduce2(sums);
   const float c1 = a.rms ? 0.f : sums.x / (float)H;
   const float c2 = sums.y / (float)H;
-  // Make the second pass load again instead of keeping the first pass's
-  // values live across the reduction.
-  if (kReread) asm volatile("" ::: "memory");
 
   T* dx = static_cast<T*>(a.dx) + row * (int64_t)H;
 #pragma unroll
@@ -96,22 +92,8 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
     const int v = k * G + t;
     if (row_ok && v < V) {
       float o[VEC];
-      if (kReread) {
-        float d[VEC], xv[VEC], w[VEC];
-        unpack<T>(Src::load(dyrow + v * VEC), d);
-        unpack<T>(Src::load(xsrow + v * VEC), xv);
-        unpack<T>(ld_vec_param(gamma + v * VEC), w);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          const float we = a.zero_centered ? 1.0f + w[e] : w[e];
-          const float xhe = (xv[e] - mean) * rstd;
-          o[e] = rstd * (d[e] * we - c1 - xhe * c2);
-        }
-      } else {
-        const int kk = kReread ? 0 : k;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) o[e] = rstd * (g[kk][e] - c1 - xh[kk][e] * c2);
-      }
+      for (int e = 0; e < VEC; ++e) o[e] = rstd * (g[k][e] - c1 - xh[k][e] * c2);
       st_vec(dx + v * VEC, pack<T>(o));
     }
   }
@@ -388,7 +370,7 @@ __global__ void __launch_bounds__(kWarpCta) bwd_warp_kernel(const BwdArgs a) {
     const float rstd = ok ? a.rstd[row] : 0.f;
     const float mean = (ok && !a.rms) ? a.mean[row] : 0.f;
     const int64_t off = row * (int64_t)a.hidden;
-    bwd_row<T, LANES, N, FromGlobal, false>(a, row, ok, l, dy + off, xs + off, mean, rstd,
+    bwd_row<T, LANES, N>(a, row, ok, l, dy + off, xs + off, mean, rstd,
                                             [](float2 v) { return group_sum2<LANES>(v); },
                                             acc_g, acc_b);
   }
@@ -406,7 +388,7 @@ __global__ void __launch_bounds__(THREADS) bwd_cta_kernel(const BwdArgs a) {
     const float rstd = a.rstd[row];
     const float mean = a.rms ? 0.f : a.mean[row];
     const int64_t off = row * (int64_t)a.hidden;
-    bwd_row<T, THREADS, N, FromGlobal, false>(
+    bwd_row<T, THREADS, N>(
         a, row, true, threadIdx.x, dy + off, xs + off, mean, rstd,
         [&](float2 v) { return cta_sum2<THREADS>(v, red); }, acc_g, acc_b);
   }

@@ -91,11 +91,6 @@ template <> __device__ __forceinline__ float from_f<float>(float v) { return v; 
 template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
 template <> __device__ __forceinline__ f16 from_f<f16>(float v) { return __float2half_rn(v); }
 
-// Round an fp32 value to T and back: the value the stored tensor holds.
-template <typename T> __device__ __forceinline__ float round_trip(float v) {
-  return to_f(from_f<T>(v));
-}
-
 // ---- 16-byte vectors -----------------------------------------------------
 // Read-only streaming load of 16 bytes (non-coherent path; inputs are never
 // written by the same kernel).

@@ -28,19 +28,11 @@
 
 namespace nf {
 
-// Where a row's 16-byte vectors come from.
-struct FromGlobal {
-  static __device__ __forceinline__ uint4 load(const void* p) { return ld_vec(p); }
-};
-struct FromSmem {
-  static __device__ __forceinline__ uint4 load(const void* p) { return ld_vec_smem(p); }
-};
-
-// One row for the vector kernels. `G` threads share the row, this one is
-// `t`; `xrow` / `rrow` point at the row's x and residual (global or shared
-// memory, per Src; rrow is null without a residual). `reduce` sums a float
-// over the G threads.
-template <typename T, int G, int N, typename Src, typename Reduce>
+// One row of the grid-stride register kernels (NORMFUSE_PATH=registers). `G`
+// threads share the row, this one is `t`; `xrow` / `rrow` point at the row's
+// x and residual in global memory (rrow is null without a residual).
+// `reduce` sums a float over the G threads.
+template <typename T, int G, int N, typename Reduce>
 __device__ __forceinline__ void fwd_row(const FwdArgs& a, int64_t row, bool row_ok, int t,
                                         const T* xrow, const T* rrow, Reduce reduce,
                                         unsigned& amax_acc, bool write_stats) {
@@ -56,8 +48,8 @@ __device__ __forceinline__ void fwd_row(const FwdArgs& a, int64_t row, bool row_
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
     if (row_ok && v < V) {
-      xr[k] = Src::load(xrow + v * VEC);
-      if (rrow) rr[k] = Src::load(rrow + v * VEC);
+      xr[k] = ld_vec(xrow + v * VEC);
+      if (rrow) rr[k] = ld_vec(rrow + v * VEC);
     }
   }
 
@@ -175,7 +167,7 @@ __global__ void __launch_bounds__(kWarpCta) fwd_warp_kernel(const FwdArgs a) {
        base += step) {
     const int64_t row = base + sub;
     const int64_t off = row * (int64_t)a.hidden;
-    fwd_row<T, LANES, N, FromGlobal>(a, row, row < a.rows, l, x + off, res ? res + off : nullptr,
+    fwd_row<T, LANES, N>(a, row, row < a.rows, l, x + off, res ? res + off : nullptr,
                                      [](float v) { return group_sum<LANES>(v); }, amax_acc,
                                      l == 0);
   }
@@ -191,7 +183,7 @@ __global__ void __launch_bounds__(THREADS) fwd_cta_kernel(const FwdArgs a) {
   unsigned amax_acc = 0;
   for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
     const int64_t off = row * (int64_t)a.hidden;
-    fwd_row<T, THREADS, N, FromGlobal>(a, row, true, threadIdx.x, x + off,
+    fwd_row<T, THREADS, N>(a, row, true, threadIdx.x, x + off,
                                        res ? res + off : nullptr,
                                        [&](float v) { return cta_sum<THREADS>(v, red); },
                                        amax_acc, threadIdx.x == 0);
