@@ -102,11 +102,14 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
 // The row body of the pipelined kernels: dy and x_sum rows in shared memory,
 // w = gamma (+1) staged in shared memory (kStaged), read from global, or
 // (kWReg) held in registers: a thread covers the same columns in every row,
-// so `wreg` is loaded once per kernel. Both passes read shared memory, so only
-// the accumulators (and wreg) stay in registers across the reduction. Values are fp32 pairs (packed fp32 math). kRms drops
+// so `wreg` is loaded once per kernel. The second pass reads shared memory
+// again, so only the accumulators (and wreg) stay in registers across the
+// reduction, except that the first kKeep vectors keep their (x - mean) and
+// g = dy * w from the first pass (registers the kernel has to spare; the same
+// values either way). Values are fp32 pairs (packed fp32 math). kRms drops
 // the mean, c1 and the dbeta accumulators at compile time; kBias adds the
 // row's fp32 dx into the dbias accumulators.
-template <typename T, int G, int N, bool kRms, bool kBias, bool kStaged, bool kWReg,
+template <typename T, int G, int N, bool kRms, bool kBias, bool kStaged, bool kWReg, int kKeep,
           typename Reduce2>
 __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool row_ok, int t,
                                              uint32_t dyrow, uint32_t xsrow, const ParamRow<T>& wr,
@@ -123,6 +126,8 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
   const float2 r2 = splat2(rstd);
   const uint32_t wa = kStaged ? wr.saddr() : 0u;
   float2 sx = splat2(0.f), sy = splat2(0.f);
+  constexpr int KK = kKeep > 0 ? kKeep : 1;
+  float2 keep_xm[KK][P], keep_g[KK][P];
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
@@ -138,8 +143,13 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
       }
 #pragma unroll
       for (int i = 0; i < P; ++i) {
-        const float2 xh = mul2(kRms ? xv[i] : add2(xv[i], neg_mean), r2);
+        const float2 xm = kRms ? xv[i] : add2(xv[i], neg_mean);
+        const float2 xh = mul2(xm, r2);
         const float2 g = mul2(d[i], w[i]);
+        if (k < kKeep) {
+          keep_xm[k < kKeep ? k : 0][i] = xm;
+          keep_g[k < kKeep ? k : 0][i] = g;
+        }
         if (!kRms) sx = add2(sx, g);
         sy = fma2(g, xh, sy);
         acc_g[k][i] = fma2(d[i], xh, acc_g[k][i]);
@@ -158,7 +168,16 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
-    if (row_ok && v < V) {
+    if (k < kKeep && row_ok && v < V) {
+      float2 o[P];
+#pragma unroll
+      for (int i = 0; i < P; ++i) {
+        o[i] = fma2(keep_xm[k < kKeep ? k : 0][i], b2,
+                    fma2(keep_g[k < kKeep ? k : 0][i], r2, a1));
+        if (kBias) acc_d[k][i] = add2(acc_d[k][i], o[i]);
+      }
+      st_vec(dx + v * VEC, pack2<T>(o));
+    } else if (row_ok && v < V) {
       float2 d[P], xv[P], w[P], o[P];
       unpack2<T>(lds_u4(dyrow + v * 16), d);
       unpack2<T>(lds_u4(xsrow + v * 16), xv);
@@ -397,6 +416,14 @@ __global__ void __launch_bounds__(THREADS) bwd_cta_kernel(const BwdArgs a) {
 
 // ---- bulk-copy pipelined kernels ------------------------------------------
 
+// Vectors per lane whose first-pass values the lane-group backward keeps for
+// the second pass: one for 16-bit LayerNorm rows of three vectors per lane
+// (384 wide with 16 lanes: 106 -> 118 registers, still two CTAs per SM;
+// 228 -> 221 us at 576000 rows; keeping two vectors, 125 registers, took
+// 253 us), none for the shapes where it was not measured.
+template <typename T, int N, bool kRms, bool kBias>
+constexpr int kKeepWarp = (sizeof(T) == 2 && !kRms && !kBias && N == 3) ? 1 : 0;
+
 template <typename T, int LANES, int N, bool kRms, bool kBias>
 __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const BwdArgs a,
                                                                          const BulkCfg c) {
@@ -446,7 +473,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
         const int64_t row = tile * c.tile_rows + local;
         const uint32_t dys = smem_addr(slot) + (uint32_t)(local * H * sizeof(T));
         const uint32_t xss = dys + in_bytes;
-        bwd_row_smem<T, LANES, N, kRms, kBias, true, false>(
+        bwd_row_smem<T, LANES, N, kRms, kBias, true, false, kKeepWarp<T, N, kRms, kBias>>(
             a, row, row < a.rows, l, dys, xss, wr, wreg, mean, rstd,
             [](float2 v) { return group_sum2<LANES>(v); }, acc_g, acc_b, acc_d);
       });
@@ -539,7 +566,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_group_kernel(const B
         const int64_t row = tile * c.tile_rows + local;
         const uint32_t dys = smem_addr(slot) + (uint32_t)(local * H * sizeof(T));
         const uint32_t xss = dys + in_bytes;
-        bwd_row_smem<T, G, N, kRms, kBias, true, false>(a, row, row < a.rows, t, dys, xss, wr,
+        bwd_row_smem<T, G, N, kRms, kBias, true, false, 0>(a, row, row < a.rows, t, dys, xss, wr,
                                                         wreg, mean, rstd, row_sum, acc_g,
                                                         acc_b, acc_d);
       });
@@ -602,7 +629,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2)
         load_stats(row + gridDim.x, nm, nr);
         const uint32_t dys = smem_addr(slot);
         const uint32_t xss = dys + in_bytes;
-        bwd_row_smem<T, kBulkThreads, N, kRms, kBias, false, kWReg>(
+        bwd_row_smem<T, kBulkThreads, N, kRms, kBias, false, kWReg, 0>(
             a, row, true, threadIdx.x, dys, xss, wr, wreg, mean, rstd,
             [&](float2 v) { return cta_sum2_db<kBulkThreads>(v, red, parity); }, acc_g, acc_b,
             acc_d);
