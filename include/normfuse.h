@@ -136,6 +136,57 @@ ln_status ln_fwd_ex(const void* x, const void* bias, const void* residual,
                     cudaStream_t stream, int64_t rows, int64_t hidden,
                     ln_dtype dtype);
 
+/* Form of the per-tile partial statistics ln_fwd_from_partials reads. */
+typedef enum {
+  LN_PARTIALS_SUM_SQ = 0, /* psum = sum of the tile's values, psq = sum of their squares */
+  LN_PARTIALS_SUM_M2 = 1  /* psum as above, psq = sum of squares about the tile's own mean */
+} ln_partials;
+
+/*
+ * ln_fwd_from_partials: y = norm(x) * w + beta with the row statistics
+ * combined from per-column-tile partial sums instead of a pass over the row.
+ *
+ * Defined by NVIDIA/cutlass discussion 874 (the reply pointing at example
+ * 37, gemm_with_layernorm.h): the GEMM that produces the row (with the
+ * residual added in its epilogue) also sums each row over the column tile
+ * every threadblock owns, and the LayerNorm that follows combines those
+ * partials into the row's mean and variance. The producing GEMM is not part
+ * of this library; this is the consumer: one read of x, one write of y.
+ *
+ * Column tiles are tile_cols wide from column 0; the last one holds the
+ * hidden - (n_tiles - 1) * tile_cols columns left, n_tiles =
+ * ceil(hidden / tile_cols). With S and Q the per-row sums over the tiles of
+ * psum and of the second quantity, and n_t a tile's width, in fp32:
+ *   LN_PARTIALS_SUM_SQ: LayerNorm mean = S / H, var = max(Q / H - mean^2, 0)
+ *     (Q = sum psq); RMSNorm mean square = Q / H.
+ *   LN_PARTIALS_SUM_M2: LayerNorm var = (sum_t psq_t +
+ *     sum_t (psum_t - n_t mean)^2 / n_t) / H (the parallel-variance
+ *     identity); RMSNorm mean square = sum_t (psq_t + psum_t^2 / n_t) / H.
+ *   rstd = 1/sqrt(var or mean square + eps); y = (x - mean) * rstd * w + beta
+ *   (RMSNorm: x * rstd * w), w = gamma or 1 + gamma; y rounded to dtype;
+ *   amax = max |y| over the stored y, as in ln_fwd.
+ * The sum-of-squares form loses precision when |mean| is large against the
+ * row's spread (Q / H and mean^2 cancel); the M2 form does not.
+ *
+ * x          [rows, hidden] dtype, the stored row (what the producer wrote),
+ *            required when rows > 0.
+ * psum, psq  [rows, n_tiles] fp32, row-major, 4-byte aligned, required when
+ *            rows > 0.
+ * n_tiles    must equal ceil(hidden / tile_cols), else LN_ERR_SHAPE.
+ * tile_cols  >= 1 (a value >= hidden means one tile).
+ * kind       LN_PARTIALS_SUM_SQ or LN_PARTIALS_SUM_M2, else LN_ERR_UNSUPPORTED.
+ * gamma, beta, eps, mode, zero_centered_gamma, y, mean, rstd, amax: as in
+ *            ln_fwd (mean, rstd are the statistics used, rounded to fp32).
+ * Shapes, alignment, limits, streams and errors: the header's conventions.
+ */
+ln_status ln_fwd_from_partials(const void* x, const float* psum, const float* psq,
+                               int64_t n_tiles, int64_t tile_cols, ln_partials kind,
+                               const void* gamma, const void* beta, float eps,
+                               ln_mode mode, int zero_centered_gamma, void* y,
+                               float* mean, float* rstd, float* amax,
+                               cudaStream_t stream, int64_t rows, int64_t hidden,
+                               ln_dtype dtype);
+
 /*
  * ln_bwd: dx, dgamma, dbeta of the normalization given dy and the forward's
  * saved sum and statistics.
@@ -220,23 +271,30 @@ ln_status ln_bwd_workspace_bytes(int64_t rows, int64_t hidden, ln_dtype dtype,
  * ln_bwd_noalloc: ln_bwd for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this entry point; it exists for callers
- * that must not call cudaMalloc or any allocator around a backward pass: code
- * recorded into a CUDA graph or running under a framework that owns every
- * device allocation through its own pool, runtimes with a fixed device memory
- * budget set up front, and callers on a path where an allocation (which may
- * synchronise the device) is not allowed. It computes exactly what ln_bwd
+ * that must not call cudaMalloc or any allocator around a backward pass: a
+ * framework that owns every device allocation through its own caching pool
+ * (a raw cudaMalloc behind its back fragments the pool and escapes its
+ * accounting), a runtime whose device memory budget is fixed up front, and a
+ * hot path where an allocation is not allowed because cudaMalloc may
+ * synchronise the device. It computes exactly what ln_bwd
  * computes, with the same kernels, arguments and results; the difference is
  * that the per-CTA dgamma/dbeta partials go to a static device array of
  * LN_NOALLOC_SCRATCH_BYTES inside the library instead of a caller workspace.
  *
- * - The array is part of the library image: every GPU that loads the library
- *   holds it until the process exits. No call allocates or frees anything.
- * - Set-up: the first call on a device looks up the array's device address
- *   (with that device current) and caches it; make that first call before any
- *   stream capture that includes it.
+ * - The array belongs to the library's device code: a context holds its
+ *   bytes from the moment the library's module is loaded in it until the
+ *   context is destroyed. Under lazy module loading (the CUDA default) that
+ *   is the first call of this entry point in the context, so that first call
+ *   commits the array; make it before any stream capture and before any
+ *   phase with a fixed memory budget. Later calls allocate and free nothing.
+ * - Set-up: every call looks up the array's device address in the current
+ *   context (the caller's device current), a host-side query that enqueues
+ *   nothing; an address is never reused across contexts, so a
+ *   cudaDeviceReset or a context of the caller's own is handled.
  * - Limit: shapes whose partials need more than LN_NOALLOC_SCRATCH_BYTES
- *   (ln_bwd_workspace_bytes() reports the need) return LN_ERR_SCRATCH_LIMIT
- *   before anything is enqueued. At 2 CTAs per SM on 152 SMs that is about
+ *   return LN_ERR_SCRATCH_LIMIT before anything is enqueued
+ *   (ln_bwd_workspace_bytes() gives a bound of the need: it also covers
+ *   ln_bwd_ex's dbias columns, which this entry point does not compute). At 2 CTAs per SM on 152 SMs that is about
  *   hidden <= 6800 for LayerNorm and hidden <= 13700 for RMSNorm (rows of
  *   2049 to 8192 bf16 elements whose backward runs from registers at 3 CTAs
  *   per SM, up to 4096 for LayerNorm, also fit).

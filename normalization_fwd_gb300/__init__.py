@@ -22,15 +22,26 @@ from .build import LIB_PATH, build as build_library
 
 __all__ = [
     "LN_F32", "LN_BF16", "LN_F16", "LN_LAYERNORM", "LN_RMSNORM", "NormError",
+    "LN_OK", "LN_ERR_NULL", "LN_ERR_ALIGN", "LN_ERR_SHAPE", "LN_ERR_UNSUPPORTED",
+    "LN_ERR_CUDA", "LN_ERR_WORKSPACE", "LN_ERR_INVALID", "LN_ERR_SCRATCH_LIMIT",
+    "LN_NOALLOC_SCRATCH_BYTES",
     "load_library", "build_library", "ln_fwd", "ln_fwd_ex", "ln_bwd", "ln_bwd_ex",
     "ln_bwd_workspace_bytes",
     "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc",
-    "exported_symbols",
+    "ln_testing_select_kernels", "exported_symbols", "ln_fwd_from_partials",
+    "LN_PARTIALS_SUM_SQ", "LN_PARTIALS_SUM_M2", "fused_norm_fwd_from_partials",
     "fused_norm_fwd", "fused_norm_bwd", "Workspace",
 ]
 
+# Mirrors of include/normfuse.h (a CPU test checks them against the header).
 LN_F32, LN_BF16, LN_F16 = 0, 1, 2
 LN_LAYERNORM, LN_RMSNORM = 0, 1
+(LN_OK, LN_ERR_NULL, LN_ERR_ALIGN, LN_ERR_SHAPE, LN_ERR_UNSUPPORTED, LN_ERR_CUDA,
+ LN_ERR_WORKSPACE, LN_ERR_INVALID, LN_ERR_SCRATCH_LIMIT) = range(9)
+LN_NOALLOC_SCRATCH_BYTES = 16 << 20
+LN_PARTIALS_SUM_SQ, LN_PARTIALS_SUM_M2 = 0, 1
+_PARTIAL_CODES = {"sum_sq": LN_PARTIALS_SUM_SQ, "sum_m2": LN_PARTIALS_SUM_M2,
+                  LN_PARTIALS_SUM_SQ: LN_PARTIALS_SUM_SQ, LN_PARTIALS_SUM_M2: LN_PARTIALS_SUM_M2}
 _DTYPE_CODES = {torch.float32: LN_F32, torch.bfloat16: LN_BF16, torch.float16: LN_F16}
 _MODE_CODES = {"layernorm": LN_LAYERNORM, "rmsnorm": LN_RMSNORM,
                LN_LAYERNORM: LN_LAYERNORM, LN_RMSNORM: LN_RMSNORM}
@@ -88,6 +99,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.ln_bwd_noalloc.restype = ci
         lib.ln_softmax_fwd.argtypes = [vp, vp, vp, i64, i64, ci]
         lib.ln_softmax_fwd.restype = ci
+        lib.ln_fwd_from_partials.argtypes = [vp, vp, vp, i64, i64, ci, vp, vp, f32, ci, ci, vp,
+                                             vp, vp, vp, vp, i64, i64, ci]
+        lib.ln_fwd_from_partials.restype = ci
+        lib.ln_testing_select_kernels.argtypes = [ci, ci, ci]
+        lib.ln_testing_select_kernels.restype = ci
         _lib = lib
         return lib
 
@@ -96,7 +112,24 @@ def exported_symbols() -> list[str]:
     """Names of the C entry points this binding wraps."""
     return ["ln_fwd", "ln_fwd_ex", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes",
             "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc",
-            "ln_softmax_fwd"]
+            "ln_softmax_fwd", "ln_testing_select_kernels", "ln_fwd_from_partials"]
+
+
+_FAMILY_CODES = {"default": 0, "ring": 1}
+
+
+def ln_testing_select_kernels(forward="default", backward="default", softmax="default") -> None:
+    """Testing hook (include/normfuse_testing.h): plan later calls with the
+    default kernels of each shape ("default") or with the bulk-copy ring
+    kernels ("ring"), per direction. Process-wide."""
+    lib = load_library()
+    try:
+        codes = [_FAMILY_CODES[v] for v in (forward, backward, softmax)]
+    except KeyError as e:
+        raise ValueError(f"unknown kernel family {e.args[0]!r}") from None
+    st = lib.ln_testing_select_kernels(*codes)
+    if st:
+        raise NormError(st, "ln_testing_select_kernels")
 
 
 def ln_status_string(status: int) -> str:
@@ -190,6 +223,28 @@ def ln_fwd_ex(x, bias, residual, gamma, beta, eps, mode, zero_centered_gamma, ou
                        _ptr(fp8_scale), _stream(stream), rows, hidden, _dtype(x))
     if st:
         raise NormError(st, "ln_fwd_ex")
+
+
+def ln_fwd_from_partials(x, psum, psq, tile_cols, kind, gamma, beta, eps, mode,
+                         zero_centered_gamma, y, mean, rstd, amax, stream=None) -> None:
+    """Enqueue the normalize step with row statistics combined from per
+    column-tile partials: ``psum``/``psq`` are fp32 [rows, ceil(hidden /
+    tile_cols)] tensors, ``kind`` "sum_sq" or "sum_m2" (see
+    ``ln_fwd_from_partials`` in include/normfuse.h)."""
+    lib = load_library()
+    rows, hidden = _shape(x)
+    n_tiles = psum.shape[-1] if psum is not None else -(-hidden // int(tile_cols))
+    try:
+        k = _PARTIAL_CODES[kind]
+    except KeyError:
+        raise ValueError(f"unknown partial kind {kind!r}") from None
+    st = lib.ln_fwd_from_partials(_ptr(x), _ptr(psum), _ptr(psq), int(n_tiles), int(tile_cols),
+                                  k, _ptr(gamma), _ptr(beta), float(eps), _mode(mode),
+                                  int(bool(zero_centered_gamma)), _ptr(y), _ptr(mean),
+                                  _ptr(rstd), _ptr(amax), _stream(stream), rows, hidden,
+                                  _dtype(x))
+    if st:
+        raise NormError(st, "ln_fwd_from_partials")
 
 
 def ln_bwd_workspace_bytes(rows: int, hidden: int, dtype, mode) -> int:
@@ -314,6 +369,22 @@ def fused_norm_fwd(x, gamma, beta=None, *, bias=None, residual=None, eps=1e-5,
     ln_fwd(x, bias, residual, gamma, None if rms else beta, eps, mode, zero_centered_gamma,
            out_sum, y, mean, rstd, am, stream)
     return {"y": y, "sum": out_sum, "mean": mean, "rstd": rstd, "amax": am}
+
+
+def fused_norm_fwd_from_partials(x, psum, psq, tile_cols, gamma, beta=None, *, kind="sum_sq",
+                                 eps=1e-5, mode="layernorm", zero_centered_gamma=False,
+                                 amax=False, stream=None):
+    """Allocate the outputs with torch and run ``ln_fwd_from_partials``;
+    returns a dict with ``y``, ``mean`` (LayerNorm), ``rstd``, ``amax``."""
+    rows, hidden = _shape(x)
+    rms = _mode(mode) == LN_RMSNORM
+    y = torch.empty_like(x)
+    mean = None if rms else torch.empty(rows, dtype=torch.float32, device=x.device)
+    rstd = torch.empty(rows, dtype=torch.float32, device=x.device)
+    am = torch.empty(1, dtype=torch.float32, device=x.device) if amax else None
+    ln_fwd_from_partials(x, psum, psq, tile_cols, kind, gamma, None if rms else beta, eps, mode,
+                         zero_centered_gamma, y, mean, rstd, am, stream)
+    return {"y": y, "mean": mean, "rstd": rstd, "amax": am}
 
 
 def fused_norm_bwd(dy, x_sum, gamma, mean, rstd, *, mode="layernorm", zero_centered_gamma=False,

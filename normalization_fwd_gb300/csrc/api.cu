@@ -1,13 +1,13 @@
 // C entry points of the fused normalization library: argument validation,
 // per-device caches, dispatch to the per-dtype launchers.
 #include <math.h>
-#include <stdlib.h>
-#include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
 #include "../../include/normfuse.h"
+#include "../../include/normfuse_testing.h"
 #include "launch.h"
 
 namespace nf {
@@ -76,12 +76,13 @@ cudaError_t by_dtype(ln_dtype dt, F&& f) {
 
 }  // namespace
 
-int path_override() {
-  static const int v = [] {
-    const char* e = getenv("NORMFUSE_PATH");
-    return (e && strcmp(e, "registers") == 0) ? kPathRegisters : kPathDefault;
-  }();
-  return v;
+namespace {
+// Kernel family per direction; changed only by ln_testing_select_kernels().
+std::atomic<int> g_family[3] = {{kFamilyDefault}, {kFamilyDefault}, {kFamilyDefault}};
+}  // namespace
+
+int kernel_family(int direction) {
+  return g_family[direction].load(std::memory_order_relaxed);
 }
 
 int device_sm_count(int* sms) {
@@ -180,6 +181,16 @@ const char* ln_status_string(ln_status s) {
 int ln_last_cuda_error(void) { return g_last_cuda_error; }
 
 void nf_set_last_cuda_error(int e) { g_last_cuda_error = e; }
+
+ln_status ln_testing_select_kernels(int forward, int backward, int softmax) {
+  const int f[3] = {forward, backward, softmax};
+  for (int v : f)
+    if (v != LN_TESTING_DEFAULT_KERNELS && v != LN_TESTING_RING_KERNELS) return LN_ERR_INVALID;
+  for (int i = 0; i < 3; ++i)
+    g_family[i].store(f[i] == LN_TESTING_RING_KERNELS ? kFamilyRing : kFamilyDefault,
+                      std::memory_order_relaxed);
+  return LN_OK;
+}
 
 ln_status ln_device_error(cudaStream_t stream, unsigned* flags) {
   if (flags == nullptr) return LN_ERR_NULL;
@@ -281,6 +292,84 @@ ln_status ln_fwd_ex(const void* x, const void* bias, const void* residual, const
     cudaError_t r = fwd_plan<T>(rows, (int)hidden, vec, residual != nullptr, n_params, &p);
     if (r != cudaSuccess) return r;
     return fwd_launch<T>(a, p, stream);
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  return LN_OK;
+}
+
+ln_status ln_fwd_from_partials(const void* x, const float* psum, const float* psq,
+                               int64_t n_tiles, int64_t tile_cols, ln_partials kind,
+                               const void* gamma, const void* beta, float eps, ln_mode mode,
+                               int zero_centered_gamma, void* y, float* mean, float* rstd,
+                               float* amax, cudaStream_t stream, int64_t rows, int64_t hidden,
+                               ln_dtype dtype) {
+  if (dtype != LN_F32 && dtype != LN_BF16 && dtype != LN_F16) return LN_ERR_UNSUPPORTED;
+  if (mode != LN_LAYERNORM && mode != LN_RMSNORM) return LN_ERR_UNSUPPORTED;
+  if (kind != LN_PARTIALS_SUM_SQ && kind != LN_PARTIALS_SUM_M2) return LN_ERR_UNSUPPORTED;
+  if (rows < 0 || hidden < 1 || tile_cols < 1) return LN_ERR_SHAPE;
+  if (n_tiles != (hidden + tile_cols - 1) / tile_cols) return LN_ERR_SHAPE;
+  if (!(eps >= 0.0f) || !isfinite(eps)) return LN_ERR_INVALID;
+  const bool rms = mode == LN_RMSNORM;
+  if (rms) {
+    beta = nullptr;
+    mean = nullptr;
+  }
+  if (gamma == nullptr) return LN_ERR_NULL;
+  if (rows > 0 && (x == nullptr || y == nullptr || psum == nullptr || psq == nullptr))
+    return LN_ERR_NULL;
+  const size_t es = elem_size(dtype);
+  const void* tensors[] = {x, gamma, beta, y};
+  for (const void* p : tensors)
+    if (!aligned(p, es)) return LN_ERR_ALIGN;
+  if (!aligned(psum, 4) || !aligned(psq, 4) || !aligned(mean, 4) || !aligned(rstd, 4) ||
+      !aligned(amax, 4))
+    return LN_ERR_ALIGN;
+  bool vec = (hidden * (int64_t)es) % 16 == 0;
+  for (const void* p : tensors)
+    if (!aligned(p, 16)) vec = false;
+  if (hidden > max_hidden(dtype, vec)) {
+    if (!vec || hidden > max_hidden(dtype, false)) return LN_ERR_SHAPE;
+    vec = false;
+  }
+  const size_t mat = (size_t)rows * (size_t)hidden * es, vecb = (size_t)hidden * es;
+  const size_t pb = (size_t)rows * (size_t)n_tiles * 4;
+  const Range outs[] = {{y, mat}, {mean, (size_t)rows * 4}, {rstd, (size_t)rows * 4},
+                        {amax, amax ? 4u : 0u}};
+  const Range ins[] = {{x, mat}, {psum, pb}, {psq, pb}, {gamma, vecb}, {beta, vecb}};
+  if (any_overlap(outs, 4, ins, 5)) return LN_ERR_INVALID;
+
+  if (amax) {
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (rows == 0) return LN_OK;
+  PartialsArgs a;
+  a.x = x;
+  a.psum = psum;
+  a.psq = psq;
+  a.gamma = gamma;
+  a.beta = beta;
+  a.y = y;
+  a.mean = mean;
+  a.rstd = rstd;
+  a.amax = reinterpret_cast<unsigned*>(amax);
+  a.rows = rows;
+  a.hidden = (int)hidden;
+  a.n_tiles = (int)n_tiles;
+  a.tile_cols = (int)(tile_cols < hidden ? tile_cols : hidden);
+  a.inv_tile = 1.0f / (float)a.tile_cols;
+  a.inv_last = 1.0f / (float)(hidden - (n_tiles - 1) * a.tile_cols);
+  a.eps = eps;
+  a.inv_hidden = 1.0f / (float)hidden;
+  a.kind = kind == LN_PARTIALS_SUM_M2 ? 1 : 0;
+  a.rms = rms ? 1 : 0;
+  a.zero_centered = zero_centered_gamma ? 1 : 0;
+  cudaError_t e = by_dtype(dtype, [&](auto t) {
+    using T = decltype(t);
+    Plan p;
+    cudaError_t r = partials_plan<T>(rows, (int)hidden, vec, &p);
+    if (r != cudaSuccess) return r;
+    return partials_launch(a, p, stream);
   });
   if (e != cudaSuccess) return cuda_fail(e);
   return LN_OK;

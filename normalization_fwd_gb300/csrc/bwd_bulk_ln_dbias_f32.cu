@@ -1,8 +1,8 @@
 // Pipelined backward kernels (LayerNorm, with dbias), f32 I/O.
 #include "tables.cuh"
 
-const void* nf::bwd_bulk_ln_dbias_table_f32(int kind, int group, int n) {
-  return bwd_bulk_table_impl<float, false, true>(kind, group, n);
+const void* nf::bwd_bulk_ln_dbias_table_f32(int kind, int group, int n, bool exact) {
+  return bwd_bulk_table_impl<float, false, true>(kind, group, n, exact);
 }
 cudaError_t nf::take_error_bwd_bulk_ln_dbias_f32(cudaStream_t st, unsigned* out) {
   return take_tu_error(st, out);

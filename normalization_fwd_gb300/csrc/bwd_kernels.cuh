@@ -19,13 +19,12 @@
 //    RMSNorm up to 8192, LayerNorm up to 4096): the row straight from global
 //    memory into registers, a CTA per row.
 //  * bwd_bulk_warp_kernel / bwd_bulk_group_kernel / bwd_bulk_cta_kernel
-//    (the other 16-byte aligned rows; all of them with NORMFUSE_BWD_PATH=ring):
+//    (the other 16-byte aligned rows, and all of them when a test selects the
+//    ring family through ln_testing_select_kernels):
 //    dy and x_sum tiles stream into a shared-memory ring by
 //    cp.async.bulk; the row is read from shared memory twice (sums, then dx)
 //    instead of being held in registers, and w = gamma (+1) sits in shared
 //    memory as fp32.
-//  * bwd_warp_kernel / bwd_cta_kernel: the row held in registers
-//    (NORMFUSE_PATH=registers).
 //  * bwd_scalar_kernel: any hidden size and alignment.
 #pragma once
 
@@ -34,70 +33,6 @@
 #include "fwd_kernels.cuh"
 
 namespace nf {
-
-// One row of the grid-stride register kernels (NORMFUSE_PATH=registers): dx
-// of the row, and the row added into acc_g (dy * xhat) and acc_b (dy). G
-// threads share the row, this one is `t`; xhat and g stay in registers
-// across the row sums.
-template <typename T, int G, int N, typename Reduce2>
-__device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_ok, int t,
-                                        const T* dyrow, const T* xsrow, float mean, float rstd,
-                                        Reduce2 reduce2, float (&acc_g)[N][Vec<T>::N],
-                                        float (&acc_b)[N][Vec<T>::N]) {
-  constexpr int VEC = Vec<T>::N;
-  const int H = a.hidden;
-  const int V = H / VEC;
-  const T* gamma = static_cast<const T*>(a.gamma);
-
-  uint4 dr[N], xr[N];
-#pragma unroll
-  for (int k = 0; k < N; ++k) {
-    const int v = k * G + t;
-    if (row_ok && v < V) {
-      dr[k] = ld_vec(dyrow + v * VEC);
-      xr[k] = ld_vec(xsrow + v * VEC);
-    }
-  }
-
-  // xhat, g = dy * w, the two row sums, and the outer-reduction partials.
-  float xh[N][VEC], g[N][VEC];
-  float2 sums = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int k = 0; k < N; ++k) {
-    const int v = k * G + t;
-    if (row_ok && v < V) {
-      float d[VEC], xv[VEC], w[VEC];
-      unpack<T>(dr[k], d);
-      unpack<T>(xr[k], xv);
-      unpack<T>(ld_vec_param(gamma + v * VEC), w);
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        const float we = a.zero_centered ? 1.0f + w[e] : w[e];
-        xh[k][e] = (xv[e] - mean) * rstd;
-        g[k][e] = d[e] * we;
-        sums.x += g[k][e];
-        sums.y = fmaf(g[k][e], xh[k][e], sums.y);
-        acc_g[k][e] = fmaf(d[e], xh[k][e], acc_g[k][e]);
-        acc_b[k][e] += d[e];
-      }
-    }
-  }
-  sums = reduce2(sums);
-  const float c1 = a.rms ? 0.f : sums.x / (float)H;
-  const float c2 = sums.y / (float)H;
-
-  T* dx = static_cast<T*>(a.dx) + row * (int64_t)H;
-#pragma unroll
-  for (int k = 0; k < N; ++k) {
-    const int v = k * G + t;
-    if (row_ok && v < V) {
-      float o[VEC];
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) o[e] = rstd * (g[k][e] - c1 - xh[k][e] * c2);
-      st_vec(dx + v * VEC, pack<T>(o));
-    }
-  }
-}
 
 // The row body of the pipelined kernels: dy and x_sum rows in shared memory,
 // w = gamma (+1) staged in shared memory (kStaged), read from global, or
@@ -108,9 +43,14 @@ __device__ __forceinline__ void bwd_row(const BwdArgs& a, int64_t row, bool row_
 // g = dy * w from the first pass (registers the kernel has to spare; the same
 // values either way). Values are fp32 pairs (packed fp32 math). kRms drops
 // the mean, c1 and the dbeta accumulators at compile time; kBias adds the
-// row's fp32 dx into the dbias accumulators.
+// row's fp32 dx into the dbias accumulators. The row means c1 and c2 are the
+// row sums times the fp32 reciprocal of the width (a multiply instead of a
+// division per row). Each vector slot of either pass is skipped as a whole
+// when it lies past the row (or the tile has no row for this group), so the
+// compiler keeps a slot's loads next to their use. kExact: the row has
+// exactly G * N vectors, so no slot lies past it.
 template <typename T, int G, int N, bool kRms, bool kBias, bool kStaged, bool kWReg, int kKeep,
-          typename Reduce2>
+          bool kExact, typename Reduce2>
 __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool row_ok, int t,
                                              uint32_t dyrow, uint32_t xsrow, const ParamRow<T>& wr,
                                              const float2 (&wreg)[N][Vec<T>::N / 2],
@@ -120,8 +60,8 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
                                              float2 (&acc_d)[N][Vec<T>::N / 2]) {
   constexpr int VEC = Vec<T>::N;
   constexpr int P = VEC / 2;
-  const int H = a.hidden;
-  const int V = H / VEC;
+  const int H = kExact ? G * N * VEC : a.hidden;
+  const int V = kExact ? G * N : H / VEC;
   const float2 neg_mean = splat2(-mean);
   const float2 r2 = splat2(rstd);
   const uint32_t wa = kStaged ? wr.saddr() : 0u;
@@ -131,7 +71,49 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     const int v = k * G + t;
-    if (row_ok && v < V) {
+    if (!row_ok || (!kExact && v >= V)) continue;
+    float2 d[P], xv[P], w[P];
+    unpack2<T>(lds_u4(dyrow + v * 16), d);
+    unpack2<T>(lds_u4(xsrow + v * 16), xv);
+    if (kWReg) {
+#pragma unroll
+      for (int i = 0; i < P; ++i) w[i] = wreg[k][i];
+    } else {
+      wr.template load2<kStaged>(v, w, wa);
+    }
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+      const float2 xm = kRms ? xv[i] : add2(xv[i], neg_mean);
+      const float2 xh = mul2(xm, r2);
+      const float2 g = mul2(d[i], w[i]);
+      if (k < kKeep) {
+        keep_xm[k < kKeep ? k : 0][i] = xm;
+        keep_g[k < kKeep ? k : 0][i] = g;
+      }
+      if (!kRms) sx = add2(sx, g);
+      sy = fma2(g, xh, sy);
+      acc_g[k][i] = fma2(d[i], xh, acc_g[k][i]);
+      if (!kRms) acc_b[k][i] = add2(acc_b[k][i], d[i]);
+    }
+  }
+  const float2 sums = reduce2(make_float2(sx.x + sx.y, sy.x + sy.y));
+  // dx = rstd * (g - c1 - xhat * c2) = (x - mean) * b2 + (g * rstd + a1)
+  const float c2 = sums.y * a.inv_hidden;
+  const float2 a1 = splat2(kRms ? 0.f : -rstd * (sums.x * a.inv_hidden));
+  const float2 b2 = splat2(-rstd * rstd * c2);
+  asm volatile("" ::: "memory");   // the second pass reads shared memory again
+
+  T* dx = static_cast<T*>(a.dx) + row * (int64_t)H;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int v = k * G + t;
+    if (!row_ok || (!kExact && v >= V)) continue;
+    float2 o[P];
+    if (k < kKeep) {
+#pragma unroll
+      for (int i = 0; i < P; ++i)
+        o[i] = fma2(keep_xm[k < kKeep ? k : 0][i], b2, fma2(keep_g[k < kKeep ? k : 0][i], r2, a1));
+    } else {
       float2 d[P], xv[P], w[P];
       unpack2<T>(lds_u4(dyrow + v * 16), d);
       unpack2<T>(lds_u4(xsrow + v * 16), xv);
@@ -144,57 +126,14 @@ __device__ __forceinline__ void bwd_row_smem(const BwdArgs& a, int64_t row, bool
 #pragma unroll
       for (int i = 0; i < P; ++i) {
         const float2 xm = kRms ? xv[i] : add2(xv[i], neg_mean);
-        const float2 xh = mul2(xm, r2);
-        const float2 g = mul2(d[i], w[i]);
-        if (k < kKeep) {
-          keep_xm[k < kKeep ? k : 0][i] = xm;
-          keep_g[k < kKeep ? k : 0][i] = g;
-        }
-        if (!kRms) sx = add2(sx, g);
-        sy = fma2(g, xh, sy);
-        acc_g[k][i] = fma2(d[i], xh, acc_g[k][i]);
-        if (!kRms) acc_b[k][i] = add2(acc_b[k][i], d[i]);
-      }
-    }
-  }
-  const float2 sums = reduce2(make_float2(sx.x + sx.y, sy.x + sy.y));
-  // dx = rstd * (g - c1 - xhat * c2) = (x - mean) * b2 + (g * rstd + a1)
-  const float c2 = sums.y / (float)H;
-  const float2 a1 = splat2(kRms ? 0.f : -rstd * (sums.x / (float)H));
-  const float2 b2 = splat2(-rstd * rstd * c2);
-  asm volatile("" ::: "memory");   // the second pass reads shared memory again
-
-  T* dx = static_cast<T*>(a.dx) + row * (int64_t)H;
-#pragma unroll
-  for (int k = 0; k < N; ++k) {
-    const int v = k * G + t;
-    if (k < kKeep && row_ok && v < V) {
-      float2 o[P];
-#pragma unroll
-      for (int i = 0; i < P; ++i) {
-        o[i] = fma2(keep_xm[k < kKeep ? k : 0][i], b2,
-                    fma2(keep_g[k < kKeep ? k : 0][i], r2, a1));
-        if (kBias) acc_d[k][i] = add2(acc_d[k][i], o[i]);
-      }
-      st_vec(dx + v * VEC, pack2<T>(o));
-    } else if (row_ok && v < V) {
-      float2 d[P], xv[P], w[P], o[P];
-      unpack2<T>(lds_u4(dyrow + v * 16), d);
-      unpack2<T>(lds_u4(xsrow + v * 16), xv);
-      if (kWReg) {
-#pragma unroll
-        for (int i = 0; i < P; ++i) w[i] = wreg[k][i];
-      } else {
-        wr.template load2<kStaged>(v, w, wa);
-      }
-#pragma unroll
-      for (int i = 0; i < P; ++i) {
-        const float2 xm = kRms ? xv[i] : add2(xv[i], neg_mean);
         o[i] = fma2(xm, b2, fma2(mul2(d[i], w[i]), r2, a1));
-        if (kBias) acc_d[k][i] = add2(acc_d[k][i], o[i]);
       }
-      st_vec(dx + v * VEC, pack2<T>(o));
     }
+    if (kBias) {
+#pragma unroll
+      for (int i = 0; i < P; ++i) acc_d[k][i] = add2(acc_d[k][i], o[i]);
+    }
+    st_vec(dx + v * VEC, pack2<T>(o));
   }
 }
 
@@ -216,18 +155,6 @@ __device__ __forceinline__ void unpair_acc(const float2 (&p)[N][Vec<T>::N / 2],
     for (int i = 0; i < Vec<T>::N / 2; ++i) {
       f[k][2 * i] = p[k][i].x;
       f[k][2 * i + 1] = p[k][i].y;
-    }
-}
-
-template <typename T, int N>
-__device__ __forceinline__ void zero_acc(float (&acc_g)[N][Vec<T>::N],
-                                         float (&acc_b)[N][Vec<T>::N]) {
-#pragma unroll
-  for (int k = 0; k < N; ++k)
-#pragma unroll
-    for (int e = 0; e < Vec<T>::N; ++e) {
-      acc_g[k][e] = 0.f;
-      acc_b[k][e] = 0.f;
     }
 }
 
@@ -366,54 +293,6 @@ __device__ __forceinline__ void store_rowgroup_partials(const BwdArgs& a,
   }
 }
 
-// ---- register kernels ------------------------------------------------------
-
-template <typename T, int LANES, int N>
-__global__ void __launch_bounds__(kWarpCta) bwd_warp_kernel(const BwdArgs a) {
-  constexpr int RPW = 32 / LANES;
-  constexpr int W = kWarpCta / 32;
-  __shared__ float red[W][LANES * Vec<T>::N];
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int sub = lane / LANES;
-  const int l = lane % LANES;
-  const T* dy = static_cast<const T*>(a.dy);
-  const T* xs = static_cast<const T*>(a.x_sum);
-  float acc_g[N][Vec<T>::N], acc_b[N][Vec<T>::N];
-  zero_acc<T, N>(acc_g, acc_b);
-
-  const int64_t step = (int64_t)gridDim.x * W * RPW;
-  for (int64_t base = ((int64_t)blockIdx.x * W + warp) * RPW; base < a.rows; base += step) {
-    const int64_t row = base + sub;
-    const bool ok = row < a.rows;
-    const float rstd = ok ? a.rstd[row] : 0.f;
-    const float mean = (ok && !a.rms) ? a.mean[row] : 0.f;
-    const int64_t off = row * (int64_t)a.hidden;
-    bwd_row<T, LANES, N>(a, row, ok, l, dy + off, xs + off, mean, rstd,
-                                            [](float2 v) { return group_sum2<LANES>(v); },
-                                            acc_g, acc_b);
-  }
-  store_group_partials<T, LANES, N, W, false, false>(a, acc_g, acc_b, acc_b, red);
-}
-
-template <typename T, int THREADS, int N>
-__global__ void __launch_bounds__(THREADS) bwd_cta_kernel(const BwdArgs a) {
-  __shared__ float2 red[THREADS / 32];
-  const T* dy = static_cast<const T*>(a.dy);
-  const T* xs = static_cast<const T*>(a.x_sum);
-  float acc_g[N][Vec<T>::N], acc_b[N][Vec<T>::N];
-  zero_acc<T, N>(acc_g, acc_b);
-  for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
-    const float rstd = a.rstd[row];
-    const float mean = a.rms ? 0.f : a.mean[row];
-    const int64_t off = row * (int64_t)a.hidden;
-    bwd_row<T, THREADS, N>(
-        a, row, true, threadIdx.x, dy + off, xs + off, mean, rstd,
-        [&](float2 v) { return cta_sum2<THREADS>(v, red); }, acc_g, acc_b);
-  }
-  store_thread_partials<T, THREADS, N, false, false>(a, threadIdx.x, acc_g, acc_b, acc_b);
-}
-
 // ---- bulk-copy pipelined kernels ------------------------------------------
 
 // Vectors per lane whose first-pass values the lane-group backward keeps for
@@ -424,7 +303,8 @@ __global__ void __launch_bounds__(THREADS) bwd_cta_kernel(const BwdArgs a) {
 template <typename T, int N, bool kRms, bool kBias>
 constexpr int kKeepWarp = (sizeof(T) == 2 && !kRms && !kBias && N == 3) ? 1 : 0;
 
-template <typename T, int LANES, int N, bool kRms, bool kBias>
+// kExact: the row has exactly LANES * N vectors (the planner's usual fit).
+template <typename T, int LANES, int N, bool kRms, bool kBias, bool kExact>
 __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const BwdArgs a,
                                                                          const BulkCfg c) {
   constexpr int RPW = 32 / LANES;
@@ -452,14 +332,15 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
   zero_acc2<T, N>(acc_g);
   zero_acc2<T, N>(acc_b);
   zero_acc2<T, N>(acc_d);
-  // Statistics of this group's row in a tile, loaded one tile ahead.
+  // Statistics of this group's row in a tile, loaded one tile ahead (a
+  // tile past the last one has no row below a.rows).
   auto load_stats = [&](int64_t tile, float& m, float& r) {
     const int64_t row = tile * c.tile_rows + local;
     m = 0.f;
     r = 0.f;
-    if (tile < c.num_tiles && row < a.rows) {
+    if (row < a.rows) {
       r = a.rstd[row];
-      if (!a.rms) m = a.mean[row];
+      if (!kRms) m = a.mean[row];
     }
   };
   float nm, nr;
@@ -473,7 +354,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
         const int64_t row = tile * c.tile_rows + local;
         const uint32_t dys = smem_addr(slot) + (uint32_t)(local * H * sizeof(T));
         const uint32_t xss = dys + in_bytes;
-        bwd_row_smem<T, LANES, N, kRms, kBias, true, false, kKeepWarp<T, N, kRms, kBias>>(
+        bwd_row_smem<T, LANES, N, kRms, kBias, true, false, kKeepWarp<T, N, kRms, kBias>, kExact>(
             a, row, row < a.rows, l, dys, xss, wr, wreg, mean, rstd,
             [](float2 v) { return group_sum2<LANES>(v); }, acc_g, acc_b, acc_d);
       });
@@ -534,9 +415,9 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_group_kernel(const B
     const int64_t row = tile * c.tile_rows + local;
     m = 0.f;
     r = 0.f;
-    if (tile < c.num_tiles && row < a.rows) {
+    if (row < a.rows) {
       r = a.rstd[row];
-      if (!a.rms) m = a.mean[row];
+      if (!kRms) m = a.mean[row];
     }
   };
   // Sum of a float2 over the group: warp butterfly, then the group's warps
@@ -566,7 +447,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_group_kernel(const B
         const int64_t row = tile * c.tile_rows + local;
         const uint32_t dys = smem_addr(slot) + (uint32_t)(local * H * sizeof(T));
         const uint32_t xss = dys + in_bytes;
-        bwd_row_smem<T, G, N, kRms, kBias, true, false, 0>(a, row, row < a.rows, t, dys, xss, wr,
+        bwd_row_smem<T, G, N, kRms, kBias, true, false, 0, false>(a, row, row < a.rows, t, dys, xss, wr,
                                                         wreg, mean, rstd, row_sum, acc_g,
                                                         acc_b, acc_d);
       });
@@ -615,7 +496,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2)
     r = 0.f;
     if (row < a.rows) {
       r = a.rstd[row];
-      if (!a.rms) m = a.mean[row];
+      if (!kRms) m = a.mean[row];
     }
   };
   float nm, nr;
@@ -629,7 +510,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2)
         load_stats(row + gridDim.x, nm, nr);
         const uint32_t dys = smem_addr(slot);
         const uint32_t xss = dys + in_bytes;
-        bwd_row_smem<T, kBulkThreads, N, kRms, kBias, false, kWReg, 0>(
+        bwd_row_smem<T, kBulkThreads, N, kRms, kBias, false, kWReg, 0, false>(
             a, row, true, threadIdx.x, dys, xss, wr, wreg, mean, rstd,
             [&](float2 v) { return cta_sum2_db<kBulkThreads>(v, red, parity); }, acc_g, acc_b,
             acc_d);
@@ -711,8 +592,8 @@ __device__ __forceinline__ void row_cta_rows(const BwdArgs& a, float2 (*red)[kCo
     const float2 sums = cta_sum2_db<kBulkThreads>(
         make_float2(kRms ? 0.f : sx.x + sx.y, sy.x + sy.y), red, parity);
     // dx = rstd * (g - c1 - xhat * c2) = (x - mean) * b2 + (g * rstd + a1)
-    const float c2 = sums.y / (float)H;
-    const float2 a1 = splat2(kRms ? 0.f : -rstd * (sums.x / (float)H));
+    const float c2 = sums.y * a.inv_hidden;
+    const float2 a1 = splat2(kRms ? 0.f : -rstd * (sums.x * a.inv_hidden));
     const float2 b2 = splat2(-rstd * rstd * c2);
     vec_fence<N>(dr);
     vec_fence<N>(xr);
@@ -784,6 +665,156 @@ __global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdA
   if (kBias) put(acc_d, kRms ? H : 2 * H);
 }
 
+// The same rows with the next row's dy and x_sum (and statistics) loaded
+// into registers while this row is worked on, so each CTA keeps two rows in
+// flight, at two CTAs per SM; w = gamma (+1 for zero-centered gamma) is
+// staged once per kernel in shared memory as fp32, each thread holding only
+// its own columns ([k][pair of float2][thread] float4: no bank conflicts, no
+// barrier), which saves the per-row unpacking of gamma. Taken when the
+// accumulators and both rows fit in registers at two CTAs per SM (the
+// planner's bwd_row_pf_fits). Results are bit-identical to
+// bwd_row_cta_kernel's: the same operations in the same order.
+template <typename T, int N, bool kRms, bool kBias>
+__global__ void __launch_bounds__(kBulkThreads, 2) bwd_row_pf_kernel(const BwdArgs a) {
+  constexpr int VEC = Vec<T>::N;
+  constexpr int P = VEC / 2;
+  constexpr int Q = P / 2;   // float4 per vector of w
+  extern __shared__ __align__(16) float4 w_s[];   // [N][Q][kBulkThreads]
+  __shared__ float2 red[2][kConsumerWarps];
+  const int t = threadIdx.x;
+  const int H = a.hidden;
+  const int V = H / VEC;
+  const T* dy = static_cast<const T*>(a.dy);
+  const T* xs = static_cast<const T*>(a.x_sum);
+  T* dx = static_cast<T*>(a.dx);
+  {
+    const T* gamma = static_cast<const T*>(a.gamma);
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int v = k * kBulkThreads + t;
+      if (v < V) {
+        float2 w[P];
+        unpack2<T>(ld_vec_param(gamma + v * VEC), w);
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+          float2 w0 = w[2 * q], w1 = w[2 * q + 1];
+          if (a.zero_centered) {
+            w0 = add2(w0, splat2(1.f));
+            w1 = add2(w1, splat2(1.f));
+          }
+          w_s[(k * Q + q) * kBulkThreads + t] = make_float4(w0.x, w0.y, w1.x, w1.y);
+        }
+      }
+    }
+  }
+  auto load_w = [&](int k, float2 (&w)[P]) {
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      const float4 f = w_s[(k * Q + q) * kBulkThreads + t];
+      w[2 * q] = make_float2(f.x, f.y);
+      w[2 * q + 1] = make_float2(f.z, f.w);
+    }
+  };
+  float2 acc_g[N][P], acc_b[N][P], acc_d[N][P];
+  zero_acc2<T, N>(acc_g);
+  zero_acc2<T, N>(acc_b);
+  zero_acc2<T, N>(acc_d);
+  uint4 nd[N], nx[N];
+  float nr = 0.f, nm = 0.f;
+  auto load_row = [&](int64_t row) {
+    const int64_t off = row * (int64_t)H;
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int v = k * kBulkThreads + t;
+      if (v < V) {
+        nd[k] = ld_vec(dy + off + v * VEC);
+        nx[k] = ld_vec(xs + off + v * VEC);
+      }
+    }
+    nr = a.rstd[row];
+    if (!kRms) nm = a.mean[row];
+  };
+  if ((int64_t)blockIdx.x < a.rows) load_row(blockIdx.x);
+  int parity = 0;
+  for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+    uint4 dr[N], xr[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      dr[k] = nd[k];
+      xr[k] = nx[k];
+    }
+    const float rstd = nr, mean = nm;
+    if (row + gridDim.x < a.rows) load_row(row + gridDim.x);
+    const int64_t off = row * (int64_t)H;
+    const float2 neg_mean = splat2(-mean);
+    const float2 r2 = splat2(rstd);
+    float2 sx = splat2(0.f), sy = splat2(0.f);
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int v = k * kBulkThreads + t;
+      if (v < V) {
+        float2 d[P], xv[P], w[P];
+        unpack2<T>(dr[k], d);
+        unpack2<T>(xr[k], xv);
+        load_w(k, w);
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+          const float2 xh = mul2(kRms ? xv[i] : add2(xv[i], neg_mean), r2);
+          const float2 g = mul2(d[i], w[i]);
+          if (!kRms) sx = add2(sx, g);
+          sy = fma2(g, xh, sy);
+          acc_g[k][i] = fma2(d[i], xh, acc_g[k][i]);
+          if (!kRms) acc_b[k][i] = add2(acc_b[k][i], d[i]);
+        }
+      }
+    }
+    const float2 sums = cta_sum2_db<kBulkThreads>(
+        make_float2(kRms ? 0.f : sx.x + sx.y, sy.x + sy.y), red, parity);
+    // dx = rstd * (g - c1 - xhat * c2) = (x - mean) * b2 + (g * rstd + a1)
+    const float c2 = sums.y * a.inv_hidden;
+    const float2 a1 = splat2(kRms ? 0.f : -rstd * (sums.x * a.inv_hidden));
+    const float2 b2 = splat2(-rstd * rstd * c2);
+    vec_fence<N>(dr);
+    vec_fence<N>(xr);
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int v = k * kBulkThreads + t;
+      if (v < V) {
+        float2 d[P], xv[P], w[P], o[P];
+        unpack2<T>(dr[k], d);
+        unpack2<T>(xr[k], xv);
+        load_w(k, w);
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+          const float2 gr = kRms ? mul2(mul2(d[i], w[i]), r2)
+                                 : fma2(mul2(d[i], w[i]), r2, a1);
+          o[i] = fma2(kRms ? xv[i] : add2(xv[i], neg_mean), b2, gr);
+          if (kBias) acc_d[k][i] = add2(acc_d[k][i], o[i]);
+        }
+        st_vec(dx + off + v * VEC, pack2<T>(o));
+      }
+    }
+  }
+  allow_dependent_launch();
+  float* ws = a.ws + (int64_t)blockIdx.x * a.ws_cols;
+  auto put = [&](const float2 (&acc)[N][P], int off) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int v = k * kBulkThreads + t;
+      if (v < V) {
+        float4* q = reinterpret_cast<float4*>(ws + off + v * VEC);
+#pragma unroll
+        for (int i = 0; i < P / 2; ++i)
+          q[i] = make_float4(acc[k][2 * i].x, acc[k][2 * i].y, acc[k][2 * i + 1].x,
+                             acc[k][2 * i + 1].y);
+      }
+    }
+  };
+  put(acc_g, 0);
+  if (!kRms) put(acc_b, H);
+  if (kBias) put(acc_d, kRms ? H : 2 * H);
+}
+
 // ---- scalar kernel ----------------------------------------------------------
 
 // Any hidden size and alignment. Dynamic shared memory: 4 * hidden floats
@@ -827,8 +858,8 @@ __global__ void __launch_bounds__(kScalarCta) bwd_scalar_kernel(const BwdArgs a)
       acc_b[j] += d;
     }
     sums = cta_sum2<kScalarCta>(sums, red);
-    const float c1 = a.rms ? 0.f : sums.x / (float)H;
-    const float c2 = sums.y / (float)H;
+    const float c1 = a.rms ? 0.f : sums.x * a.inv_hidden;
+    const float c2 = sums.y * a.inv_hidden;
     for (int j = threadIdx.x; j < H; j += kScalarCta) {
       const float o = rstd * (sg[j] - c1 - sxh[j] * c2);
       dx[off + j] = from_f<T>(o);

@@ -1,4 +1,4 @@
-// Register and scalar backward kernels, bf16 I/O.
+// Scalar backward kernel (any width and alignment), bf16 I/O.
 #include "tables.cuh"
 
 const void* nf::bwd_reg_table_bf16(int kind, int group, int n) {

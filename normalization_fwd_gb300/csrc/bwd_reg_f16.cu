@@ -1,4 +1,4 @@
-// Register and scalar backward kernels, f16 I/O.
+// Scalar backward kernel (any width and alignment), f16 I/O.
 #include "tables.cuh"
 
 const void* nf::bwd_reg_table_f16(int kind, int group, int n) {

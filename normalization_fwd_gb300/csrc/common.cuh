@@ -14,7 +14,6 @@ using bf16 = __nv_bfloat16;
 using f16 = __half;
 
 // Block shapes shared by the kernels and the host-side planner.
-constexpr int kWarpCta = 256;          // threads per CTA of the register kernels
 constexpr int kScalarCta = 256;        // threads per CTA of the scalar kernels
 constexpr int kConsumerWarps = 8;      // warps of a pipelined CTA
 constexpr int kBulkThreads = kConsumerWarps * 32;

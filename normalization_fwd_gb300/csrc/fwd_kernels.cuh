@@ -12,13 +12,11 @@
 //    per row (rows of more than 256 vectors), as many CTAs as that takes;
 //    rows go straight from global memory into registers and the CTA
 //    scheduler keeps loads in flight as CTAs end and start.
-//  * fwd_bulk_warp_kernel / fwd_bulk_cta_kernel (NORMFUSE_FWD_PATH=ring):
+//  * fwd_bulk_warp_kernel / fwd_bulk_cta_kernel (selected by a test through
+//    ln_testing_select_kernels):
 //    persistent CTAs; tiles of rows stream into a shared-memory ring by
 //    cp.async.bulk (every slot in flight, each refilled by the warp that
 //    frees it last) and 8 warps normalize them from shared memory.
-//  * fwd_warp_kernel / fwd_cta_kernel: persistent grid-stride loops with the
-//    row loaded straight into registers (NORMFUSE_PATH=registers, or when
-//    the ring does not fit).
 //  * fwd_scalar_kernel: any hidden size and alignment; element-wise loads,
 //    the row staged in shared memory.
 #pragma once
@@ -27,169 +25,6 @@
 #include "common.cuh"
 
 namespace nf {
-
-// One row of the grid-stride register kernels (NORMFUSE_PATH=registers). `G`
-// threads share the row, this one is `t`; `xrow` / `rrow` point at the row's
-// x and residual in global memory (rrow is null without a residual).
-// `reduce` sums a float over the G threads.
-template <typename T, int G, int N, typename Reduce>
-__device__ __forceinline__ void fwd_row(const FwdArgs& a, int64_t row, bool row_ok, int t,
-                                        const T* xrow, const T* rrow, Reduce reduce,
-                                        unsigned& amax_acc, bool write_stats) {
-  constexpr int VEC = Vec<T>::N;
-  const int H = a.hidden;
-  const int V = H / VEC;
-  const int64_t off = row * (int64_t)H;
-  const T* bias = static_cast<const T*>(a.bias);
-
-  // Issue every load of the row before using any of it.
-  uint4 xr[N], rr[N];
-#pragma unroll
-  for (int k = 0; k < N; ++k) {
-    const int v = k * G + t;
-    if (row_ok && v < V) {
-      xr[k] = ld_vec(xrow + v * VEC);
-      if (rrow) rr[k] = ld_vec(rrow + v * VEC);
-    }
-  }
-
-  // F1: s = (x + bias) + residual in fp32, rounded to T and stored; the
-  // statistics see the stored value.
-  float s[N][VEC];
-#pragma unroll
-  for (int k = 0; k < N; ++k) {
-    const int v = k * G + t;
-    const bool ok = row_ok && v < V;
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) s[k][e] = 0.f;
-    if (ok) {
-      unpack<T>(xr[k], s[k]);
-      if (bias) {
-        float b[VEC];
-        unpack<T>(ld_vec_param(bias + v * VEC), b);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) s[k][e] += b[e];
-      }
-      if (rrow) {
-        float r[VEC];
-        unpack<T>(rr[k], r);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) s[k][e] += r[e];
-      }
-      const uint4 packed = pack<T>(s[k]);
-      if (a.out_sum) st_vec(static_cast<T*>(a.out_sum) + off + v * VEC, packed);
-      unpack<T>(packed, s[k]);
-    }
-  }
-
-  // F2: mean, then the centred sum of squares from the registers
-  // (RMSNorm: the plain sum of squares).
-  float mean = 0.f;
-  if (!a.rms) {
-    float t1 = 0.f;
-#pragma unroll
-    for (int k = 0; k < N; ++k)
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) t1 += s[k][e];
-    mean = reduce(t1) / (float)H;
-  }
-  // Centre in place (s - mean is needed twice).
-  float t2 = 0.f;
-#pragma unroll
-  for (int k = 0; k < N; ++k) {
-    const bool ok = row_ok && (k * G + t) < V;
-    if (ok) {
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        s[k][e] -= mean;
-        t2 = fmaf(s[k][e], s[k][e], t2);
-      }
-    }
-  }
-  const float var = reduce(t2) / (float)H;
-  const float rstd = 1.0f / sqrtf(var + a.eps);
-
-  if (row_ok && write_stats) {
-    if (a.mean) a.mean[row] = mean;
-    if (a.rstd) a.rstd[row] = rstd;
-  }
-
-  // F3: normalize and affine; F4: amax of the stored y.
-  const T* gamma = static_cast<const T*>(a.gamma);
-  const T* beta = static_cast<const T*>(a.beta);
-  T* y = static_cast<T*>(a.y) + off;
-#pragma unroll
-  for (int k = 0; k < N; ++k) {
-    const int v = k * G + t;
-    if (row_ok && v < V) {
-      float w[VEC], b[VEC], o[VEC];
-      unpack<T>(ld_vec_param(gamma + v * VEC), w);
-      if (beta) {
-        unpack<T>(ld_vec_param(beta + v * VEC), b);
-      } else {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) b[e] = 0.f;
-      }
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        const float we = a.zero_centered ? 1.0f + w[e] : w[e];
-        o[e] = fmaf(s[k][e] * rstd, we, b[e]);
-      }
-      const uint4 packed = pack<T>(o);
-      if (a.y) st_vec(y + v * VEC, packed);
-      if (a.amax) amax_update<T>(amax_acc, packed);
-      if (a.y_fp8) {           // FP8 of the stored (rounded) y
-        float2 yr[VEC / 2];
-        unpack2<T>(packed, yr);
-        store_fp8<VEC>(a.y_fp8 + off + v * VEC, yr, *a.fp8_scale);
-      }
-    }
-  }
-}
-
-// ---- register kernels ------------------------------------------------------
-
-template <typename T, int LANES, int N>
-__global__ void __launch_bounds__(kWarpCta) fwd_warp_kernel(const FwdArgs a) {
-  constexpr int RPW = 32 / LANES;     // rows per warp step
-  constexpr int W = kWarpCta / 32;
-  __shared__ unsigned red_amax[W];
-  const int lane = threadIdx.x & 31;
-  const int sub = lane / LANES;
-  const int l = lane % LANES;
-  const T* x = static_cast<const T*>(a.x);
-  const T* res = static_cast<const T*>(a.residual);
-  unsigned amax_acc = 0;
-  const int64_t step = (int64_t)gridDim.x * W * RPW;
-  // The loop bound is uniform over the warp so every lane takes part in the
-  // shuffles; a group past the last row runs with its loads and stores off.
-  for (int64_t base = ((int64_t)blockIdx.x * W + (threadIdx.x >> 5)) * RPW; base < a.rows;
-       base += step) {
-    const int64_t row = base + sub;
-    const int64_t off = row * (int64_t)a.hidden;
-    fwd_row<T, LANES, N>(a, row, row < a.rows, l, x + off, res ? res + off : nullptr,
-                                     [](float v) { return group_sum<LANES>(v); }, amax_acc,
-                                     l == 0);
-  }
-  if (a.amax) cta_amax_commit(amax_bits<T>(amax_acc), a.amax, red_amax);
-}
-
-template <typename T, int THREADS, int N>
-__global__ void __launch_bounds__(THREADS) fwd_cta_kernel(const FwdArgs a) {
-  __shared__ float red[THREADS / 32];
-  __shared__ unsigned red_amax[THREADS / 32];
-  const T* x = static_cast<const T*>(a.x);
-  const T* res = static_cast<const T*>(a.residual);
-  unsigned amax_acc = 0;
-  for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
-    const int64_t off = row * (int64_t)a.hidden;
-    fwd_row<T, THREADS, N>(a, row, true, threadIdx.x, x + off,
-                                       res ? res + off : nullptr,
-                                       [&](float v) { return cta_sum<THREADS>(v, red); },
-                                       amax_acc, threadIdx.x == 0);
-  }
-  if (a.amax) cta_amax_commit(amax_bits<T>(amax_acc), a.amax, red_amax);
-}
 
 // ---- bulk-copy pipelined kernels ------------------------------------------
 

@@ -1,4 +1,4 @@
-// Register and scalar forward kernels, bf16 I/O.
+// Scalar forward kernel (any width and alignment), bf16 I/O.
 #include "tables.cuh"
 
 const void* nf::fwd_reg_table_bf16(int kind, int group, int n) {

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "partials_kernels.cuh"
 
 namespace nf {
 
@@ -21,7 +22,8 @@ struct Plan {
   int kind = -1;       // 0 lane group per row, 1 CTA per row, 2 scalar, 3 row group (backward),
                        // 4 lane group from registers, one CTA per row tile,
                        // 5 CTA per row from registers (forward and softmax: one
-                       // CTA per row; backward: a persistent grid over the rows)
+                       // CTA per row; backward: a persistent grid over the rows),
+                       // 6 backward CTA per row with the next row prefetched
   int group = 0;       // threads sharing a row
   int n = 0;           // 16-byte vectors per thread per row
   int block = 0;
@@ -38,23 +40,30 @@ int resident_blocks(const void* fn, int block, size_t smem, int* out);  // retur
 // static shared memory passes the default 48 KiB (cached per kernel).
 int allow_dyn_smem(const void* fn, size_t smem);  // returns cudaError_t
 
-// Kernel family override from the NORMFUSE_PATH environment variable
-// ("registers" selects the register kernels for aligned rows), read once.
-constexpr int kPathDefault = 0;
-constexpr int kPathRegisters = 1;
-int path_override();
+// Kernel family per direction (api.cu): 0 = the default for each shape,
+// 1 = the bulk-copy ring kernels wherever they apply. Only the testing hook
+// ln_testing_select_kernels() changes it; nothing reads the environment.
+constexpr int kFamilyForward = 0;
+constexpr int kFamilyBackward = 1;
+constexpr int kFamilySoftmax = 2;
+constexpr int kFamilyDefault = 0;
+constexpr int kFamilyRing = 1;
+int kernel_family(int direction);
 
 // Kernel tables, one per family and dtype, each defined in its own
-// translation unit: (kind, lanes or threads, vectors per thread) -> kernel.
+// translation unit: (kind, lanes or threads, vectors per thread) -> kernel;
+// the backward's also take whether a lane group's row has exactly
+// lanes * vectors per thread vectors.
 #define NF_DECLARE_TABLES(NAME)                                           \
   const void* fwd_bulk_table_##NAME(int kind, int group, int n);          \
   const void* fwd_reg_table_##NAME(int kind, int group, int n);           \
-  const void* bwd_bulk_ln_table_##NAME(int kind, int group, int n);       \
-  const void* bwd_bulk_rms_table_##NAME(int kind, int group, int n);      \
-  const void* bwd_bulk_ln_dbias_table_##NAME(int kind, int group, int n); \
-  const void* bwd_bulk_rms_dbias_table_##NAME(int kind, int group, int n); \
+  const void* bwd_bulk_ln_table_##NAME(int kind, int group, int n, bool exact);       \
+  const void* bwd_bulk_rms_table_##NAME(int kind, int group, int n, bool exact);      \
+  const void* bwd_bulk_ln_dbias_table_##NAME(int kind, int group, int n, bool exact); \
+  const void* bwd_bulk_rms_dbias_table_##NAME(int kind, int group, int n, bool exact); \
   const void* bwd_reg_table_##NAME(int kind, int group, int n);           \
   const void* softmax_table_##NAME(int kind, int group, int n);           \
+  const void* partials_table_##NAME(int kind, int group, int n);          \
   cudaError_t take_error_softmax_##NAME(cudaStream_t st, unsigned* out);  \
   cudaError_t take_error_fwd_bulk_##NAME(cudaStream_t st, unsigned* out); \
   cudaError_t take_error_bwd_bulk_ln_##NAME(cudaStream_t st, unsigned* out); \
@@ -76,6 +85,10 @@ cudaError_t bwd_plan(int64_t rows, int hidden, bool rms, bool dbias, bool vec, P
 template <typename T>
 cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, void* dgamma, void* dbeta, void* dbias,
                        int grad_dtype, cudaStream_t st);
+
+// Normalize from partial statistics: plan and launch (plan.cu).
+template <typename T> cudaError_t partials_plan(int64_t rows, int hidden, bool vec, Plan* p);
+cudaError_t partials_launch(const PartialsArgs& a, const Plan& p, cudaStream_t st);
 
 // Row softmax: plan and launch (plan.cu).
 template <typename T> cudaError_t softmax_plan(int64_t rows, int hidden, bool vec, Plan* p);

@@ -1,37 +1,29 @@
 // ln_bwd_noalloc: the fused backward for callers that cannot allocate device
 // memory. Its scratch (the per-CTA dgamma/dbeta partials) lives in a static
 // device array of this translation unit instead of a caller workspace.
-#include <mutex>
-
 #include "../../include/normfuse.h"
 #include "launch.h"
 
 namespace {
 
-// The scratch array. Every GPU that loads the library holds these bytes until
-// the process exits. In host code the name is only a stand-in for the symbol;
-// its device address comes from cudaGetSymbolAddress.
+// The scratch array. It belongs to this library's module: a context holds
+// its bytes from the moment the module is loaded in it (on the first call
+// under lazy module loading) until the context is destroyed. In host code
+// the name is only a stand-in for the symbol; its device address comes from
+// cudaGetSymbolAddress.
 __device__ __align__(256) float g_noalloc_scratch[LN_NOALLOC_SCRATCH_BYTES / sizeof(float)];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
-
-// Device address of the scratch array on the current device, looked up once
-// per device (the first call on a device does it, with that device current).
+// Device address of the scratch array in the current context. It is looked
+// up on every call, with the caller's device current, rather than cached: a
+// cached address would outlive a cudaDeviceReset (which rebuilds the primary
+// context and reloads the module at another address) or be handed to a
+// different context made current on the same device. Once the module is
+// loaded the lookup is a host-side table query; it enqueues nothing.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

@@ -1,9 +1,6 @@
 // Host-side planning and launching: which kernel runs a call, its grid,
 // block and shared memory, and the launch itself. Kernels come from the
 // per-family tables of the kernel translation units (tables.cuh).
-#include <stdlib.h>
-#include <string.h>
-
 #include <algorithm>
 
 #include "bulk.cuh"
@@ -81,13 +78,15 @@ template <typename T> struct Tables;
   template <> struct Tables<T> {                                                    \
     static const void* fwd_bulk(int k, int g, int n) { return fwd_bulk_table_##NAME(k, g, n); } \
     static const void* fwd_reg(int k, int g, int n) { return fwd_reg_table_##NAME(k, g, n); }   \
-    static const void* bwd_bulk(int k, int g, int n, bool rms, bool dbias) {        \
-      if (dbias) return rms ? bwd_bulk_rms_dbias_table_##NAME(k, g, n)              \
-                            : bwd_bulk_ln_dbias_table_##NAME(k, g, n);              \
-      return rms ? bwd_bulk_rms_table_##NAME(k, g, n) : bwd_bulk_ln_table_##NAME(k, g, n); \
+    static const void* bwd_bulk(int k, int g, int n, bool rms, bool dbias, bool exact) {  \
+      if (dbias) return rms ? bwd_bulk_rms_dbias_table_##NAME(k, g, n, exact)             \
+                            : bwd_bulk_ln_dbias_table_##NAME(k, g, n, exact);             \
+      return rms ? bwd_bulk_rms_table_##NAME(k, g, n, exact)                              \
+                 : bwd_bulk_ln_table_##NAME(k, g, n, exact);                              \
     }                                                                               \
     static const void* bwd_reg(int k, int g, int n) { return bwd_reg_table_##NAME(k, g, n); }   \
     static const void* softmax(int k, int g, int n) { return softmax_table_##NAME(k, g, n); }   \
+    static const void* partials(int k, int g, int n) { return partials_table_##NAME(k, g, n); } \
   };
 NF_TABLES(float, f32)
 NF_TABLES(bf16, bf16)
@@ -99,37 +98,32 @@ NF_TABLES(f16, f16)
 // slots. The lane-group forward (<= 74 registers) runs three CTAs per SM.
 constexpr size_t kRingTarget = 104 * 1024;
 constexpr size_t kRingTargetFwdGroup = 68 * 1024;
+// The lane-group backward keeps at most three slots once a slot holds
+// 20 KiB or more (three slots of 16 rows at 384 bf16: 199.9 against 201.1 us
+// for four at 576000 rows; the smaller ring leaves more of the SM's on-chip
+// memory to L1, which serves the statistics).
+constexpr size_t kBwdGroupBigSlot = 20 * 1024;
+constexpr int kBwdGroupBigSlotStages = 3;
 constexpr size_t kMaxDynSmem = 200 * 1024;
 constexpr size_t kRingTargetSmx = 48 * 1024;
 
-// Ring targets may be overridden (in KiB) through NORMFUSE_RING_KB_FWD /
-// NORMFUSE_RING_KB_BWD for tuning; read once.
-inline size_t ring_target_kb_env(const char* name) {
-  const char* e = getenv(name);
-  if (e == nullptr) return 0;
-  const long v = strtol(e, nullptr, 10);
-  return (v >= 16 && v <= 200) ? (size_t)v * 1024 : 0;
-}
 // three_ctas: kernels built for three CTAs per SM (the lane-group forward)
 // get the smaller ring. (For the CTA-per-row RMSNorm backward, 2 CTAs with
 // 3 slots measured 167 us at 16384 x 8192 against 176 us for 3 CTAs with 2.)
-inline size_t ring_target(bool bwd, bool three_ctas) {
-  static const size_t fwd_env = ring_target_kb_env("NORMFUSE_RING_KB_FWD");
-  static const size_t bwd_env = ring_target_kb_env("NORMFUSE_RING_KB_BWD");
-  if (bwd && bwd_env) return bwd_env;
-  if (!bwd && fwd_env) return fwd_env;
+inline size_t ring_target(bool three_ctas) {
   return three_ctas ? kRingTargetFwdGroup : kRingTarget;
 }
 
 // Fill in a pipelined plan; false when the ring does not fit. `extra`:
 // shared bytes after the ring's barriers (the backward's fp32 weight row).
 inline bool fill_bulk(Plan* p, const Choice& c, int64_t rows, int hidden, size_t esize, int n_in,
-                      size_t extra, size_t target) {
+                      size_t extra, size_t target, bool bwd_group) {
   const int tile_rows = c.kind == 0 ? kConsumerWarps * (32 / c.group)
                                     : (c.kind == 3 ? kBulkThreads / c.group : 1);
   const size_t slot = (size_t)n_in * tile_rows * hidden * esize;
   const size_t room = target > extra ? target - extra : 0;
   int stages = (int)std::min<size_t>(8, std::max<size_t>(2, room / slot));
+  if (bwd_group && slot >= kBwdGroupBigSlot) stages = std::min(stages, kBwdGroupBigSlotStages);
   size_t smem = (size_t)stages * slot + ring_aux_bytes(stages) + extra;
   if (smem > kMaxDynSmem) return false;
   p->bulk = true;
@@ -144,26 +138,14 @@ inline bool fill_bulk(Plan* p, const Choice& c, int64_t rows, int hidden, size_t
   return true;
 }
 
-// Fill block, shared memory and the rows one CTA covers per loop step of the
-// register or scalar kernels.
-inline int64_t fill_shape(Plan* p, const Choice& c, int hidden, bool bwd, bool dbias) {
+// Block and shared memory of the scalar kernels (one row per CTA step).
+inline void fill_scalar(Plan* p, int hidden, bool bwd, bool dbias) {
   p->bulk = false;
-  p->kind = c.kind;
-  p->group = c.group;
-  p->n = c.n;
-  if (c.kind == 0) {
-    p->block = kWarpCta;
-    p->smem = 0;
-    return (kWarpCta / 32) * (32 / c.group);
-  }
-  if (c.kind == 1) {
-    p->block = c.group;
-    p->smem = 0;
-    return 1;
-  }
+  p->kind = 2;
+  p->group = kScalarCta;
+  p->n = 0;
   p->block = kScalarCta;
   p->smem = (size_t)hidden * sizeof(float) * (bwd ? (dbias ? 5 : 4) : 1);
-  return 1;
 }
 
 // Persistent grid: every CTA resident at once, never more CTAs than row steps.
@@ -184,53 +166,65 @@ inline cudaError_t size_grid(Plan* p, int64_t steps) {
 // Plan shared by both directions. n_in: streamed [rows, hidden] inputs;
 // n_params: [hidden] parameter rows the pipelined kernels stage in shared
 // memory as fp32.
+//
 // Forward: rows straight into registers with one CTA per row tile (kind 4,
-// lane groups) or per row (kind 5, rows of more than 256 vectors), the
-// default; NORMFUSE_FWD_PATH=ring selects the bulk-copy ring kernels.
-inline bool fwd_tile_path() {
-  static const bool v = [] {
-    const char* e = getenv("NORMFUSE_FWD_PATH");
-    return !(e && strcmp(e, "ring") == 0);
-  }();
-  return v;
-}
-
+// lane groups) or per row (kind 5, rows of more than 256 vectors); the ring
+// family selects the bulk-copy ring kernels instead.
+//
 // Backward rows of more than 256 vectors run from registers with a CTA per
-// row (kind 5) when its accumulators (n * VEC floats per reduction: dgamma;
-// dbeta for LayerNorm; dbias) and the row's two inputs (8n registers) fit in
-// 64 registers' worth (56 for LayerNorm, which also keeps the mean and a
-// second row sum live), so the kernel keeps three CTAs per SM without
-// spilling; NORMFUSE_BWD_PATH=ring keeps the pipelined kernel for them.
-inline bool bwd_reg_cta_path() {
-  static const bool v = [] {
-    const char* e = getenv("NORMFUSE_BWD_PATH");
-    return !(e && strcmp(e, "ring") == 0);
-  }();
-  return v;
+// row when the accumulators (n * VEC floats per reduction: dgamma; dbeta for
+// LayerNorm; dbias) and the row's two inputs (8n registers) fit in 64
+// registers' worth (56 for LayerNorm, which also keeps the mean and a second
+// row sum live), so that kernel (kind 5) keeps three or more CTAs per SM
+// without spilling. Its variant with the next row prefetched (kind 6, two
+// CTAs per SM, both rows' inputs in 16n registers) holds four rows per SM in
+// flight; it is taken where it fits in 96 registers' worth and the one-row
+// kernel would hold fewer than four (measured at 16384 x 8192 bf16 RMSNorm
+// 121.6 against 127.7 us, 21845 x 6144 LayerNorm 135.5 against 159.4 us;
+// at 32768 x 4096 RMSNorm, where kind 5 runs four CTAs per SM, 138.5
+// against 128.9 us). The other aligned rows, and these too under the ring
+// family, stream through the bulk-copy ring.
+inline int bwd_acc_floats(int n, int vec_elems, bool rms, bool dbias) {
+  return n * vec_elems * (1 + (rms ? 0 : 1) + (dbias ? 1 : 0));
+}
+inline bool bwd_row_pf_fits(int n, int vec_elems, bool rms, bool dbias) {
+  return n <= 4 && bwd_acc_floats(n, vec_elems, rms, dbias) + 16 * n <= 96;
 }
 inline bool bwd_row_cta_fits(int n, int vec_elems, bool rms, bool dbias) {
-  const int acc = n * vec_elems * (1 + (rms ? 0 : 1) + (dbias ? 1 : 0));
-  return n <= 4 && acc + 8 * n <= (rms ? 64 : 56);
+  return n <= 4 && bwd_acc_floats(n, vec_elems, rms, dbias) + 8 * n <= (rms ? 64 : 56);
 }
+constexpr int kRowsInFlightPf = 4;   // kind 6: two CTAs per SM, two rows each
 
 template <typename T>
 cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bool dbias,
                       int n_in, int n_params, Plan* p) {
-  Choice c = choose(hidden, Vec<T>::N, vec);
-  if (bwd && vec && c.kind == 1 && path_override() != kPathRegisters && bwd_reg_cta_path()) {
+  const Choice c = choose(hidden, Vec<T>::N, vec);
+  const bool ring = kernel_family(bwd ? kFamilyBackward : kFamilyForward) == kFamilyRing;
+  if (bwd && vec && c.kind == 1 && !ring) {
     const int n = bulk_cta_n(hidden, Vec<T>::N);
-    if (bwd_row_cta_fits(n, Vec<T>::N, rms, dbias)) {
+    const bool one = bwd_row_cta_fits(n, Vec<T>::N, rms, dbias);
+    bool pf = bwd_row_pf_fits(n, Vec<T>::N, rms, dbias);
+    if (pf && one) {
+      // keep the one-row kernel where it already holds as many rows per SM
+      int per_sm = 0;
+      cudaError_t e = (cudaError_t)resident_blocks(
+          Tables<T>::bwd_bulk(5, kBulkThreads, n, rms, dbias, false), kBulkThreads, 0, &per_sm);
+      if (e != cudaSuccess) return e;
+      pf = per_sm < kRowsInFlightPf;
+    }
+    if (pf || one) {
       p->bulk = false;
-      p->kind = 5;
+      p->kind = pf ? 6 : 5;
       p->group = kBulkThreads;
       p->n = n;
       p->block = kBulkThreads;
-      p->smem = 0;
-      p->fn = Tables<T>::bwd_bulk(5, kBulkThreads, n, rms, dbias);
+      // kind 6 stages w as fp32: n vectors of VEC floats per thread
+      p->smem = pf ? (size_t)n * Vec<T>::N * sizeof(float) * kBulkThreads : 0;
+      p->fn = Tables<T>::bwd_bulk(p->kind, kBulkThreads, n, rms, dbias, false);
       return size_grid(p, rows);
     }
   }
-  if (!bwd && vec && c.kind == 1 && path_override() != kPathRegisters && fwd_tile_path()) {
+  if (!bwd && vec && c.kind == 1 && !ring) {
     p->bulk = false;
     p->kind = 5;
     p->group = kBulkThreads;
@@ -244,7 +238,7 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
     p->grid = (int)rows;
     return cudaSuccess;
   }
-  if (!bwd && vec && c.kind == 0 && path_override() != kPathRegisters && fwd_tile_path()) {
+  if (!bwd && vec && c.kind == 0 && !ring) {
     p->bulk = false;
     p->kind = 4;
     p->group = c.group;
@@ -260,33 +254,26 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
     p->grid = (int)ctas;
     return cudaSuccess;
   }
-  bool want_bulk = vec && path_override() != kPathRegisters;
-  // The register kernels do not accumulate dbias: in register mode a dbias
-  // call takes the scalar kernel when the row fits it, else the pipelined one.
-  if (bwd && dbias && vec && !want_bulk) {
-    if (hidden <= kMaxHiddenScalar) {
-      c = choose(hidden, 1, false);
-    } else {
-      want_bulk = true;
-    }
-  }
-  if (want_bulk) {
+  if (vec) {
     Choice b = bwd ? bwd_choice(c, hidden, Vec<T>::N, rms, dbias) : c;
     if (c.kind == 1) b.n = bulk_cta_n(hidden, Vec<T>::N);
     // Lane-group and row-group kernels stage the parameter rows in shared
     // memory as fp32; CTA-per-row kernels read them from global memory.
     const size_t extra = (b.kind == 0 || b.kind == 3) ? (size_t)n_params * hidden * sizeof(float) : 0;
     const bool three = !bwd && b.kind == 0 && b.n <= 4;
-    const size_t target = ring_target(bwd, three);
-    if (fill_bulk(p, b, rows, hidden, sizeof(T), n_in, extra, target)) {
-      p->fn = bwd ? Tables<T>::bwd_bulk(b.kind, b.group, b.n, rms, dbias)
+    if (fill_bulk(p, b, rows, hidden, sizeof(T), n_in, extra, ring_target(three),
+                  bwd && b.kind == 0)) {
+      const bool exact = b.kind == 0 && b.group * b.n * Vec<T>::N == hidden;
+      p->fn = bwd ? Tables<T>::bwd_bulk(b.kind, b.group, b.n, rms, dbias, exact)
                   : Tables<T>::fwd_bulk(b.kind, b.group, b.n);
       return size_grid(p, p->cfg.num_tiles);
     }
+    // No ring fits (not reached by any supported width): the scalar kernel.
+    if (hidden > kMaxHiddenScalar) return cudaErrorInvalidConfiguration;
   }
-  p->fn = bwd ? Tables<T>::bwd_reg(c.kind, c.group, c.n) : Tables<T>::fwd_reg(c.kind, c.group, c.n);
-  const int64_t rpc = fill_shape(p, c, hidden, bwd, dbias);
-  return size_grid(p, (rows + rpc - 1) / rpc);
+  p->fn = bwd ? Tables<T>::bwd_reg(2, 0, 0) : Tables<T>::fwd_reg(2, 0, 0);
+  fill_scalar(p, hidden, bwd, dbias);
+  return size_grid(p, rows);
 }
 
 template <typename T>
@@ -333,10 +320,7 @@ cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, void* dgamma, void* dbet
 // Wider rows (more registers, two CTAs per SM) keep the 104 KiB ring.
 template <typename T> cudaError_t softmax_plan(int64_t rows, int hidden, bool vec, Plan* p) {
   const Choice c = choose(hidden, Vec<T>::N, vec);
-  static const int smx_path = [] {
-    const char* e = getenv("NORMFUSE_SMX_PATH");   // "ring": the pipelined kernels
-    return (e && strcmp(e, "ring") == 0) ? 1 : 0;
-  }();
+  const int smx_path = kernel_family(kFamilySoftmax);
   if (smx_path == 0 && c.kind == 1) {
     // Rows of more than 256 vectors: one CTA per row from registers.
     p->bulk = false;
@@ -373,9 +357,8 @@ template <typename T> cudaError_t softmax_plan(int64_t rows, int hidden, bool ve
   if (c.kind == 0 || c.kind == 1) {
     Choice b = c;
     if (c.kind == 1) b.n = bulk_cta_n(hidden, Vec<T>::N);
-    static const size_t env = ring_target_kb_env("NORMFUSE_RING_KB_SMX");
-    const size_t target = env ? env : (b.n <= 4 ? kRingTargetSmx : kRingTarget);
-    if (fill_bulk(p, b, rows, hidden, sizeof(T), 1, 0, target)) {
+    const size_t target = b.n <= 4 ? kRingTargetSmx : kRingTarget;
+    if (fill_bulk(p, b, rows, hidden, sizeof(T), 1, 0, target, false)) {
       p->fn = Tables<T>::softmax(b.kind, b.group, b.n);
       return size_grid(p, p->cfg.num_tiles);
     }
@@ -383,7 +366,7 @@ template <typename T> cudaError_t softmax_plan(int64_t rows, int hidden, bool ve
   }
   if (c.kind != 2) return cudaErrorInvalidConfiguration;
   p->fn = Tables<T>::softmax(2, 0, 0);
-  fill_shape(p, c, hidden, false, false);
+  fill_scalar(p, hidden, false, false);
   return size_grid(p, rows);
 }
 
@@ -391,8 +374,49 @@ cudaError_t softmax_launch(const SmxArgs& a, const Plan& p, cudaStream_t st) {
   return launch_plan(p, const_cast<SmxArgs*>(&a), st);
 }
 
+// Normalize from partials: the forward's register shapes (a lane group per
+// row and one CTA per row tile, or one CTA per row beyond 256 vectors), as
+// many CTAs as the rows need; unaligned rows take the scalar kernel, one CTA
+// per row.
+template <typename T> cudaError_t partials_plan(int64_t rows, int hidden, bool vec, Plan* p) {
+  const Choice c = choose(hidden, Vec<T>::N, vec);
+  p->bulk = false;
+  p->smem = 0;
+  p->block = kBulkThreads;
+  int64_t ctas = rows;
+  if (c.kind == 0) {
+    p->kind = 4;
+    p->group = c.group;
+    p->n = c.n;
+    const int64_t rpc = (int64_t)kConsumerWarps * (32 / c.group);
+    ctas = (rows + rpc - 1) / rpc;
+  } else if (c.kind == 1) {
+    p->kind = 5;
+    p->group = kBulkThreads;
+    p->n = bulk_cta_n(hidden, Vec<T>::N);
+  } else {
+    p->kind = 2;
+    p->group = kScalarCta;
+    p->n = 0;
+    p->block = kScalarCta;
+  }
+  p->fn = Tables<T>::partials(p->kind, p->group, p->n);
+  cudaError_t e = size_grid(p, 1);   // occupancy check
+  if (e != cudaSuccess) return e;
+  if (ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  p->grid = (int)ctas;
+  return cudaSuccess;
+}
+
+cudaError_t partials_launch(const PartialsArgs& a, const Plan& p, cudaStream_t st) {
+  return launch_plan(p, const_cast<PartialsArgs*>(&a), st);
+}
+
 }  // namespace nf
 
+template cudaError_t nf::partials_plan<float>(int64_t, int, bool, nf::Plan*);
+template cudaError_t nf::partials_plan<nf::bf16>(int64_t, int, bool, nf::Plan*);
+template cudaError_t nf::partials_plan<nf::f16>(int64_t, int, bool, nf::Plan*);
 template cudaError_t nf::softmax_plan<float>(int64_t, int, bool, nf::Plan*);
 template cudaError_t nf::softmax_plan<nf::bf16>(int64_t, int, bool, nf::Plan*);
 template cudaError_t nf::softmax_plan<nf::f16>(int64_t, int, bool, nf::Plan*);

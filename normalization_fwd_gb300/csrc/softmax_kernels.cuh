@@ -9,7 +9,8 @@
 //  * smx_reg_kernel / smx_reg_cta_kernel (default for 16-byte aligned rows):
 //    one CTA per tile of rows (lane groups) or per row, rows straight from
 //    global memory into registers.
-//  * smx_bulk_warp_kernel / smx_bulk_cta_kernel (NORMFUSE_SMX_PATH=ring):
+//  * smx_bulk_warp_kernel / smx_bulk_cta_kernel (selected by a test through
+//    ln_testing_select_kernels):
 //    tiles of rows stream into a shared-memory ring by cp.async.bulk (the
 //    ring and refill scheme of the normalization kernels) and 8 warps work on
 //    them from shared memory: a lane group of LANES lanes per row, or all 256

@@ -21,22 +21,16 @@ namespace nf {
     case 8: return (const void*)KERNEL<T, L, 8>;   \
     default: return nullptr;                       \
   }
-#define NF_CTA_CASES(KERNEL, T, TH)                \
-  switch (n) {                                     \
-    case 3: return (const void*)KERNEL<T, TH, 3>;  \
-    case 4: return (const void*)KERNEL<T, TH, 4>;  \
-    default: return nullptr;                       \
-  }
-#define NF_BULK_WARP_CASES_M(KERNEL, T, L, M, B)      \
-  switch (n) {                                        \
-    case 1: return (const void*)KERNEL<T, L, 1, M, B>; \
-    case 2: return (const void*)KERNEL<T, L, 2, M, B>; \
-    case 3: return (const void*)KERNEL<T, L, 3, M, B>; \
-    case 4: return (const void*)KERNEL<T, L, 4, M, B>; \
-    case 5: return (const void*)KERNEL<T, L, 5, M, B>; \
-    case 6: return (const void*)KERNEL<T, L, 6, M, B>; \
-    case 8: return (const void*)KERNEL<T, L, 8, M, B>; \
-    default: return nullptr;                          \
+#define NF_BULK_WARP_CASES_M(KERNEL, T, L, M, B, E)      \
+  switch (n) {                                           \
+    case 1: return (const void*)KERNEL<T, L, 1, M, B, E>; \
+    case 2: return (const void*)KERNEL<T, L, 2, M, B, E>; \
+    case 3: return (const void*)KERNEL<T, L, 3, M, B, E>; \
+    case 4: return (const void*)KERNEL<T, L, 4, M, B, E>; \
+    case 5: return (const void*)KERNEL<T, L, 5, M, B, E>; \
+    case 6: return (const void*)KERNEL<T, L, 6, M, B, E>; \
+    case 8: return (const void*)KERNEL<T, L, 8, M, B, E>; \
+    default: return nullptr;                             \
   }
 #define NF_BULK_CTA_CASES_M(KERNEL, T, M, B)          \
   switch (n) {                                        \
@@ -86,27 +80,24 @@ template <typename T> const void* fwd_bulk_table_impl(int kind, int group, int n
   return nullptr;
 }
 
+// The scalar forward (any width and alignment); `group` and `n` are unused.
 template <typename T> const void* fwd_reg_table_impl(int kind, int group, int n) {
-  if (kind == 0) {
-    if (group == 8) { NF_WARP_CASES(fwd_warp_kernel, T, 8) }
-    if (group == 16) { NF_WARP_CASES(fwd_warp_kernel, T, 16) }
-    if (group == 32) { NF_WARP_CASES(fwd_warp_kernel, T, 32) }
-  } else if (kind == 1) {
-    if (group == 128) { NF_CTA_CASES(fwd_cta_kernel, T, 128) }
-    if (group == 256) { NF_CTA_CASES(fwd_cta_kernel, T, 256) }
-    if (group == 512) { NF_CTA_CASES(fwd_cta_kernel, T, 512) }
-  } else if (kind == 2) {
-    return (const void*)fwd_scalar_kernel<T>;
-  }
-  return nullptr;
+  (void)group;
+  (void)n;
+  return kind == 2 ? (const void*)fwd_scalar_kernel<T> : nullptr;
 }
 
+// exact (lane groups only): the row has exactly group * n vectors.
 template <typename T, bool kRms, bool kBias>
-const void* bwd_bulk_table_impl(int kind, int group, int n) {
-  if (kind == 0) {
-    if (group == 8) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 8, kRms, kBias) }
-    if (group == 16) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 16, kRms, kBias) }
-    if (group == 32) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 32, kRms, kBias) }
+const void* bwd_bulk_table_impl(int kind, int group, int n, bool exact) {
+  if (kind == 0 && exact) {
+    if (group == 8) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 8, kRms, kBias, true) }
+    if (group == 16) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 16, kRms, kBias, true) }
+    if (group == 32) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 32, kRms, kBias, true) }
+  } else if (kind == 0) {
+    if (group == 8) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 8, kRms, kBias, false) }
+    if (group == 16) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 16, kRms, kBias, false) }
+    if (group == 32) { NF_BULK_WARP_CASES_M(bwd_bulk_warp_kernel, T, 32, kRms, kBias, false) }
   } else if (kind == 1) {
     NF_BULK_CTA_CASES_M(bwd_bulk_cta_kernel, T, kRms, kBias)
   } else if (kind == 3) {
@@ -119,23 +110,22 @@ const void* bwd_bulk_table_impl(int kind, int group, int n) {
       case 4: return (const void*)bwd_row_cta_kernel<T, 4, kRms, kBias>;
       default: return nullptr;
     }
+  } else if (kind == 6) {
+    switch (n) {
+      case 2: return (const void*)bwd_row_pf_kernel<T, 2, kRms, kBias>;
+      case 3: return (const void*)bwd_row_pf_kernel<T, 3, kRms, kBias>;
+      case 4: return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias>;
+      default: return nullptr;
+    }
   }
   return nullptr;
 }
 
+// The scalar backward (any width and alignment); `group` and `n` are unused.
 template <typename T> const void* bwd_reg_table_impl(int kind, int group, int n) {
-  if (kind == 0) {
-    if (group == 8) { NF_WARP_CASES(bwd_warp_kernel, T, 8) }
-    if (group == 16) { NF_WARP_CASES(bwd_warp_kernel, T, 16) }
-    if (group == 32) { NF_WARP_CASES(bwd_warp_kernel, T, 32) }
-  } else if (kind == 1) {
-    if (group == 128) { NF_CTA_CASES(bwd_cta_kernel, T, 128) }
-    if (group == 256) { NF_CTA_CASES(bwd_cta_kernel, T, 256) }
-    if (group == 512) { NF_CTA_CASES(bwd_cta_kernel, T, 512) }
-  } else if (kind == 2) {
-    return (const void*)bwd_scalar_kernel<T>;
-  }
-  return nullptr;
+  (void)group;
+  (void)n;
+  return kind == 2 ? (const void*)bwd_scalar_kernel<T> : nullptr;
 }
 
 }  // namespace nf

@@ -15,7 +15,7 @@ import pytest
 import normalization_fwd_gb300 as nf
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "normfuse.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("normfuse.h", "normfuse_testing.h")]
 
 OK, NULL, ALIGN, SHAPE, UNSUPPORTED, CUDA, WORKSPACE, INVALID, SCRATCH_LIMIT = range(9)
 
@@ -27,23 +27,42 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:ln_status|const char\*|int|size_t)\s+(ln_\w+)\s*\(",
-                                 text, flags=re.M)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:ln_status|const char\*|int|size_t)\s+(ln_\w+)\s*\(",
+                                text, flags=re.M))
+    return sorted(names)
+
+
+def test_every_header_is_checked():
+    on_disk = sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
+    assert on_disk == sorted(os.path.basename(h) for h in HEADERS)
 
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["ln_fwd", "ln_fwd_ex", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes",
          "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc",
-         "ln_softmax_fwd"])
+         "ln_softmax_fwd", "ln_testing_select_kernels", "ln_fwd_from_partials"])
 
 
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
     assert sorted(nf.exported_symbols()) == declared_functions()
+
+
+def test_binding_constants_match_the_header():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADERS[0]).read(), flags=re.S)
+    enum = re.search(r"typedef enum \{([^{}]*)\} ln_status;", text, flags=re.S).group(1)
+    codes = dict((k, int(v)) for k, v in re.findall(r"(LN_\w+)\s*=\s*(\d+)", enum))
+    assert codes == {k: getattr(nf, k) for k in codes}
+    assert len(codes) == 9
+    m = re.search(r"#define LN_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert int(m.group(1)) << int(m.group(2)) == nf.LN_NOALLOC_SCRATCH_BYTES
+    for k in ("LN_F32", "LN_BF16", "LN_F16"):
+        assert re.search(rf"{k} = {getattr(nf, k)}\b", text), k
 
 
 def test_status_strings(lib):
@@ -195,6 +214,57 @@ def test_workspace_query_on_host(lib):
     assert lib.ln_bwd_workspace_bytes(10, 0, 1, 0, ctypes.byref(out)) == SHAPE
     assert lib.ln_bwd_workspace_bytes(10, 384, 7, 0, ctypes.byref(out)) == UNSUPPORTED
     assert lib.ln_bwd_workspace_bytes(10, 20000, 1, 0, ctypes.byref(out)) == SHAPE
+
+
+PS, PQ = 0x7f0100000000, 0x7f0110000000
+
+
+def fwdp(lib, x=X, psum=PS, psq=PQ, n_tiles=3, tile_cols=128, kind=0, gamma=G, beta=B,
+         eps=1e-5, mode=0, zc=0, y=Y, mean=M, rstd=R, amax=None, rows=8, hidden=384, dtype=1):
+    return lib.ln_fwd_from_partials(x, psum, psq, n_tiles, tile_cols, kind, gamma, beta, eps,
+                                    mode, zc, y, mean, rstd, amax, None, rows, hidden, dtype)
+
+
+@pytest.mark.parametrize("kw,want", [
+    ({"dtype": 7}, UNSUPPORTED),
+    ({"mode": 3}, UNSUPPORTED),
+    ({"kind": 2}, UNSUPPORTED),
+    ({"rows": -1}, SHAPE),
+    ({"hidden": 0}, SHAPE),
+    ({"tile_cols": 0}, SHAPE),
+    ({"n_tiles": 4}, SHAPE),                 # ceil(384 / 128) = 3
+    ({"n_tiles": 2, "tile_cols": 100}, SHAPE),  # ceil(384 / 100) = 4
+    ({"eps": -1.0}, INVALID),
+    ({"eps": float("inf")}, INVALID),
+    ({"gamma": None}, NULL),
+    ({"x": None}, NULL),
+    ({"psum": None}, NULL),
+    ({"psq": None}, NULL),
+    ({"y": None}, NULL),
+    ({"psum": PS + 2}, ALIGN),
+    ({"x": X + 1}, ALIGN),
+    ({"y": X}, INVALID),                      # output overlaps an input
+    ({"mean": PS}, INVALID),
+])
+def test_fwd_from_partials_rejects_on_host(lib, kw, want):
+    assert fwdp(lib, **kw) == want
+
+
+def test_kernel_family_hook_validates_on_host(lib):
+    assert lib.ln_testing_select_kernels(2, 0, 0) == INVALID
+    assert lib.ln_testing_select_kernels(0, -1, 0) == INVALID
+    assert lib.ln_testing_select_kernels(0, 0, 0) == OK
+    with pytest.raises(ValueError):
+        nf.ln_testing_select_kernels(forward="registers")
+
+
+def test_library_reads_no_environment():
+    """Kernel choice depends on the arguments and the device only: no source
+    of the library reads an environment variable."""
+    csrc = os.path.join(ROOT, "normalization_fwd_gb300", "csrc")
+    for name in os.listdir(csrc):
+        if name.endswith((".cu", ".cuh", ".h")):
+            assert "getenv" not in open(os.path.join(csrc, name)).read(), name
 
 
 def test_device_error_query_rejects_null(lib):

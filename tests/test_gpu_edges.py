@@ -138,6 +138,38 @@ def test_unaligned_pointers_use_scalar_path(cuda_lib, dtype):
     fwd_bwd_parity(cuda_lib, w, seed=2, x_override=x_shifted)
 
 
+# Wide rows with more rows than CTAs, so every CTA of the CTA-per-row
+# backward works on several rows (with the next one prefetched where its
+# registers allow) and the last steps are ragged: each n of the prefetching
+# kernel for both modes, with dbias, in each dtype.
+WIDE = [("bf16", 2056, W.LAYERNORM), ("bf16", 4096, W.RMSNORM), ("bf16", 6144, W.LAYERNORM),
+        ("bf16", 6144, W.RMSNORM), ("bf16", 8192, W.RMSNORM), ("bf16", 8192, W.LAYERNORM),
+        ("f16", 3000, W.RMSNORM), ("f32", 2048, W.LAYERNORM), ("f32", 3072, W.RMSNORM)]
+
+
+@pytest.mark.parametrize("dtype,hidden,mode", WIDE, ids=lambda v: str(v))
+@pytest.mark.parametrize("dbias", [False, True])
+def test_wide_rows_many_rows_per_cta(cuda_lib, dtype, hidden, mode, dbias):
+    w = wl(dtype, 701, hidden, mode, zero_centered_gamma=hidden % 3 == 0)
+    inp = make_inputs(w, seed=12)
+    ref = oracle_fwd(w, inp)
+    dt = W.TORCH_DTYPES[w.dtype]
+    x_sum = torch.from_numpy(ref["sum"]).to(dt)
+    mean = None if ref["mean"] is None else torch.from_numpy(ref["mean"]).float()
+    rstd = torch.from_numpy(ref["rstd"]).float()
+    bref = oracle_bwd_rows(w, inp["dy"], x_sum, inp["gamma"], mean, rstd, slice(None))
+    got = gpu_bwd(cuda_lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd, need_dbias=dbias)
+    assert got["guards_ok"]
+    scale = dx_row_scale(as_f64(inp["dy"]), as_f64(inp["gamma"]), as_f64(rstd),
+                         w.zero_centered_gamma)
+    check_elementwise(as_f64(got["dx"]), bref["dx_exact"], w.dtype, "dx", scale_rows=scale)
+    check_rel_l2(as_f64(got["dgamma"]), bref["dgamma"], 1e-4, "dgamma")
+    if bref["dbeta"] is not None:
+        check_rel_l2(as_f64(got["dbeta"]), bref["dbeta"], 1e-4, "dbeta")
+    if dbias:
+        check_rel_l2(as_f64(got["dbias"]), bref["dbias"], 1e-4, "dbias")
+
+
 @pytest.mark.parametrize("rows,hidden,mode,zc", [
     (50001, 384, W.LAYERNORM, False),     # pipelined lane-group backward
     (3001, 8192, W.RMSNORM, False),       # register CTA-per-row backward
