@@ -1,11 +1,13 @@
 """GPU parity of the FP8 (E4M3) copy of y written by ln_fwd_ex.
 
-Against the oracle: y_fp8 = E4M3(fp32(y_stored * scale)) with the oracle's
-own y; the kernel's stored y may differ from the oracle's by the ulp the
-bf16/fp16 rules allow, which can move a code by one step, so >= 99.9 % of
-codes must be equal and every code within one E4M3 step. As a property of
-the kernel's own output: every code equals torch's float32 -> float8_e4m3fn
-cast of (stored y * scale) clamped to +-448 (the saturating cast).
+The decision the kernel takes, E4M3(fp32(y_stored * scale)) of its own
+stored y, is checked bit for bit against the oracle's ``quantize_fp8_e4m3``
+applied to that stored y (both take the product in fp32, the precision the
+kernel decides in), with torch's float32 -> float8_e4m3fn cast (clamped to
++-448, the saturating cast) as a second opinion. Against the oracle's own y
+(which the kernel's y may differ from by the ulp the bf16/fp16 rules allow,
+moving a code by one step): >= 99.9 % of codes equal and every code within
+one E4M3 step.
 """
 
 import numpy as np
@@ -67,7 +69,12 @@ def test_fp8_output(cuda_lib, w, scale):
     inp = make_inputs(w, seed=21)
     y, q, amax = run_fp8(cuda_lib, w, inp, scale)
     got = decode(q)
-    # property: the saturating E4M3 cast of the kernel's own stored y
+    # bit-exact: the oracle's E4M3 of the kernel's own stored y (value and
+    # sign, which together fix the code of a non-NaN E4M3 number) ...
+    want_own = quantize_fp8_e4m3(as_f64(y), scale)
+    np.testing.assert_array_equal(got, want_own)
+    np.testing.assert_array_equal(np.signbit(got), np.signbit(want_own))
+    # ... and torch's saturating cast of the same product agrees
     prod = y.to(torch.float32) * torch.tensor(scale, dtype=torch.float32)
     want_t = prod.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).to(torch.float64).numpy()
     np.testing.assert_array_equal(got, want_t)
