@@ -201,11 +201,17 @@ def dx_row_scale(dy_rows, gamma, rstd_rows, zero_centered_gamma: bool) -> np.nda
     return np.asarray(rstd_rows, dtype=np.float64) * g.max(axis=1)
 
 
-def check_elementwise(got, ref_exact, fmt: str, what: str, row_scale=True, scale_rows=None):
+def check_elementwise(got, ref_exact, fmt: str, what: str, row_scale=True, scale_rows=None,
+                      max_floored=None):
     """Apply the dtype's element tolerance; returns a short report dict.
 
     ``scale_rows`` (optional, per row) replaces max_row |ref| as the row
-    scale of the ulp floor."""
+    scale of the ulp floor. The report also gives the same counts without
+    the floor (ulp taken at |ref| alone): ``worst_ulp_raw``, ``within1_raw``
+    and ``floored``, the number of elements more than 2 ulp off by that plain
+    rule, i.e. the elements the row-scale floor decided. With
+    ``max_floored`` set, their fraction must not pass it, so an error that
+    hides behind the floor fails loudly."""
     got = np.asarray(got, dtype=np.float64)
     ref_exact = np.asarray(ref_exact, dtype=np.float64)
     assert got.shape == ref_exact.shape, (what, got.shape, ref_exact.shape)
@@ -217,25 +223,42 @@ def check_elementwise(got, ref_exact, fmt: str, what: str, row_scale=True, scale
         assert err <= 2e-5, f"{what}: max abs error {err:.3e} > 2e-5"
         return {"what": what, "max_abs": float(err)}
     ref_r = round_to_format(ref_exact, fmt)
-    mag = np.abs(ref_exact)
+    diff = np.abs(got - ref_r)
+    mag_raw = np.abs(ref_exact)
+    d_raw = diff / ulp(mag_raw, fmt)
+    mag = mag_raw
     if row_scale and ref_exact.ndim == 2:
-        rs = np.max(mag, axis=1) if scale_rows is None else np.maximum(
-            np.max(mag, axis=1), np.asarray(scale_rows, dtype=np.float64))
-        mag = np.maximum(mag, np.ldexp(rs, -8)[:, None])
-    d = np.abs(got - ref_r) / ulp(mag, fmt)
+        rs = np.max(mag_raw, axis=1) if scale_rows is None else np.maximum(
+            np.max(mag_raw, axis=1), np.asarray(scale_rows, dtype=np.float64))
+        mag = np.maximum(mag_raw, np.ldexp(rs, -8)[:, None])
+    d = diff / ulp(mag, fmt)
     worst = float(d.max())
     within1 = float((d <= 1.0).mean())
+    floored = int((d_raw > 2.0).sum())
+    report = {"what": what, "n": int(d.size), "worst_ulp": worst, "within1": within1,
+              "worst_ulp_raw": float(d_raw.max()), "within1_raw": float((d_raw <= 1.0).mean()),
+              "floored": floored, "floored_frac": floored / d.size}
     assert worst <= 2.0, f"{what}: worst {worst:.2f} ulp > 2"
     assert within1 >= 0.999, f"{what}: only {within1:.5f} within 1 ulp"
-    return {"what": what, "worst_ulp": worst, "within1": within1}
+    if max_floored is not None:
+        assert report["floored_frac"] <= max_floored, (
+            f"{what}: {floored} of {d.size} elements pass only through the row-scale floor "
+            f"(> {max_floored:g}): {report}")
+    return report
 
 
 def check_mean(got, mean_exact, sum_rows, what="mean"):
+    """Mean error within 1e-5 of the row's scale mean_j |s_j|; returns how
+    many rows that rule decided (more than 1e-5 off relative to |mean|
+    itself, which means nothing for a mean that cancels to ~0)."""
     got = np.asarray(got, dtype=np.float64)
     scale = np.abs(np.asarray(sum_rows, dtype=np.float64)).mean(axis=1)
     err = np.abs(got - mean_exact)
     ok = err <= 1e-5 * np.maximum(scale, np.finfo(np.float32).tiny)
     assert ok.all(), f"{what}: worst {float((err / np.maximum(scale, 1e-30)).max()):.3e} of row scale"
+    decided = int((err > 1e-5 * np.abs(mean_exact)).sum())
+    return {"what": what, "n": int(err.size), "row_scale_decided": decided,
+            "row_scale_decided_frac": decided / max(err.size, 1)}
 
 
 def check_rel(got, ref, tol, what):
