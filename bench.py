@@ -83,28 +83,83 @@ def softmax_bytes(w) -> int:
 
 
 # ---------------------------------------------------------------- clocks
+_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown"}
+
+
 class ClockSampler:
-    """Polls nvidia-smi in the background; keeps timestamped samples."""
+    """Samples the GPU's SM clock, power and clock-event reasons in a
+    background thread while the workload runs.
+
+    Reads NVML directly through ctypes (libnvidia-ml ships with the driver;
+    only read-only queries are made) every ``period_s`` (2 ms), so even a
+    timed region of a few milliseconds gets samples; falls back to
+    ``nvidia-smi -lms 10`` when NVML cannot be loaded."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int, period_ms: int = 100):
-        self.samples = []
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.samples = []       # (time, sm_mhz, sm_max_mhz, power_w, [reasons])
         self.proc = None
-        ids = []
+        self.source = None
+        self._stop = threading.Event()
+        uuid = None
         try:
-            props = torch.cuda.get_device_properties(device_index)
-            uuid = getattr(props, "uuid", None)
-            if uuid:
-                ids.append("GPU-" + str(uuid))
+            u = getattr(torch.cuda.get_device_properties(device_index), "uuid", None)
+            uuid = ("GPU-" + str(u)) if u else None
         except Exception:
             pass
-        ids.append(None)
-        for gid in ids:
+        if self._nvml_open(uuid):
+            self.source = f"nvml every {period_s * 1e3:.0f} ms"
+            self.thread = threading.Thread(target=self._poll_nvml, args=(period_s,), daemon=True)
+            self.thread.start()
+        else:
+            self._smi_open(uuid)
+
+    # -- NVML
+    def _nvml_open(self, uuid) -> bool:
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return False
+            h = ctypes.c_void_p()
+            if uuid is not None:
+                if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+                    return False
+            elif lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                return False
+            self._nvml, self._h, self._ct = lib, h, ctypes
+            mx = ctypes.c_uint(0)
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))      # 1 = NVML_CLOCK_SM
+            self._max = float(mx.value) or None
+            self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            return True
+        except (OSError, AttributeError):
+            return False
+
+    def _poll_nvml(self, period_s):
+        ct, lib, h = self._ct, self._nvml, self._h
+        clk, pw, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        while not self._stop.is_set():
+            t = time.time()
+            ok = lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0
+            p = float(pw.value) / 1000.0 if lib.nvmlDeviceGetPowerUsage(h, ct.byref(pw)) == 0 \
+                else None
+            r = int(rs.value) if self._reasons_fn(h, ct.byref(rs)) == 0 else 0
+            if ok:
+                self.samples.append((t, float(clk.value), self._max, p,
+                                     [n for b, n in _REASONS.items() if r & b]))
+            self._stop.wait(period_s)
+
+    # -- nvidia-smi fallback
+    def _smi_open(self, uuid):
+        for gid in ([uuid] if uuid else []) + [None]:
             cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                   "-lms", str(period_ms)]
+                   "-lms", "10"]
             if gid:
                 cmd += ["-i", gid]
             try:
@@ -115,18 +170,29 @@ class ClockSampler:
             time.sleep(0.3)
             if p.poll() is None:
                 self.proc = p
+                self.source = "nvidia-smi -lms 10"
                 break
         if self.proc is not None:
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread = threading.Thread(target=self._read_smi, daemon=True)
             self.thread.start()
 
-    def _read(self):
+    def _read_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
         for line in self.proc.stdout:
-            parts = [s.strip() for s in line.split(",")]
-            if len(parts) >= 9:
-                self.samples.append((time.time(), parts))
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9 and num(parts[1]) is not None:
+                self.samples.append((time.time(), num(parts[1]), num(parts[2]), num(parts[3]),
+                                     [n for n, v in zip(names, parts[5:9])
+                                      if v.lower() == "active"]))
 
     def stop(self):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -134,23 +200,20 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, t0: float, t1: float):
-        win = [p for t, p in self.samples if t0 <= t <= t1]
+    def summary(self, t0: float, t1: float, window: str):
+        win = [x for x in self.samples if t0 <= x[0] <= t1]
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": len(win),
+               "window": window, "source": self.source}
         if not win:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        def num(s):
-            try:
-                return float(s)
-            except ValueError:
-                return None
-        sm = [num(p[1]) for p in win if num(p[1]) is not None]
-        smax = [num(p[2]) for p in win if num(p[2]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for p in win for n, v in zip(names, p[5:9]) if v.lower() == "active"})
-        power = [num(p[3]) for p in win if num(p[3]) is not None]
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
-                "samples": len(win), "power_w_max": max(power) if power else None}
+            return out
+        sm = [x[1] for x in win]
+        smax = [x[2] for x in win if x[2] is not None]
+        power = [x[3] for x in win if x[3] is not None]
+        out.update({"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
+                    "sm_max_mhz": max(smax) if smax else None,
+                    "reasons": sorted({r for x in win for r in x[4]}),
+                    "power_w_max": max(power) if power else None})
+        return out
 
 
 # ---------------------------------------------------------------- helpers
@@ -392,7 +455,7 @@ def run_reference(args, w, rank):
         return
     smx = is_softmax(w)
     inp = W.make_softmax_inputs(w, seed=0) if smx else W.make_inputs(w, seed=0)
-    budget = 150.0
+    budget = 60.0   # seconds of oracle work over all steps of the arm
     probe = min(1024, w.rows)
     t0 = time.perf_counter()
     oracle_any_step(w, inp, probe)
@@ -408,11 +471,16 @@ def run_reference(args, w, rank):
     value = rows * args.steps / el
     what = "softmax" if smx else "fwd+bwd"
     sample = f"first {rows} of {w.rows} rows per step, fp64 numpy oracle {what}, 1 thread"
+    ms_step = 1000.0 * el / args.steps
     line = {
         "impl": "reference", "metric": SOFTMAX_METRIC if smx else METRIC, "value": value,
         "unit": "rows/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1000.0 * el / args.steps * (w.rows / rows), "higher_is_better": True,
+        # measured: one step is the oracle over the sampled rows
+        "ms_per_step": ms_step, "rows_per_step": rows,
+        # what a step over every row of the workload would take at that rate
+        "ms_per_step_full_rows_extrapolated": ms_step * (w.rows / rows),
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, args.gpus),
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
@@ -436,12 +504,24 @@ def config_of(w, n):
             "parallelism": "replicas" if n > 1 else "single-gpu"}
 
 
-def run_ours(args, w, rank, world, local_rank):
-    import normalization_fwd_gb300 as nf
-    nf.load_library()
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    inp_host = W.make_inputs(w, seed=0)
+def clock_record(sampler, t_warm0, t_host0, t_host1):
+    """The clock samples of the timed region; when it is too short for a few
+    samples (a few ms at --steps 20), those of the warm-up plus the timed
+    region, which run the same kernels back to back. Both are kept."""
+    if sampler is None:
+        return None
+    time.sleep(0.01)   # let the sampler thread append the samples it is taking
+    timed = sampler.summary(t_host0, t_host1, "timed")
+    rec = timed if timed["samples"] >= 3 else sampler.summary(t_warm0, t_host1, "warmup+timed")
+    rec = dict(rec)
+    rec["timed_region"] = timed
+    return rec
+
+
+def time_fwd_bwd(nf, w, inp_host, device, args, world, sampler):
+    """Warm up, then time exactly K fused steps (ln_fwd + ln_bwd) between
+    barriers with CUDA events on the launching stream; per-kernel means from
+    events around each call."""
     step = Step(nf, w, inp_host, device)
     stream = torch.cuda.current_stream(device)
 
@@ -449,6 +529,8 @@ def run_ours(args, w, rank, world, local_rank):
         if world > 1:
             torch.distributed.barrier()
 
+    torch.cuda.synchronize(device)
+    t_warm0 = time.time()
     for _ in range(args.warmup):
         step.fwd(stream)
         step.bwd(stream)
@@ -458,9 +540,6 @@ def run_ours(args, w, rank, world, local_rank):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local_rank) if (rank == 0 and not args.no_clocks) else None
-    if sampler is not None:
-        time.sleep(0.3)
     barrier()
     torch.cuda.synchronize(device)
     t_host0 = time.time()
@@ -476,28 +555,21 @@ def run_ours(args, w, rank, world, local_rank):
     t_host1 = time.time()
     barrier()
     elapsed = max_over_ranks(start.elapsed_time(end), world, device)
-    clocks = None
-    if sampler is not None:
-        time.sleep(0.25)
-        sampler.stop()
-        clocks = sampler.summary(t_host0, t_host1)
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    del step
+    torch.cuda.empty_cache()
+    return {"ms_step": elapsed / K, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "clocks": clock_record(sampler, t_warm0, t_host0, t_host1)}
 
-    # end to end through the same calls, inputs from pinned host memory and
-    # every output read back, each step
-    e2e = None
-    if not args.no_e2e:
-        del step
-        torch.cuda.empty_cache()
-        e2e = run_e2e(nf, w, inp_host, device, min(args.e2e_steps, max(K, 1)))
 
-    if rank != 0:
-        return
+def kernel_report(w, t):
+    """Per-kernel algorithmic GB/s against the measured copy peak and the
+    nominal 8 TB/s, and the roofline of the dominant kernel."""
     peak, peak_kind = measured_peak()
     fb, bb = fwd_bytes(w), bwd_bytes(w)
     kernels = {}
-    for name, ms, by in (("ln_fwd", fwd_ms, fb), ("ln_bwd", bwd_ms, bb)):
+    for name, ms, by in (("ln_fwd", t["fwd_ms"], fb), ("ln_bwd", t["bwd_ms"], bb)):
         gbs = by / (ms * 1e-3) / 1e9
         kernels[name] = {"us": ms * 1e3, "algorithmic_bytes": by, "GBps": gbs,
                          f"frac_of_{peak_kind}": gbs / peak, "frac_of_8TBps": gbs / NOMINAL_HBM_GBS,
@@ -507,19 +579,66 @@ def run_ours(args, w, rank, world, local_rank):
     roofline = {"bound": "hbm", "kernel": dom, "achieved": d["GBps"], "peak": peak,
                 "unit": "GB/s", "frac": d["GBps"] / peak, "peak_kind": peak_kind,
                 "traffic": d["traffic"]}
+    return kernels, roofline, (fb + bb) / (t["ms_step"] * 1e-3) / 1e9
+
+
+# The second shape the HBM target is stated at: timed in the same run as the
+# default workload and reported under "workloads" on the same line.
+SECOND_GATE_WORKLOAD = W.BENCH_RMS_BF16_16384x8192
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import normalization_fwd_gb300 as nf
+    nf.load_library()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    inp_host = W.make_inputs(w, seed=0)
+    sampler = ClockSampler(local_rank) if (rank == 0 and not args.no_clocks) else None
+    if sampler is not None:
+        time.sleep(0.3)
+    t = time_fwd_bwd(nf, w, inp_host, device, args, world, sampler)
+
+    # the second gate shape, same steps and warm-up (default workload only)
+    extra = {}
+    second = (not args.no_second and args.rows is None
+              and w.name == W.BENCH_LN_BF16_576000x384.name)
+    if second:
+        w2 = SECOND_GATE_WORKLOAD
+        t2 = time_fwd_bwd(nf, w2, W.make_inputs(w2, seed=0), device, args, world, sampler)
+        k2, r2, g2 = kernel_report(w2, t2)
+        extra[w2.name] = {
+            "value": replica_throughput(w2.rows, world, t2["ms_step"]), "unit": "rows/s",
+            "ms_per_step": t2["ms_step"], "config": config_of(w2, world), "roofline": r2,
+            "kernels": k2, "step_GBps": g2, "gpu_launches": 3 * args.steps,
+            "clocks": t2["clocks"]}
+    if sampler is not None:
+        time.sleep(0.05)
+        sampler.stop()
+
+    # end to end through the same calls, inputs from pinned host memory and
+    # every output read back, each step
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(nf, w, inp_host, device, min(args.e2e_steps, max(args.steps, 1)))
+
+    if rank != 0:
+        return
+    kernels, roofline, step_gbs = kernel_report(w, t)
     cpu = cpu_all = None
     if not args.no_cpu_baseline and world == 1:
         cpu, cpu_all = cpu_baselines(w, inp_host, "fwd+bwd")
-    ms_step = elapsed / K
+    K = args.steps
     line = {
-        "metric": METRIC, "value": replica_throughput(w.rows, world, ms_step), "unit": "rows/s",
-        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": config_of(w, world), "roofline": roofline,
-        "kernels": kernels, "step_GBps": (fb + bb) / (ms_step * 1e-3) / 1e9,
+        "metric": METRIC, "value": replica_throughput(w.rows, world, t["ms_step"]),
+        "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": t["ms_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config_of(w, world),
+        "roofline": roofline, "kernels": kernels, "step_GBps": step_gbs,
         "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all, "e2e": e2e,
-        "gpu_launches": 3 * K, "clocks": clocks, "impl": "ours",
+        "gpu_launches": 3 * K, "clocks": t["clocks"], "impl": "ours",
     }
+    if extra:
+        line["workloads"] = extra
     print(json.dumps(line), flush=True)
 
 
@@ -537,15 +656,17 @@ def run_softmax(args, w, rank, world, local_rank):
         if world > 1:
             torch.distributed.barrier()
 
+    sampler = ClockSampler(local_rank) if (rank == 0 and not args.no_clocks) else None
+    if sampler is not None:
+        time.sleep(0.3)
+    torch.cuda.synchronize(device)
+    t_warm0 = time.time()
     for _ in range(args.warmup):
         step.run(stream)
     torch.cuda.synchronize(device)
     K = args.steps
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local_rank) if (rank == 0 and not args.no_clocks) else None
-    if sampler is not None:
-        time.sleep(0.3)
     barrier()
     torch.cuda.synchronize(device)
     t_host0 = time.time()
@@ -557,11 +678,9 @@ def run_softmax(args, w, rank, world, local_rank):
     t_host1 = time.time()
     barrier()
     elapsed = max_over_ranks(start.elapsed_time(end), world, device)
-    clocks = None
+    clocks = clock_record(sampler, t_warm0, t_host0, t_host1)
     if sampler is not None:
-        time.sleep(0.25)
         sampler.stop()
-        clocks = sampler.summary(t_host0, t_host1)
     e2e = None
     if not args.no_e2e:
         del step
@@ -662,6 +781,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-second", action="store_true",
+                    help="time only the chosen workload (the default run also times the "
+                         "16384 x 8192 RMSNorm step and reports it under 'workloads')")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
