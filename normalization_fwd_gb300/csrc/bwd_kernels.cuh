@@ -666,28 +666,34 @@ __global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdA
 }
 
 // The same rows with the next row's dy and x_sum (and statistics) loaded
-// into registers while this row is worked on, so each CTA keeps two rows in
-// flight, at two CTAs per SM; w = gamma (+1 for zero-centered gamma) is
-// staged once per kernel in shared memory as fp32, each thread holding only
-// its own columns ([k][pair of float2][thread] float4: no bank conflicts, no
-// barrier), which saves the per-row unpacking of gamma. Taken when the
-// accumulators and both rows fit in registers at two CTAs per SM (the
-// planner's bwd_row_pf_fits). Results are bit-identical to
-// bwd_row_cta_kernel's: the same operations in the same order.
+// into registers while this row is worked on. One CTA per SM holds two row
+// groups of 256 threads; group g of CTA b takes rows 2b + g, 2b + g + 2G, ...
+// (G CTAs), so each SM keeps four rows in flight (two groups, two rows each).
+// Each group sums its row behind a named barrier of its own threads, so the
+// groups never wait for each other inside the row loop. w = gamma (+1 for
+// zero-centered gamma) is staged once per kernel in shared memory as fp32
+// ([k][pair of float2][thread] float4: no bank conflicts), which saves the
+// per-row unpacking of gamma. At the end the two groups' column sums are
+// added (group 0's plus group 1's) through shared memory, so the CTA writes
+// one partial row: half as many partials for the finalize to read as two
+// CTAs per SM would leave. Per-row results are those of bwd_row_cta_kernel
+// (the same operations in the same order). Taken when the accumulators and
+// both rows fit in registers (the planner's bwd_row_pf_fits).
 template <typename T, int N, bool kRms, bool kBias>
-__global__ void __launch_bounds__(kBulkThreads, 2) bwd_row_pf_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs a) {
   constexpr int VEC = Vec<T>::N;
   constexpr int P = VEC / 2;
   constexpr int Q = P / 2;   // float4 per vector of w
   extern __shared__ __align__(16) float4 w_s[];   // [N][Q][kBulkThreads]
-  __shared__ float2 red[2][kConsumerWarps];
-  const int t = threadIdx.x;
+  __shared__ float2 red[kPfGroups][2][kConsumerWarps];
+  const int grp = threadIdx.x / kBulkThreads;
+  const int t = threadIdx.x % kBulkThreads;
   const int H = a.hidden;
   const int V = H / VEC;
   const T* dy = static_cast<const T*>(a.dy);
   const T* xs = static_cast<const T*>(a.x_sum);
   T* dx = static_cast<T*>(a.dx);
-  {
+  if (grp == 0) {
     const T* gamma = static_cast<const T*>(a.gamma);
 #pragma unroll
     for (int k = 0; k < N; ++k) {
@@ -707,6 +713,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_row_pf_kernel(const BwdAr
       }
     }
   }
+  __syncthreads();
   auto load_w = [&](int k, float2 (&w)[P]) {
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
@@ -714,6 +721,22 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_row_pf_kernel(const BwdAr
       w[2 * q] = make_float2(f.x, f.y);
       w[2 * q + 1] = make_float2(f.z, f.w);
     }
+  };
+  // Sum of a float2 over the group: warp butterfly, then the group's 8 warps
+  // in order through a double-buffered exchange behind the group's barrier.
+  int parity = 0;
+  auto group_row_sum = [&](float2 v) {
+    v = group_sum2<32>(v);
+    if ((t & 31) == 0) red[grp][parity][t >> 5] = v;
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(kBulkThreads) : "memory");
+    float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kConsumerWarps; ++i) {
+      s.x += red[grp][parity][i].x;
+      s.y += red[grp][parity][i].y;
+    }
+    parity ^= 1;
+    return s;
   };
   float2 acc_g[N][P], acc_b[N][P], acc_d[N][P];
   zero_acc2<T, N>(acc_g);
@@ -734,9 +757,10 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_row_pf_kernel(const BwdAr
     nr = a.rstd[row];
     if (!kRms) nm = a.mean[row];
   };
-  if ((int64_t)blockIdx.x < a.rows) load_row(blockIdx.x);
-  int parity = 0;
-  for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+  const int64_t first = (int64_t)blockIdx.x * kPfGroups + grp;
+  const int64_t stride = (int64_t)gridDim.x * kPfGroups;
+  if (first < a.rows) load_row(first);
+  for (int64_t row = first; row < a.rows; row += stride) {
     uint4 dr[N], xr[N];
 #pragma unroll
     for (int k = 0; k < N; ++k) {
@@ -744,7 +768,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_row_pf_kernel(const BwdAr
       xr[k] = nx[k];
     }
     const float rstd = nr, mean = nm;
-    if (row + gridDim.x < a.rows) load_row(row + gridDim.x);
+    if (row + stride < a.rows) load_row(row + stride);
     const int64_t off = row * (int64_t)H;
     const float2 neg_mean = splat2(-mean);
     const float2 r2 = splat2(rstd);
@@ -768,8 +792,7 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_row_pf_kernel(const BwdAr
         }
       }
     }
-    const float2 sums = cta_sum2_db<kBulkThreads>(
-        make_float2(kRms ? 0.f : sx.x + sx.y, sy.x + sy.y), red, parity);
+    const float2 sums = group_row_sum(make_float2(kRms ? 0.f : sx.x + sx.y, sy.x + sy.y));
     // dx = rstd * (g - c1 - xhat * c2) = (x - mean) * b2 + (g * rstd + a1)
     const float c2 = sums.y * a.inv_hidden;
     const float2 a1 = splat2(kRms ? 0.f : -rstd * (sums.x * a.inv_hidden));
@@ -796,17 +819,34 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_row_pf_kernel(const BwdAr
     }
   }
   allow_dependent_launch();
+  // One partial row per CTA: group 1's sums go through shared memory (the
+  // staged w is no longer needed) and group 0 adds them to its own.
   float* ws = a.ws + (int64_t)blockIdx.x * a.ws_cols;
-  auto put = [&](const float2 (&acc)[N][P], int off) {
+  auto put = [&](float2 (&acc)[N][P], int off) {
+    __syncthreads();
+    if (grp == 1) {
 #pragma unroll
-    for (int k = 0; k < N; ++k) {
-      const int v = k * kBulkThreads + t;
-      if (v < V) {
-        float4* q = reinterpret_cast<float4*>(ws + off + v * VEC);
+      for (int k = 0; k < N; ++k)
 #pragma unroll
-        for (int i = 0; i < P / 2; ++i)
-          q[i] = make_float4(acc[k][2 * i].x, acc[k][2 * i].y, acc[k][2 * i + 1].x,
-                             acc[k][2 * i + 1].y);
+        for (int q = 0; q < Q; ++q)
+          w_s[(k * Q + q) * kBulkThreads + t] =
+              make_float4(acc[k][2 * q].x, acc[k][2 * q].y, acc[k][2 * q + 1].x, acc[k][2 * q + 1].y);
+    }
+    __syncthreads();
+    if (grp == 0) {
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        const int v = k * kBulkThreads + t;
+        if (v < V) {
+          float4* dst = reinterpret_cast<float4*>(ws + off + v * VEC);
+#pragma unroll
+          for (int q = 0; q < Q; ++q) {
+            const float4 o = w_s[(k * Q + q) * kBulkThreads + t];
+            const float2 lo = add2(acc[k][2 * q], make_float2(o.x, o.y));
+            const float2 hi = add2(acc[k][2 * q + 1], make_float2(o.z, o.w));
+            dst[q] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          }
+        }
       }
     }
   };

@@ -17,6 +17,9 @@ using f16 = __half;
 constexpr int kScalarCta = 256;        // threads per CTA of the scalar kernels
 constexpr int kConsumerWarps = 8;      // warps of a pipelined CTA
 constexpr int kBulkThreads = kConsumerWarps * 32;
+// Threads of the prefetching CTA-per-row backward: two row groups of 256.
+constexpr int kPfGroups = 2;
+constexpr int kPfThreads = kPfGroups * kBulkThreads;
 
 // Elements per 16-byte vector.
 template <typename T> struct Vec;

@@ -176,13 +176,14 @@ inline cudaError_t size_grid(Plan* p, int64_t steps) {
 // LayerNorm; dbias) and the row's two inputs (8n registers) fit in 64
 // registers' worth (56 for LayerNorm, which also keeps the mean and a second
 // row sum live), so that kernel (kind 5) keeps three or more CTAs per SM
-// without spilling. Its variant with the next row prefetched (kind 6, two
-// CTAs per SM, both rows' inputs in 16n registers) holds four rows per SM in
-// flight; it is taken where it fits in 96 registers' worth and the one-row
-// kernel would hold fewer than four (measured at 16384 x 8192 bf16 RMSNorm
-// 121.6 against 127.7 us, 21845 x 6144 LayerNorm 135.5 against 159.4 us;
-// at 32768 x 4096 RMSNorm, where kind 5 runs four CTAs per SM, 138.5
-// against 128.9 us). The other aligned rows, and these too under the ring
+// without spilling. Its variant with the next row prefetched (kind 6, one
+// CTA of two 256-thread row groups per SM, both rows' inputs in 16n
+// registers) holds four rows per SM in flight; it is taken where it fits in
+// 96 registers' worth and the one-row kernel would hold fewer than four
+// (measured with two 256-thread CTAs per SM, the same four rows in flight:
+// 16384 x 8192 bf16 RMSNorm 121.6 against 127.7 us, 21845 x 6144
+// LayerNorm 135.5 against 159.4 us; at 32768 x 4096 RMSNorm, where kind 5
+// runs four CTAs per SM, 138.5 against 128.9 us). The other aligned rows, and these too under the ring
 // family, stream through the bulk-copy ring.
 inline int bwd_acc_floats(int n, int vec_elems, bool rms, bool dbias) {
   return n * vec_elems * (1 + (rms ? 0 : 1) + (dbias ? 1 : 0));
@@ -193,7 +194,7 @@ inline bool bwd_row_pf_fits(int n, int vec_elems, bool rms, bool dbias) {
 inline bool bwd_row_cta_fits(int n, int vec_elems, bool rms, bool dbias) {
   return n <= 4 && bwd_acc_floats(n, vec_elems, rms, dbias) + 8 * n <= (rms ? 64 : 56);
 }
-constexpr int kRowsInFlightPf = 4;   // kind 6: two CTAs per SM, two rows each
+constexpr int kRowsInFlightPf = 4;   // kind 6: two row groups per SM, two rows each
 
 template <typename T>
 cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bool dbias,
@@ -217,7 +218,7 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
       p->kind = pf ? 6 : 5;
       p->group = kBulkThreads;
       p->n = n;
-      p->block = kBulkThreads;
+      p->block = pf ? kPfThreads : kBulkThreads;
       // kind 6 stages w as fp32: n vectors of VEC floats per thread
       p->smem = pf ? (size_t)n * Vec<T>::N * sizeof(float) * kBulkThreads : 0;
       p->fn = Tables<T>::bwd_bulk(p->kind, kBulkThreads, n, rms, dbias, false);
