@@ -41,7 +41,13 @@ import workloads as W  # noqa: E402
 METRIC = "fwd+bwd rows/s and achieved HBM GB/s vs ~8 TB/s peak at (576000×384) bf16"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-BENCH_WORKLOADS = {w.name: w for w in (W.BENCH_LN_BF16_576000x384, W.BENCH_RMS_BF16_16384x8192)}
+BENCH_WORKLOADS = {w.name: w for w in (W.BENCH_LN_BF16_576000x384, W.BENCH_RMS_BF16_16384x8192,
+                                        W.BENCH_LN_FP8_DBIAS_BF16_576000x384)}
+# The normalize-from-partials step is measured on its own workload (its own
+# metric line, like the softmax).
+PARTIALS_METRIC = ("normalize-from-partials rows/s and achieved HBM GB/s (one read of x and the "
+                   "partials, one write of y and the statistics)")
+PARTIALS_WORKLOADS = {W.PARTIALS_BF16_576000x384.name: W.PARTIALS_BF16_576000x384}
 # The row softmax is measured on its own workloads (its own metric line).
 SOFTMAX_METRIC = "softmax rows/s and achieved HBM GB/s (one read of x, one write of y)"
 SOFTMAX_WORKLOADS = {w.name: w for w in (W.SMX_BF16_576000x384, W.SMX_BF16_16384x8192)}
@@ -58,14 +64,16 @@ def elem_bytes(w) -> int:
 
 def fwd_bytes(w) -> int:
     """Minimal HBM bytes of one ln_fwd: each input read once, each output
-    written once (x, residual, bias, gamma, beta in; sum, y, stats, amax out)."""
+    written once (x, residual, bias, gamma, beta in; sum, y, stats, amax out;
+    with an FP8 copy of y, its R * H bytes and the 4-byte scale)."""
     R, H, e = w.rows, w.hidden, elem_bytes(w)
     has_res = w.residual_std is not None
     store_sum = has_res or w.bias_std is not None
     nstats = 2 if w.mode == W.LAYERNORM else 1
     nparams = 1 + (w.mode == W.LAYERNORM and w.beta_std is not None) + (w.bias_std is not None)
+    fp8 = (R * H + 4) if w.fp8_out else 0
     return (R * H * e * (1 + has_res) + R * H * e * (1 + store_sum) + R * 4 * nstats
-            + H * e * nparams + (4 if w.amax else 0))
+            + H * e * nparams + (4 if w.amax else 0) + fp8)
 
 
 def bwd_bytes(w) -> int:
@@ -73,8 +81,19 @@ def bwd_bytes(w) -> int:
     dgamma (and dbeta) out. The workspace partials are not counted."""
     R, H, e = w.rows, w.hidden, elem_bytes(w)
     nstats = 2 if w.mode == W.LAYERNORM else 1
-    ngrads = 2 if w.mode == W.LAYERNORM else 1
+    ngrads = (2 if w.mode == W.LAYERNORM else 1) + (1 if w.dbias else 0)
     return 3 * R * H * e + R * 4 * nstats + H * e + H * 4 * ngrads
+
+
+def partials_bytes(w, tile_cols) -> int:
+    """Minimal HBM bytes of one ln_fwd_from_partials: x and the two fp32
+    partials per tile read once; y, the statistics and amax written once."""
+    R, H, e = w.rows, w.hidden, elem_bytes(w)
+    T = -(-H // tile_cols)
+    nstats = 2 if w.mode == W.LAYERNORM else 1
+    nparams = 1 + (w.mode == W.LAYERNORM and w.beta_std is not None)
+    return (2 * R * H * e + R * T * 8 + R * 4 * nstats + H * e * nparams
+            + (4 if w.amax else 0))
 
 
 def softmax_bytes(w) -> int:
@@ -276,17 +295,32 @@ class Step:
         self.dx = torch.empty(R, H, dtype=dt, device=device)
         self.dgamma = torch.empty(H, **f32)
         self.dbeta = None if self.rms else torch.empty(H, **f32)
+        self.dbias = torch.empty(H, **f32) if w.dbias else None
+        # FP8 copy of y with a per-tensor scale (delayed scaling: 448 over an
+        # amax of an earlier step; a fixed value here)
+        self.y_fp8 = torch.empty(R, H, dtype=torch.uint8, device=device) if w.fp8_out else None
+        self.fp8_scale = torch.full((1,), 64.0, **f32) if w.fp8_out else None
         need = nf.ln_bwd_workspace_bytes(R, H, dt, w.mode)
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
 
     def fwd(self, stream):
         g, w = self.inp, self.w
+        if w.fp8_out:
+            self.nf.ln_fwd_ex(g["x"], g["bias"], g["residual"], g["gamma"], g["beta"], w.eps,
+                              w.mode, w.zero_centered_gamma, self.sum, self.y, self.mean,
+                              self.rstd, self.amax, self.y_fp8, self.fp8_scale, stream)
+            return
         self.nf.ln_fwd(g["x"], g["bias"], g["residual"], g["gamma"], g["beta"], w.eps, w.mode,
                        w.zero_centered_gamma, self.sum, self.y, self.mean, self.rstd, self.amax,
                        stream)
 
     def bwd(self, stream):
         g, w = self.inp, self.w
+        if w.dbias:
+            self.nf.ln_bwd_ex(g["dy"], self.sum, g["gamma"], self.mean, self.rstd, self.dx,
+                              self.dgamma, self.dbeta, self.dbias, stream, mode=w.mode,
+                              zero_centered_gamma=w.zero_centered_gamma, workspace=self.ws)
+            return
         self.nf.ln_bwd(g["dy"], self.sum, g["gamma"], self.mean, self.rstd, self.dx, self.dgamma,
                        self.dbeta, stream, mode=w.mode, zero_centered_gamma=w.zero_centered_gamma,
                        workspace=self.ws)
@@ -302,7 +336,60 @@ class Step:
     def d2h_tensors(self):
         out = [("sum", self.sum), ("y", self.y), ("mean", self.mean), ("rstd", self.rstd),
                ("amax", self.amax), ("dx", self.dx), ("dgamma", self.dgamma),
-               ("dbeta", self.dbeta)]
+               ("dbeta", self.dbeta), ("dbias", self.dbias), ("y_fp8", self.y_fp8)]
+        return [(k, t) for k, t in out if t is not None]
+
+
+def producer_partials(x, tile_cols):
+    """Stand-in for the producer of the partials (a GEMM epilogue, outside
+    this library): per row and column tile, the fp32 sum and sum of squares
+    of the stored row, taken with torch on the device as input data."""
+    R, H = x.shape
+    T = -(-H // tile_cols)
+    xf = torch.nn.functional.pad(x.float(), (0, T * tile_cols - H)).view(R, T, tile_cols)
+    return xf.sum(-1).contiguous(), (xf * xf).sum(-1).contiguous()
+
+
+def make_partials_inputs(w, seed=0):
+    """The workload's x, gamma, beta and the producer stand-in's partials
+    (computed on the host in 65536-row blocks)."""
+    inp = W.make_inputs(w, seed=seed)
+    parts = [producer_partials(inp["x"][i:i + 65536], W.PARTIALS_TILE_COLS)
+             for i in range(0, w.rows, 65536)]
+    inp["psum"] = torch.cat([p[0] for p in parts])
+    inp["psq"] = torch.cat([p[1] for p in parts])
+    return inp
+
+
+class PartialsStep:
+    """Device buffers and the C-ABI call of one normalize-from-partials step."""
+
+    def __init__(self, nf, w, inp_host, device):
+        self.nf, self.w = nf, w
+        self.tile = W.PARTIALS_TILE_COLS
+        self.x = inp_host["x"].to(device)
+        self.gamma = inp_host["gamma"].to(device)
+        self.beta = inp_host["beta"].to(device) if inp_host["beta"] is not None else None
+        self.psum = inp_host["psum"].to(device)
+        self.psq = inp_host["psq"].to(device)
+        R = w.rows
+        f32 = dict(dtype=torch.float32, device=device)
+        self.y = torch.empty_like(self.x)
+        self.mean = None if w.mode == W.RMSNORM else torch.empty(R, **f32)
+        self.rstd = torch.empty(R, **f32)
+        self.amax = torch.empty(1, **f32) if w.amax else None
+
+    def run(self, stream):
+        w = self.w
+        self.nf.ln_fwd_from_partials(self.x, self.psum, self.psq, self.tile, "sum_sq", self.gamma,
+                                     self.beta, w.eps, w.mode, w.zero_centered_gamma, self.y,
+                                     self.mean, self.rstd, self.amax, stream)
+
+    def h2d_tensors(self):
+        return [("x", self.x), ("psum", self.psum), ("psq", self.psq)]
+
+    def d2h_tensors(self):
+        out = [("y", self.y), ("mean", self.mean), ("rstd", self.rstd), ("amax", self.amax)]
         return [(k, t) for k, t in out if t is not None]
 
 
@@ -366,9 +453,24 @@ def oracle_softmax_step(w, x, rows):
     softmax_fwd(W.as_f64(x[:rows]), w.dtype)
 
 
+def oracle_partials_step(w, inp, rows):
+    """One fp64 oracle normalize-from-partials over the first `rows` rows."""
+    from oracle import norm_fwd_from_partials
+    f = W.as_f64
+    norm_fwd_from_partials(f(inp["x"][:rows]), f(inp["psum"][:rows]), f(inp["psq"][:rows]),
+                           W.PARTIALS_TILE_COLS, "sum_sq", f(inp["gamma"]), f(inp["beta"]), w.eps,
+                           w.mode, w.zero_centered_gamma, w.dtype)
+
+
+def is_partials(w) -> bool:
+    return w.name.split("@")[0] in PARTIALS_WORKLOADS
+
+
 def oracle_any_step(w, inp, rows):
     if is_softmax(w):
         oracle_softmax_step(w, inp, rows)
+    elif is_partials(w):
+        oracle_partials_step(w, inp, rows)
     else:
         oracle_step(w, inp, rows)
 
@@ -395,7 +497,12 @@ def _oracle_worker(args):
     import time as _t
     smx = isinstance(w, W.SoftmaxWorkload)
     sample = w.with_(rows=rows)
-    inp = W.make_softmax_inputs(sample, seed=seed) if smx else W.make_inputs(sample, seed=seed)
+    if smx:
+        inp = W.make_softmax_inputs(sample, seed=seed)
+    elif is_partials(w):
+        inp = make_partials_inputs(sample, seed=seed)
+    else:
+        inp = W.make_inputs(sample, seed=seed)
     barrier.wait()
     t0 = _t.perf_counter()
     oracle_any_step(sample, inp, rows)
@@ -454,7 +561,12 @@ def run_reference(args, w, rank):
     if rank != 0:
         return
     smx = is_softmax(w)
-    inp = W.make_softmax_inputs(w, seed=0) if smx else W.make_inputs(w, seed=0)
+    if smx:
+        inp = W.make_softmax_inputs(w, seed=0)
+    elif is_partials(w):
+        inp = make_partials_inputs(w, seed=0)
+    else:
+        inp = W.make_inputs(w, seed=0)
     budget = 60.0   # seconds of oracle work over all steps of the arm
     probe = min(1024, w.rows)
     t0 = time.perf_counter()
@@ -469,11 +581,11 @@ def run_reference(args, w, rank):
         oracle_any_step(w, inp, rows)
     el = time.perf_counter() - t0
     value = rows * args.steps / el
-    what = "softmax" if smx else "fwd+bwd"
+    what = "softmax" if smx else ("normalize from partials" if is_partials(w) else "fwd+bwd")
     sample = f"first {rows} of {w.rows} rows per step, fp64 numpy oracle {what}, 1 thread"
     ms_step = 1000.0 * el / args.steps
     line = {
-        "impl": "reference", "metric": SOFTMAX_METRIC if smx else METRIC, "value": value,
+        "impl": "reference", "metric": metric_of(w), "value": value,
         "unit": "rows/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         # measured: one step is the oracle over the sampled rows
@@ -491,17 +603,33 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+def metric_of(w):
+    if is_softmax(w):
+        return SOFTMAX_METRIC
+    if is_partials(w):
+        return PARTIALS_METRIC
+    return METRIC
+
+
 def config_of(w, n):
     if is_softmax(w):
         return {"workload": w.name, "rows": w.rows, "hidden": w.hidden, "io_dtype": w.dtype,
                 "x_std": w.x_std, "mask_frac": w.mask_frac,
                 "l2": "no flush: x and y are each larger than the 129 MB L2",
                 "parallelism": "replicas" if n > 1 else "single-gpu"}
-    return {"workload": w.name, "rows": w.rows, "hidden": w.hidden, "mode": w.mode,
-            "io_dtype": w.dtype, "stats_dtype": "f32", "bias": w.bias_std is not None,
-            "residual": w.residual_std is not None, "amax": w.amax, "eps": w.eps,
-            "l2": "no flush: every [rows, hidden] input is larger than the 129 MB L2",
-            "parallelism": "replicas" if n > 1 else "single-gpu"}
+    c = {"workload": w.name, "rows": w.rows, "hidden": w.hidden, "mode": w.mode,
+         "io_dtype": w.dtype, "stats_dtype": "f32", "bias": w.bias_std is not None,
+         "residual": w.residual_std is not None, "amax": w.amax, "eps": w.eps,
+         "l2": "no flush: every [rows, hidden] input is larger than the 129 MB L2",
+         "parallelism": "replicas" if n > 1 else "single-gpu"}
+    if w.fp8_out:
+        c["fp8_out"] = "E4M3 copy of y, per-tensor scale"
+    if w.dbias:
+        c["dbias"] = True
+    if is_partials(w):
+        c["partials"] = {"kind": "sum_sq", "tile_cols": W.PARTIALS_TILE_COLS,
+                         "producer": "fp32 tile sums of the stored row, precomputed (stand-in)"}
+    return c
 
 
 def clock_record(sampler, t_warm0, t_host0, t_host1):
@@ -643,13 +771,17 @@ def run_ours(args, w, rank, world, local_rank):
 
 
 def run_softmax(args, w, rank, world, local_rank):
-    """Time ln_softmax_fwd alone on a softmax workload (its own JSON line)."""
+    """Time ln_softmax_fwd alone on a softmax workload, or
+    ln_fwd_from_partials alone on a partials workload (its own JSON line)."""
     import normalization_fwd_gb300 as nf
     nf.load_library()
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
-    x_host = W.make_softmax_inputs(w, seed=0)
-    step = SoftmaxStep(nf, w, x_host, device)
+    part = is_partials(w)
+    x_host = make_partials_inputs(w, seed=0) if part else W.make_softmax_inputs(w, seed=0)
+    step_cls = PartialsStep if part else SoftmaxStep
+    kname = "ln_fwd_from_partials" if part else "ln_softmax_fwd"
+    step = step_cls(nf, w, x_host, device)
     stream = torch.cuda.current_stream(device)
 
     def barrier():
@@ -686,25 +818,24 @@ def run_softmax(args, w, rank, world, local_rank):
         del step
         torch.cuda.empty_cache()
         e2e = run_e2e(nf, w, x_host, device, min(args.e2e_steps, max(K, 1)),
-                      make_step=SoftmaxStep)
+                      make_step=step_cls)
     if rank != 0:
         return
     peak, peak_kind = measured_peak()
     ms = elapsed / K
-    by = softmax_bytes(w)
+    by = partials_bytes(w, W.PARTIALS_TILE_COLS) if part else softmax_bytes(w)
     gbs = by / (ms * 1e-3) / 1e9
-    kernels = {"ln_softmax_fwd": {"us": ms * 1e3, "algorithmic_bytes": by, "GBps": gbs,
-                                  f"frac_of_{peak_kind}": gbs / peak,
-                                  "frac_of_8TBps": gbs / NOMINAL_HBM_GBS,
-                                  "traffic": ncu_traffic(w.name, "ln_softmax_fwd")}}
-    roofline = {"bound": "hbm", "kernel": "ln_softmax_fwd", "achieved": gbs, "peak": peak,
+    kernels = {kname: {"us": ms * 1e3, "algorithmic_bytes": by, "GBps": gbs,
+                       f"frac_of_{peak_kind}": gbs / peak, "frac_of_8TBps": gbs / NOMINAL_HBM_GBS,
+                       "traffic": ncu_traffic(w.name, kname)}}
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": gbs, "peak": peak,
                 "unit": "GB/s", "frac": gbs / peak, "peak_kind": peak_kind,
-                "traffic": kernels["ln_softmax_fwd"]["traffic"]}
+                "traffic": kernels[kname]["traffic"]}
     cpu = cpu_all = None
     if not args.no_cpu_baseline and world == 1:
-        cpu, cpu_all = cpu_baselines(w, x_host, "softmax")
+        cpu, cpu_all = cpu_baselines(w, x_host, "normalize from partials" if part else "softmax")
     line = {
-        "metric": SOFTMAX_METRIC, "value": replica_throughput(w.rows, world, ms),
+        "metric": metric_of(w), "value": replica_throughput(w.rows, world, ms),
         "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic", "config": config_of(w, world),
@@ -761,10 +892,37 @@ def run_e2e(nf, w, inp_host, device, steps, make_step=Step):
     z.record(down)
     torch.cuda.synchronize(device)
     ms = a.elapsed_time(z) / steps
+    bi = sum(nbytes(t) for _, t in h2d[0])
+    bo = sum(nbytes(t) for _, t in d2h[0])
+    # Which side limits: each direction's bytes over the step time, against
+    # the copy engines' own rate measured here on one buffer set.
+    link = host_link_rates(h2d[0], d2h[0], host_in, host_out[0], device)
     return {"value": w.rows / (ms * 1e-3), "unit": "rows/s", "ms_per_step": ms,
-            "steps": steps, "h2d_bytes_per_step": sum(nbytes(t) for _, t in h2d[0]),
-            "d2h_bytes_per_step": sum(nbytes(t) for _, t in d2h[0]),
+            "steps": steps, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "h2d_GBps": bi / (ms * 1e-3) / 1e9, "d2h_GBps": bo / (ms * 1e-3) / 1e9,
+            "host_link": link,
             "pipeline": "2 buffer sets; upload, compute and download on 3 streams"}
+
+
+def host_link_rates(h2d, d2h, host_in, host_out, device):
+    """GB/s of the step's uploads alone and of its downloads alone (pinned
+    host memory, one stream each, CUDA events), so the e2e record shows
+    whether the step is bound by the host link or by the device."""
+    s = torch.cuda.Stream(device)
+    out = {}
+    for name, pairs in (("h2d_GBps_alone", [(t, host_in[k]) for k, t in h2d]),
+                        ("d2h_GBps_alone", [(host_out[k], t) for k, t in d2h])):
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            a.record(s)
+            for dst, src in pairs:
+                dst.copy_(src, non_blocking=True)
+            z.record(s)
+        torch.cuda.synchronize(device)
+        by = sum(nbytes(d) for d, _ in pairs)
+        out[name] = by / (a.elapsed_time(z) * 1e-3) / 1e9
+    return out
 
 
 def main():
@@ -773,7 +931,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS) + sorted(SOFTMAX_WORKLOADS),
+    ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS) + sorted(SOFTMAX_WORKLOADS)
+                    + sorted(PARTIALS_WORKLOADS),
                     default=W.BENCH_LN_BF16_576000x384.name)
     ap.add_argument("--rows", type=int, default=None,
                     help="override the workload's row count (smaller profiling captures)")
@@ -787,7 +946,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = BENCH_WORKLOADS.get(args.workload) or SOFTMAX_WORKLOADS[args.workload]
+    w = (BENCH_WORKLOADS.get(args.workload) or SOFTMAX_WORKLOADS.get(args.workload)
+         or PARTIALS_WORKLOADS[args.workload])
     if args.rows is not None:
         w = w.with_(rows=args.rows, name=f"{w.name}@rows={args.rows}")
 
@@ -804,7 +964,7 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
     try:
-        if is_softmax(w):
+        if is_softmax(w) or is_partials(w):
             run_softmax(args, w, rank, world, local_rank)
         else:
             run_ours(args, w, rank, world, local_rank)

@@ -34,6 +34,25 @@ def test_backward_bytes():
         assert bench.bwd_bytes(w) == 3 * 8192 * h * 2 + 2 * 8192 * 4 + h * 2 + 2 * h * 4
 
 
+def test_fp8_dbias_step_bytes():
+    R, H = 576000, 384
+    w = W.BENCH_LN_FP8_DBIAS_BF16_576000x384
+    # the forward also writes one E4M3 byte per element and reads the scale
+    assert bench.fwd_bytes(w) == 1_774_082_308 + R * H + 4
+    # the backward also writes dbias (fp32)
+    assert bench.bwd_bytes(w) == 1_331_715_840 + H * 4
+
+
+def test_partials_bytes():
+    R, H = 576000, 384
+    w = W.PARTIALS_BF16_576000x384
+    # x in, y out (bf16); three 128-column tiles of (sum, sum of squares)
+    # fp32 in; mean, rstd out; gamma, beta in; amax out
+    want = 2 * R * H * 2 + R * 3 * 2 * 4 + 2 * R * 4 + 2 * H * 2 + 4
+    assert bench.partials_bytes(w, 128) == want
+    assert bench.partials_bytes(w, 100) == want + R * 2 * 4   # four tiles
+
+
 def test_softmax_bytes():
     assert bench.softmax_bytes(W.SMX_BF16_576000x384) == 576000 * 384 * 2 * 2
     assert bench.softmax_bytes(W.SMX_BF16_16384x8192) == 16384 * 8192 * 2 * 2

@@ -52,6 +52,8 @@ class Workload:
     forward: bool = True
     outlier_frac: float = 0.0
     outlier_scale: float = 1.0
+    fp8_out: bool = False                # the step also writes an E4M3 copy of y
+    dbias: bool = False                  # the step's backward also writes dbias
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -100,11 +102,21 @@ BENCH_LN_BF16_576000x384 = Workload(
     gamma_std=0.02, beta_std=0.02, amax=True)
 BENCH_RMS_BF16_16384x8192 = RMS_BF16_16384x8192.with_(
     name="rms_fwd_bwd_bf16_16384x8192", amax=True)
+# The same step with the options of the next rows of the scope table: an
+# FP8 (E4M3) copy of y scaled from a per-tensor scale, and dbias.
+BENCH_LN_FP8_DBIAS_BF16_576000x384 = BENCH_LN_BF16_576000x384.with_(
+    name="ln_fwd_bwd_fp8_dbias_bf16_576000x384", fp8_out=True, dbias=True)
+# The normalize step fed by per-column-tile partial statistics, on the
+# 576000 x 384 rows with 128-column tiles (three tiles per row).
+PARTIALS_BF16_576000x384 = BENCH_LN_BF16_576000x384.with_(
+    name="partials_bf16_576000x384", residual_std=None, bias_std=None, backward=False)
+PARTIALS_TILE_COLS = 128
 
 WORKLOADS = {w.name: w for w in (
     LN_F32_4096x384, BWD_BF16_576000x384_LN, BWD_BF16_576000x384_RMS,
     FWD_AMAX_BF16_32768x768, *UNET_F16.values(), RMS_BF16_16384x8192,
-    BENCH_LN_BF16_576000x384, BENCH_RMS_BF16_16384x8192)}
+    BENCH_LN_BF16_576000x384, BENCH_RMS_BF16_16384x8192, BENCH_LN_FP8_DBIAS_BF16_576000x384,
+    PARTIALS_BF16_576000x384)}
 
 
 def to_dtype(a64: np.ndarray, dtype: str) -> torch.Tensor:
