@@ -50,35 +50,42 @@ struct PartialsArgs {
   int zero_centered;
 };
 
-// This thread's share of the row statistics: its tiles t = t0, t0 + step,
-// ... combined in increasing t. Returns (sum, sum of squares or M2 term)
-// for the first pass; `mean` is used by the M2 form's second pass only.
-__device__ __forceinline__ float partial_sum(const PartialsArgs& a, int64_t row, int t0,
-                                             int step) {
+// This thread's share of the first pass over its tiles t = t0, t0 + step,
+// ... in increasing t: x = the sum of psum; y = the sum of psq for kind 0.
+// For kind 1 the psq of those tiles are prefetched into L1 for the second
+// pass, so both passes' loads leave together and the second pass, which
+// needs the row mean, finds them on chip.
+__device__ __forceinline__ float2 partial_first(const PartialsArgs& a, int64_t row, int t0,
+                                                int step) {
   const float* ps = a.psum + row * (int64_t)a.n_tiles;
-  float s = 0.f;
-  for (int t = t0; t < a.n_tiles; t += step) s += ps[t];
-  return s;
+  const float* pq = a.psq + row * (int64_t)a.n_tiles;
+  float s = 0.f, q = 0.f;
+  for (int t = t0; t < a.n_tiles; t += step) {
+    s += ps[t];
+    if (a.kind == 0) {
+      q += pq[t];
+    } else {
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(pq + t));
+    }
+  }
+  return make_float2(s, q);
 }
 
-// The second quantity: kind 0 sums psq; kind 1 LayerNorm sums
-// psq_t + (psum_t - n_t mean)^2 / n_t; kind 1 RMSNorm psq_t + psum_t^2 / n_t.
+// Kind 1's second pass over the same tiles: psq_t + (psum_t - n_t mean)^2
+// / n_t for LayerNorm (the row mean from the first pass), psq_t +
+// psum_t^2 / n_t for RMSNorm.
 __device__ __forceinline__ float partial_second(const PartialsArgs& a, int64_t row, int t0,
                                                 int step, float mean) {
   const float* ps = a.psum + row * (int64_t)a.n_tiles;
   const float* pq = a.psq + row * (int64_t)a.n_tiles;
   float q = 0.f;
   for (int t = t0; t < a.n_tiles; t += step) {
-    if (a.kind == 0) {
-      q += pq[t];
-    } else {
-      const bool last = t == a.n_tiles - 1;
-      const float n = last ? (float)(a.hidden - (a.n_tiles - 1) * a.tile_cols)
-                           : (float)a.tile_cols;
-      const float inv_n = last ? a.inv_last : a.inv_tile;
-      const float d = a.rms ? ps[t] : fmaf(-n, mean, ps[t]);
-      q += fmaf(d * d, inv_n, pq[t]);
-    }
+    const bool last = t == a.n_tiles - 1;
+    const float n = last ? (float)(a.hidden - (a.n_tiles - 1) * a.tile_cols)
+                         : (float)a.tile_cols;
+    const float inv_n = last ? a.inv_last : a.inv_tile;
+    const float d = a.rms ? ps[t] : fmaf(-n, mean, ps[t]);
+    q += fmaf(d * d, inv_n, pq[t]);
   }
   return q;
 }
@@ -151,10 +158,14 @@ __global__ void __launch_bounds__(kBulkThreads) fwdp_tile_kernel(const PartialsA
   }
   // Statistics: every lane group runs its butterflies (whole warps take
   // part in the shuffles); a group past the last row reads no partials.
-  const float S = group_sum<LANES>(row_ok ? partial_sum(a, row, l, LANES) : 0.f);
-  const float mean0 = a.rms ? 0.f : S * a.inv_hidden;
-  const float Q = group_sum<LANES>(row_ok ? partial_second(a, row, l, LANES, mean0) : 0.f);
-  const float2 st = partial_stats(a, S, Q);
+  const float2 sq = group_sum2<LANES>(row_ok ? partial_first(a, row, l, LANES)
+                                             : make_float2(0.f, 0.f));
+  float Q = sq.y;
+  if (a.kind == 1) {
+    const float mean0 = a.rms ? 0.f : sq.x * a.inv_hidden;
+    Q = group_sum<LANES>(row_ok ? partial_second(a, row, l, LANES, mean0) : 0.f);
+  }
+  const float2 st = partial_stats(a, sq.x, Q);
   if (row_ok && l == 0) {
     if (a.mean) a.mean[row] = st.x;
     if (a.rstd) a.rstd[row] = st.y;
@@ -172,7 +183,9 @@ __global__ void __launch_bounds__(kBulkThreads) fwdp_tile_kernel(const PartialsA
 template <typename T, int N>
 __global__ void __launch_bounds__(kBulkThreads) fwdp_cta_kernel(const PartialsArgs a) {
   constexpr int VEC = Vec<T>::N;
-  __shared__ float red[2][kConsumerWarps];
+  __shared__ float2 red[2][kConsumerWarps];
+  __shared__ float red1[2][kConsumerWarps];
+  int parity1 = 0;
   __shared__ unsigned red_amax[kConsumerWarps];
   const int64_t row = blockIdx.x;
   const int V = a.hidden / VEC;
@@ -184,12 +197,15 @@ __global__ void __launch_bounds__(kBulkThreads) fwdp_cta_kernel(const PartialsAr
     if (v < V) xr[k] = ld_vec(x + v * VEC);
   }
   int parity = 0;
-  const float S = cta_sum_db<kBulkThreads>(partial_sum(a, row, threadIdx.x, kBulkThreads), red,
-                                           parity);
-  const float mean0 = a.rms ? 0.f : S * a.inv_hidden;
-  const float Q = cta_sum_db<kBulkThreads>(
-      partial_second(a, row, threadIdx.x, kBulkThreads, mean0), red, parity);
-  const float2 st = partial_stats(a, S, Q);
+  const float2 sq = cta_sum2_db<kBulkThreads>(partial_first(a, row, threadIdx.x, kBulkThreads),
+                                              red, parity);
+  float Q = sq.y;
+  if (a.kind == 1) {
+    const float mean0 = a.rms ? 0.f : sq.x * a.inv_hidden;
+    Q = cta_sum_db<kBulkThreads>(partial_second(a, row, threadIdx.x, kBulkThreads, mean0),
+                                 red1, parity1);
+  }
+  const float2 st = partial_stats(a, sq.x, Q);
   if (threadIdx.x == 0) {
     if (a.mean) a.mean[row] = st.x;
     if (a.rstd) a.rstd[row] = st.y;
@@ -207,17 +223,21 @@ __global__ void __launch_bounds__(kBulkThreads) fwdp_cta_kernel(const PartialsAr
 // Any width and alignment: one CTA per row, element-wise.
 template <typename T>
 __global__ void __launch_bounds__(kScalarCta) fwdp_scalar_kernel(const PartialsArgs a) {
-  __shared__ float red[2][kScalarCta / 32];
+  __shared__ float2 red[2][kScalarCta / 32];
+  __shared__ float red1[2][kScalarCta / 32];
   __shared__ unsigned red_amax[kScalarCta / 32];
   const int64_t row = blockIdx.x;
   const int H = a.hidden;
-  int parity = 0;
-  const float S = cta_sum_db<kScalarCta>(partial_sum(a, row, threadIdx.x, kScalarCta), red,
-                                         parity);
-  const float mean0 = a.rms ? 0.f : S * a.inv_hidden;
-  const float Q = cta_sum_db<kScalarCta>(
-      partial_second(a, row, threadIdx.x, kScalarCta, mean0), red, parity);
-  const float2 st = partial_stats(a, S, Q);
+  int parity = 0, parity1 = 0;
+  const float2 sq = cta_sum2_db<kScalarCta>(partial_first(a, row, threadIdx.x, kScalarCta), red,
+                                            parity);
+  float Q = sq.y;
+  if (a.kind == 1) {
+    const float mean0 = a.rms ? 0.f : sq.x * a.inv_hidden;
+    Q = cta_sum_db<kScalarCta>(partial_second(a, row, threadIdx.x, kScalarCta, mean0), red1,
+                               parity1);
+  }
+  const float2 st = partial_stats(a, sq.x, Q);
   if (threadIdx.x == 0) {
     if (a.mean) a.mean[row] = st.x;
     if (a.rstd) a.rstd[row] = st.y;

@@ -5,6 +5,7 @@
 
 #include "bulk.cuh"
 #include "launch.h"
+#include "softmax_kernels.cuh"
 
 namespace nf {
 
@@ -323,7 +324,7 @@ template <typename T> cudaError_t softmax_plan(int64_t rows, int hidden, bool ve
   const Choice c = choose(hidden, Vec<T>::N, vec);
   const int smx_path = kernel_family(kFamilySoftmax);
   if (smx_path == 0 && c.kind == 1) {
-    // Rows of more than 256 vectors: one CTA per row from registers.
+    // Rows of more than 256 vectors: a CTA per one or two rows, from registers.
     p->bulk = false;
     p->kind = 5;
     p->group = kBulkThreads;
@@ -333,8 +334,9 @@ template <typename T> cudaError_t softmax_plan(int64_t rows, int hidden, bool ve
     p->fn = Tables<T>::softmax(5, kBulkThreads, p->n);
     cudaError_t e = size_grid(p, 1);
     if (e != cudaSuccess) return e;
-    if (rows > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    p->grid = (int)rows;
+    const int64_t ctas = smx_cta_grid(rows, p->n);
+    if (ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    p->grid = (int)ctas;
     return cudaSuccess;
   }
   if (smx_path == 0 && c.kind == 0) {

@@ -79,6 +79,7 @@ SHAPES = [
     ("f32", 37, 8192), ("f32", 50, 1025), ("f32", 9, 1),
     ("bf16", 1000, 384), ("bf16", 515, 8), ("bf16", 300, 24), ("bf16", 129, 2048),
     ("bf16", 77, 4096), ("bf16", 33, 16384), ("bf16", 100, 1000), ("bf16", 40, 8191),
+    ("bf16", 41, 8192), ("bf16", 23, 6144),    # two rows per CTA with an odd row count
     ("bf16", 17, 3),
     ("f16", 8192, 320), ("f16", 999, 640), ("f16", 601, 1280), ("f16", 65, 12288),
     ("f16", 31, 7),
