@@ -30,6 +30,9 @@ def test_entries_are_near_the_algorithmic_bytes():
         if workload in bench.SOFTMAX_WORKLOADS:
             w = bench.SOFTMAX_WORKLOADS[workload]
             algo = {"ln_softmax_fwd": bench.softmax_bytes(w)}
+        elif workload in bench.PARTIALS_WORKLOADS:
+            w = bench.PARTIALS_WORKLOADS[workload]
+            algo = {"ln_fwd_from_partials": bench.partials_bytes(w, bench.W.PARTIALS_TILE_COLS)}
         else:
             w = bench.BENCH_WORKLOADS[workload]
             algo = {"ln_fwd": bench.fwd_bytes(w), "ln_bwd": bench.bwd_bytes(w)}
