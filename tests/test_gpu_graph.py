@@ -1,8 +1,9 @@
 """The C-ABI calls inside a captured CUDA graph: ln_fwd, ln_bwd (with its
-workspace and the programmatically launched finalize) and ln_softmax_fwd are
-captured once, the graph is replayed on new inputs copied into the same
-buffers, and every output must equal, bit for bit, eager calls on those
-inputs (same kernels, same deterministic partial order)."""
+workspace and the programmatically launched finalize), ln_fwd_from_partials
+and ln_softmax_fwd are captured once, the graph is replayed on new inputs
+copied into the same buffers, and every output must equal, bit for bit,
+eager calls on those inputs (same kernels, same deterministic partial
+order)."""
 
 import pytest
 import torch
@@ -14,6 +15,25 @@ pytestmark = pytest.mark.gpu
 
 def _bits(t):
     return t.view(torch.int16) if t.element_size() == 2 else t.view(torch.int32)
+
+
+TILE = 128
+
+
+def _with_partials(inp):
+    """Per-128-column-tile (sum, M2) partials of x, from torch ops (input data
+    for ln_fwd_from_partials, standing in for a producing GEMM's epilogue)."""
+    x = inp["x"].float()
+    R, H = x.shape
+    T = -(-H // TILE)
+    t = torch.nn.functional.pad(x, (0, T * TILE - H)).view(R, T, TILE)
+    n = torch.full((T,), float(TILE), device=x.device)
+    n[-1] = H - (T - 1) * TILE
+    psum = t.sum(-1)
+    mask = (torch.arange(T * TILE, device=x.device) < H).view(T, TILE).float()
+    psq = (((t - (psum / n)[..., None]) * mask) ** 2).sum(-1)
+    inp["psum"], inp["psq"] = psum.contiguous(), psq.contiguous()
+    return inp
 
 
 @pytest.mark.parametrize("base", [W.BENCH_LN_BF16_576000x384, W.BENCH_RMS_BF16_16384x8192],
@@ -28,12 +48,15 @@ def test_fwd_bwd_softmax_replay_in_a_cuda_graph(cuda_lib, base):
 
     def buffers():
         inp = {k: (v.to(dev) if v is not None else None) for k, v in W.make_inputs(w, seed=1).items()}
+        inp = _with_partials(inp)
         f32 = dict(dtype=torch.float32, device=dev)
         out = dict(sum=torch.empty(R, H, dtype=dt, device=dev), y=torch.empty(R, H, dtype=dt, device=dev),
                    mean=None if rms else torch.empty(R, **f32), rstd=torch.empty(R, **f32),
                    amax=torch.empty(1, **f32), dx=torch.empty(R, H, dtype=dt, device=dev),
                    dgamma=torch.empty(H, **f32), dbeta=None if rms else torch.empty(H, **f32),
-                   sm=torch.empty(R, H, dtype=dt, device=dev))
+                   sm=torch.empty(R, H, dtype=dt, device=dev),
+                   py=torch.empty(R, H, dtype=dt, device=dev),
+                   pmean=None if rms else torch.empty(R, **f32), prstd=torch.empty(R, **f32))
         ws = torch.empty(max(16, nf.ln_bwd_workspace_bytes(R, H, dt, w.mode)), dtype=torch.uint8,
                          device=dev)
         return inp, out, ws
@@ -46,6 +69,9 @@ def test_fwd_bwd_softmax_replay_in_a_cuda_graph(cuda_lib, base):
                   out["dgamma"], out["dbeta"], stream, mode=w.mode,
                   zero_centered_gamma=w.zero_centered_gamma, workspace=ws)
         nf.ln_softmax_fwd(out["y"], out["sm"], stream)
+        nf.ln_fwd_from_partials(inp["x"], inp["psum"], inp["psq"], TILE, "sum_m2", inp["gamma"],
+                                inp["beta"], w.eps, w.mode, w.zero_centered_gamma, out["py"],
+                                out["pmean"], out["prstd"], None, stream)
 
     inp, out, ws = buffers()
     s = torch.cuda.Stream()
@@ -60,7 +86,8 @@ def test_fwd_bwd_softmax_replay_in_a_cuda_graph(cuda_lib, base):
         step(inp, out, ws, torch.cuda.current_stream())
 
     # new inputs into the captured buffers, replay
-    fresh = {k: (v.to(dev) if v is not None else None) for k, v in W.make_inputs(w, seed=2).items()}
+    fresh = _with_partials({k: (v.to(dev) if v is not None else None)
+                            for k, v in W.make_inputs(w, seed=2).items()})
     for k, v in fresh.items():
         if v is not None:
             inp[k].copy_(v)
