@@ -158,12 +158,35 @@ __global__ void __launch_bounds__(kBulkThreads) fwdp_tile_kernel(const PartialsA
   }
   // Statistics: every lane group runs its butterflies (whole warps take
   // part in the shuffles); a group past the last row reads no partials.
-  const float2 sq = group_sum2<LANES>(row_ok ? partial_first(a, row, l, LANES)
-                                             : make_float2(0.f, 0.f));
-  float Q = sq.y;
-  if (a.kind == 1) {
-    const float mean0 = a.rms ? 0.f : sq.x * a.inv_hidden;
-    Q = group_sum<LANES>(row_ok ? partial_second(a, row, l, LANES, mean0) : 0.f);
+  float2 sq;
+  float Q;
+  if (a.n_tiles <= LANES) {
+    // At most one tile per lane: lane l holds tile l's (psum, psq) in
+    // registers for both passes, loaded together with no loop. The sums
+    // are those of the general path below (one term per lane).
+    const bool has = row_ok && l < a.n_tiles;
+    float ps = 0.f, pq = 0.f;
+    if (has) {
+      ps = a.psum[row * (int64_t)a.n_tiles + l];
+      pq = a.psq[row * (int64_t)a.n_tiles + l];
+    }
+    sq = group_sum2<LANES>(make_float2(ps, a.kind == 0 ? pq : 0.f));
+    Q = sq.y;
+    if (a.kind == 1) {
+      const bool last = l == a.n_tiles - 1;
+      const float n = last ? (float)(a.hidden - (a.n_tiles - 1) * a.tile_cols)
+                           : (float)a.tile_cols;
+      const float inv_n = last ? a.inv_last : a.inv_tile;
+      const float d = a.rms ? ps : fmaf(-n, sq.x * a.inv_hidden, ps);
+      Q = group_sum<LANES>(has ? fmaf(d * d, inv_n, pq) : 0.f);
+    }
+  } else {
+    sq = group_sum2<LANES>(row_ok ? partial_first(a, row, l, LANES) : make_float2(0.f, 0.f));
+    Q = sq.y;
+    if (a.kind == 1) {
+      const float mean0 = a.rms ? 0.f : sq.x * a.inv_hidden;
+      Q = group_sum<LANES>(row_ok ? partial_second(a, row, l, LANES, mean0) : 0.f);
+    }
   }
   const float2 st = partial_stats(a, sq.x, Q);
   if (row_ok && l == 0) {
