@@ -679,12 +679,55 @@ __global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdA
 // CTAs per SM would leave. Per-row results are those of bwd_row_cta_kernel
 // (the same operations in the same order). Taken when the accumulators and
 // both rows fit in registers (the planner's bwd_row_pf_fits).
-template <typename T, int N, bool kRms, bool kBias>
+//
+// kSmem: where the column sums live. 0: registers. 1: dbeta (LayerNorm) and
+// dbias in shared memory after w, [N][Q][thread] float4 per sum, each thread
+// its own slots (no barrier guards them inside the row loop), dgamma in
+// registers. 2: dgamma in shared memory too. Moving the sums out of
+// registers is what lets rows of four vectors per thread keep both rows in
+// registers without spilling; the same sums in the same order as the
+// register form, one 16-byte shared load and store per two pairs and sum.
+template <typename T, int N, bool kRms, bool kBias, int kSmem = 0>
 __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs a) {
   constexpr int VEC = Vec<T>::N;
   constexpr int P = VEC / 2;
   constexpr int Q = P / 2;   // float4 per vector of w
-  extern __shared__ __align__(16) float4 w_s[];   // [N][Q][kBulkThreads]
+  extern __shared__ __align__(16) float4 w_s[];   // [N][Q][kBulkThreads], then the kSmem slots
+  // Shared-memory sums in order: dgamma (kSmem 2), dbeta (LayerNorm), dbias.
+  constexpr bool kGS = kSmem == 2;
+  constexpr bool kBS = kSmem >= 1 && !kRms;
+  constexpr bool kDS = kSmem >= 1 && kBias;
+  constexpr int kSlotB = kGS ? 1 : 0;
+  constexpr int kSlotD = kSlotB + (kBS ? 1 : 0);
+  constexpr int kAccS = (kGS ? 1 : 0) + (kBS ? 1 : 0) + (kDS ? 1 : 0);
+  float4* acc_s = w_s + N * Q * kBulkThreads;
+  auto acc_slot = [&](int which, int k, int q) -> float4& {
+    return acc_s[((which * N + k) * Q + q) * kPfThreads + threadIdx.x];
+  };
+  auto acc_add = [&](int which, int k, const float2 (&v)[P]) {
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      float4& s = acc_slot(which, k, q);
+      const float2 lo = add2(make_float2(s.x, s.y), v[2 * q]);
+      const float2 hi = add2(make_float2(s.z, s.w), v[2 * q + 1]);
+      s = make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+  };
+  auto acc_fma = [&](int which, int k, const float2 (&u)[P], const float2 (&v)[P]) {
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      float4& s = acc_slot(which, k, q);
+      const float2 lo = fma2(u[2 * q], v[2 * q], make_float2(s.x, s.y));
+      const float2 hi = fma2(u[2 * q + 1], v[2 * q + 1], make_float2(s.z, s.w));
+      s = make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+  };
+#pragma unroll
+  for (int which = 0; which < kAccS; ++which)
+#pragma unroll
+    for (int k = 0; k < N; ++k)
+#pragma unroll
+      for (int q = 0; q < Q; ++q) acc_slot(which, k, q) = make_float4(0.f, 0.f, 0.f, 0.f);
   __shared__ float2 red[kPfGroups][2][kConsumerWarps];
   const int grp = threadIdx.x / kBulkThreads;
   const int t = threadIdx.x % kBulkThreads;
@@ -782,14 +825,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
         unpack2<T>(xr[k], xv);
         load_w(k, w);
 #pragma unroll
+        float2 xh[P];
+#pragma unroll
         for (int i = 0; i < P; ++i) {
-          const float2 xh = mul2(kRms ? xv[i] : add2(xv[i], neg_mean), r2);
+          xh[i] = mul2(kRms ? xv[i] : add2(xv[i], neg_mean), r2);
           const float2 g = mul2(d[i], w[i]);
           if (!kRms) sx = add2(sx, g);
-          sy = fma2(g, xh, sy);
-          acc_g[k][i] = fma2(d[i], xh, acc_g[k][i]);
-          if (!kRms) acc_b[k][i] = add2(acc_b[k][i], d[i]);
+          sy = fma2(g, xh[i], sy);
+          if (!kGS) acc_g[k][i] = fma2(d[i], xh[i], acc_g[k][i]);
+          if (!kRms && !kBS) acc_b[k][i] = add2(acc_b[k][i], d[i]);
         }
+        if (kGS) acc_fma(0, k, d, xh);
+        if (kBS) acc_add(kSlotB, k, d);
       }
     }
     const float2 sums = group_row_sum(make_float2(kRms ? 0.f : sx.x + sx.y, sy.x + sy.y));
@@ -812,8 +859,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
           const float2 gr = kRms ? mul2(mul2(d[i], w[i]), r2)
                                  : fma2(mul2(d[i], w[i]), r2, a1);
           o[i] = fma2(kRms ? xv[i] : add2(xv[i], neg_mean), b2, gr);
-          if (kBias) acc_d[k][i] = add2(acc_d[k][i], o[i]);
+          if (kBias && !kDS) acc_d[k][i] = add2(acc_d[k][i], o[i]);
         }
+        if (kDS) acc_add(kSlotD, k, o);
         st_vec(dx + off + v * VEC, pack2<T>(o));
       }
     }
@@ -850,9 +898,31 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
       }
     }
   };
-  put(acc_g, 0);
-  if (!kRms) put(acc_b, H);
-  if (kBias) put(acc_d, kRms ? H : 2 * H);
+  // Shared-memory sums: group 0 adds group 1's slots (thread t + 256) to its
+  // own, after a barrier that orders the row loop's last shared stores.
+  auto put_s = [&](int which, int off) {
+    __syncthreads();
+    if (grp == 0) {
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        const int v = k * kBulkThreads + t;
+        if (v < V) {
+          float4* dst = reinterpret_cast<float4*>(ws + off + v * VEC);
+#pragma unroll
+          for (int q = 0; q < Q; ++q) {
+            const float4 m = acc_slot(which, k, q);
+            const float4 o = acc_s[((which * N + k) * Q + q) * kPfThreads + kBulkThreads + t];
+            const float2 lo = add2(make_float2(m.x, m.y), make_float2(o.x, o.y));
+            const float2 hi = add2(make_float2(m.z, m.w), make_float2(o.z, o.w));
+            dst[q] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          }
+        }
+      }
+    }
+  };
+  if (kGS) put_s(0, 0); else put(acc_g, 0);
+  if (kBS) put_s(kSlotB, H); else if (!kRms) put(acc_b, H);
+  if (kDS) put_s(kSlotD, kRms ? H : 2 * H); else if (kBias) put(acc_d, kRms ? H : 2 * H);
 }
 
 // ---- scalar kernel ----------------------------------------------------------

@@ -23,7 +23,9 @@ struct Plan {
                        // 4 lane group from registers, one CTA per row tile,
                        // 5 CTA per row from registers (forward and softmax: one
                        // CTA per row; backward: a persistent grid over the rows),
-                       // 6 backward CTA per row with the next row prefetched
+                       // 6 backward CTA per row with the next row prefetched,
+                       // 7 the same with dbeta / dbias summed in shared memory,
+                       // 8 with every column sum in shared memory
   int group = 0;       // threads sharing a row
   int n = 0;           // 16-byte vectors per thread per row
   int block = 0;

@@ -184,8 +184,10 @@ inline cudaError_t size_grid(Plan* p, int64_t steps) {
 // (measured with two 256-thread CTAs per SM, the same four rows in flight:
 // 16384 x 8192 bf16 RMSNorm 121.6 against 127.7 us, 21845 x 6144
 // LayerNorm 135.5 against 159.4 us; at 32768 x 4096 RMSNorm, where kind 5
-// runs four CTAs per SM, 138.5 against 128.9 us). The other aligned rows, and these too under the ring
-// family, stream through the bulk-copy ring.
+// runs four CTAs per SM, 138.5 against 128.9 us). Where neither fits, kinds
+// 7 and 8 (below) keep some or all column sums in shared memory. The other
+// aligned rows, and these too under the ring family, stream through the
+// bulk-copy ring.
 inline int bwd_acc_floats(int n, int vec_elems, bool rms, bool dbias) {
   return n * vec_elems * (1 + (rms ? 0 : 1) + (dbias ? 1 : 0));
 }
@@ -194,6 +196,31 @@ inline bool bwd_row_pf_fits(int n, int vec_elems, bool rms, bool dbias) {
 }
 inline bool bwd_row_cta_fits(int n, int vec_elems, bool rms, bool dbias) {
   return n <= 4 && bwd_acc_floats(n, vec_elems, rms, dbias) + 8 * n <= (rms ? 64 : 56);
+}
+// Kinds 7 and 8: kind 6 with column sums in shared memory, each thread its
+// own slots. Kind 7 moves dbeta and dbias there, so only dgamma's (n * VEC
+// floats) count against the registers; kind 8 moves dgamma's too, and is
+// taken for LayerNorm without dbias (rows of four vectors: kind 7 spills a
+// little there). Measured at 16384 x 8192 bf16, kernel alone: LayerNorm
+// 150 us as kind 8 against 166 as kind 7 and 171 on the ring; LayerNorm
+// with dbias 189 as kind 7 against 232 as kind 8 (224 KiB of shared memory
+// leave L1 little room) and 246 on the ring; RMSNorm with dbias 135 as kind
+// 7 against 142 as kind 8; 21845 x 6144 LayerNorm with dbias 146 as kind 7
+// against 174 as kind 8 and 189 on the ring.
+inline bool bwd_row_pf_smem_fits(int n, int vec_elems, bool rms, bool dbias) {
+  return n >= 3 && n <= 4 && (!rms || dbias) && n * vec_elems + 16 * n <= 96;
+}
+inline bool bwd_row_pf_all_smem(int n, bool rms, bool dbias) {
+  return n == 4 && !rms && !dbias;
+}
+// Dynamic shared memory of kinds 6-8: w staged as fp32 (n vectors of VEC
+// floats per thread of a row group), then the shared-memory sums of both
+// row groups (smem_sums: 1 for kind 7, 2 for kind 8).
+inline size_t bwd_row_pf_smem(int n, int vec_elems, bool rms, bool dbias, int smem_sums) {
+  const size_t per = (size_t)n * vec_elems * sizeof(float);
+  const int n_acc = smem_sums == 0 ? 0
+                                   : (smem_sums == 2 ? 1 : 0) + (rms ? 0 : 1) + (dbias ? 1 : 0);
+  return per * kBulkThreads + per * kPfThreads * n_acc;
 }
 constexpr int kRowsInFlightPf = 4;   // kind 6: two row groups per SM, two rows each
 
@@ -214,14 +241,15 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
       if (e != cudaSuccess) return e;
       pf = per_sm < kRowsInFlightPf;
     }
-    if (pf || one) {
+    const bool pf_smem = !pf && !one && bwd_row_pf_smem_fits(n, Vec<T>::N, rms, dbias);
+    if (pf || one || pf_smem) {
+      const int smem_sums = pf_smem ? (bwd_row_pf_all_smem(n, rms, dbias) ? 2 : 1) : 0;
       p->bulk = false;
-      p->kind = pf ? 6 : 5;
+      p->kind = pf ? 6 : (pf_smem ? 6 + smem_sums : 5);
       p->group = kBulkThreads;
       p->n = n;
-      p->block = pf ? kPfThreads : kBulkThreads;
-      // kind 6 stages w as fp32: n vectors of VEC floats per thread
-      p->smem = pf ? (size_t)n * Vec<T>::N * sizeof(float) * kBulkThreads : 0;
+      p->block = (pf || pf_smem) ? kPfThreads : kBulkThreads;
+      p->smem = (pf || pf_smem) ? bwd_row_pf_smem(n, Vec<T>::N, rms, dbias, smem_sums) : 0;
       p->fn = Tables<T>::bwd_bulk(p->kind, kBulkThreads, n, rms, dbias, false);
       return size_grid(p, rows);
     }

@@ -117,6 +117,16 @@ const void* bwd_bulk_table_impl(int kind, int group, int n, bool exact) {
       case 4: return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias>;
       default: return nullptr;
     }
+  } else if (kind == 7 && (!kRms || kBias)) {
+    // dbeta / dbias sums in shared memory (RMSNorm without dbias has none)
+    switch (n) {
+      case 3: return (const void*)bwd_row_pf_kernel<T, 3, kRms, kBias, 1>;
+      case 4: return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 1>;
+      default: return nullptr;
+    }
+  } else if (kind == 8 && !kRms && !kBias && n == 4) {
+    // every column sum in shared memory (LayerNorm rows of four vectors)
+    return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 2>;
   }
   return nullptr;
 }

@@ -141,10 +141,13 @@ def test_unaligned_pointers_use_scalar_path(cuda_lib, dtype):
 # Wide rows with more rows than CTAs, so every CTA of the CTA-per-row
 # backward works on several rows (with the next one prefetched where its
 # registers allow) and the last steps are ragged: each n of the prefetching
-# kernel for both modes, with dbias, in each dtype.
+# kernel for both modes, with dbias, in each dtype, and the form that keeps
+# the dbeta / dbias sums in shared memory (8192-wide LayerNorm in 16-bit
+# types, 6144-wide LayerNorm and 8192-wide RMSNorm with dbias).
 WIDE = [("bf16", 2056, W.LAYERNORM), ("bf16", 4096, W.RMSNORM), ("bf16", 6144, W.LAYERNORM),
         ("bf16", 6144, W.RMSNORM), ("bf16", 8192, W.RMSNORM), ("bf16", 8192, W.LAYERNORM),
-        ("f16", 3000, W.RMSNORM), ("f32", 2048, W.LAYERNORM), ("f32", 3072, W.RMSNORM)]
+        ("f16", 3000, W.RMSNORM), ("f16", 8192, W.LAYERNORM), ("f32", 2048, W.LAYERNORM),
+        ("f32", 3072, W.RMSNORM)]
 
 
 @pytest.mark.parametrize("dtype,hidden,mode", WIDE, ids=lambda v: str(v))
@@ -174,7 +177,8 @@ def test_wide_rows_many_rows_per_cta(cuda_lib, dtype, hidden, mode, dbias):
     (50001, 384, W.LAYERNORM, False),     # pipelined lane-group backward
     (3001, 8192, W.RMSNORM, False),       # register CTA-per-row backward
     (2001, 3072, W.LAYERNORM, True),      # the same with zero-centered gamma
-], ids=["ln384", "rms8192", "ln3072zc"])
+    (3001, 8192, W.LAYERNORM, False),     # dbeta summed in shared memory
+], ids=["ln384", "rms8192", "ln3072zc", "ln8192"])
 def test_backward_is_deterministic(cuda_lib, rows, hidden, mode, zc):
     w = wl("bf16", rows, hidden, mode, zero_centered_gamma=zc)
     inp = make_inputs(w, seed=3)
