@@ -17,6 +17,8 @@ using f16 = __half;
 constexpr int kScalarCta = 256;        // threads per CTA of the scalar kernels
 constexpr int kConsumerWarps = 8;      // warps of a pipelined CTA
 constexpr int kBulkThreads = kConsumerWarps * 32;
+constexpr int kMaxFitThreads = 512;   // largest CTA of the row-fitted kernels
+constexpr int kMaxFitWarps = kMaxFitThreads / 32;
 // Threads of the prefetching CTA-per-row backward: two row groups of 256.
 constexpr int kPfGroups = 2;
 constexpr int kPfThreads = kPfGroups * kBulkThreads;
@@ -350,6 +352,20 @@ __device__ __forceinline__ float2 cta_sum2_db(float2 v, float2 (*red)[THREADS / 
     t.x += red[parity][i].x;
     t.y += red[parity][i].y;
   }
+  parity ^= 1;
+  return t;
+}
+
+// cta_sum_db for a CTA of any whole number of warps up to kMaxFitWarps
+// (blockDim.x chosen at launch): the warps' sums added in warp order.
+__device__ __forceinline__ float cta_sum_db_fit(float v, float (*red)[kMaxFitWarps], int& parity) {
+  const int W = blockDim.x >> 5;
+  v = group_sum<32>(v);
+  if ((threadIdx.x & 31) == 0) red[parity][threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll 4
+  for (int i = 0; i < W; ++i) t += red[parity][i];
   parity ^= 1;
   return t;
 }

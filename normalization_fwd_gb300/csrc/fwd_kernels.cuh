@@ -60,14 +60,16 @@ __device__ __forceinline__ FwdParams<T> fwd_params(const FwdArgs& a, float* p_s)
 // The row body: `xr` / `rr` hold the thread's 16-byte vectors k * G + t of
 // the x and residual rows (those below V; rr only with a residual),
 // parameters staged in shared memory (kStaged) or read from global memory.
-// Values are kept as fp32 pairs (packed fp32 math).
-template <typename T, int G, int N, bool kStaged, typename Reduce>
+// Values are kept as fp32 pairs (packed fp32 math). G = 0: the row's
+// threads are the whole CTA, blockDim.x of them.
+template <typename T, int G0, int N, bool kStaged, typename Reduce>
 __device__ __forceinline__ void fwd_row_regs(const FwdArgs& a, int64_t row, bool row_ok, int t,
                                              const uint4 (&xr)[N], const uint4 (&rr)[N],
                                              bool has_res, const FwdParams<T>& p, Reduce reduce,
                                              unsigned& amax_acc, bool write_stats) {
   constexpr int VEC = Vec<T>::N;
   constexpr int P = VEC / 2;
+  const int G = G0 > 0 ? G0 : (int)blockDim.x;
   const int H = a.hidden;
   const int V = H / VEC;
   T* sum_row = a.out_sum ? static_cast<T*>(a.out_sum) + row * (int64_t)H : nullptr;
@@ -220,11 +222,17 @@ __global__ void __launch_bounds__(kBulkThreads, N <= 3 ? 4 : 2) fwd_tile_kernel(
 // Rows of more than 256 vectors from registers: one CTA per row, as many
 // CTAs as rows; the row sums go through the CTA (double-buffered, one
 // barrier each).
+// One CTA per row, its size fitted to the row at launch (blockDim.x = NT,
+// a whole number of warps up to kMaxFitThreads, NT * N >= the row's
+// vectors): small CTAs of a few vectors per thread keep more rows in flight
+// per SM than a fixed 256 threads that leave vector slots idle (2560 bf16,
+// 52428 rows: 157 us as 64 x 5 against 228 as 256 x 2).
 template <typename T, int N>
-__global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 3 : 2) fwd_tile_cta_kernel(const FwdArgs a) {
+__global__ void __launch_bounds__(kMaxFitThreads, N <= 4 ? 2 : 1) fwd_tile_cta_kernel(const FwdArgs a) {
   constexpr int VEC = Vec<T>::N;
-  __shared__ float red[2][kConsumerWarps];
-  __shared__ unsigned red_amax[kConsumerWarps];
+  __shared__ float red[2][kMaxFitWarps];
+  __shared__ unsigned red_amax[kMaxFitWarps];
+  const int nt = blockDim.x;
   const int64_t row = blockIdx.x;
   const int H = a.hidden;
   const int V = H / VEC;
@@ -233,7 +241,7 @@ __global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 3 : 2) fwd_tile_cta_ker
   uint4 xr[N], rr[N];
 #pragma unroll
   for (int k = 0; k < N; ++k) {
-    const int v = k * kBulkThreads + threadIdx.x;
+    const int v = k * nt + threadIdx.x;
     if (v < V) {
       xr[k] = ld_vec(x + v * VEC);
       if (res) rr[k] = ld_vec(res + v * VEC);
@@ -242,16 +250,15 @@ __global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 3 : 2) fwd_tile_cta_ker
   const FwdParams<T> p = fwd_params<T>(a, nullptr);
   unsigned amax_acc = 0;
   int parity = 0;
-  fwd_row_regs<T, kBulkThreads, N, false>(
+  fwd_row_regs<T, 0, N, false>(
       a, row, true, threadIdx.x, xr, rr, res != nullptr, p,
-      [&](float v) { return cta_sum_db<kBulkThreads>(v, red, parity); }, amax_acc,
-      threadIdx.x == 0);
+      [&](float v) { return cta_sum_db_fit(v, red, parity); }, amax_acc, threadIdx.x == 0);
   if (a.amax) {
     unsigned m = __reduce_max_sync(0xffffffffu, amax_bits<T>(amax_acc));
     if ((threadIdx.x & 31) == 0) red_amax[threadIdx.x >> 5] = m;
     __syncthreads();
     if (threadIdx.x == 0) {
-      for (int i = 1; i < kConsumerWarps; ++i) m = max(m, red_amax[i]);
+      for (int i = 1; i < (nt >> 5); ++i) m = max(m, red_amax[i]);
       if (m > *(volatile unsigned*)a.amax) atomicMax(a.amax, m);
     }
   }

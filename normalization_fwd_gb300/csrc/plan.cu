@@ -64,6 +64,37 @@ inline Choice bwd_choice(const Choice& c, int hidden, int vec_elems, bool rms, b
   return c;
 }
 
+// CTA size (a whole number of warps, 64 to kMaxFitThreads) and vectors per
+// thread of the row-fitted CTA-per-row kernels, for rows of V > 256
+// vectors: four vectors per thread where that splits the row into whole
+// warps, else five, three, six, eight or two; failing all, the split of
+// four, five, three or six per thread that leaves the fewest vector slots
+// idle. (Forward at 268 MB per tensor, bf16: 2560 wide 157 us as 64 x 5,
+// 228 as 256 x 2; 3072 156 as 96 x 4, 199 as 256 x 2; 4096 157 as
+// 128 x 4, 176 as 256 x 2; 5120 156 as 160 x 4, 168 as 256 x 3.)
+struct Fit {
+  int threads, n;
+};
+inline Fit cta_fit(int V) {
+  for (int n : {4, 5, 3, 6, 8, 2}) {
+    if (V % n) continue;
+    const int nt = V / n;
+    if (nt % 32 == 0 && nt >= 64 && nt <= kMaxFitThreads) return {nt, n};
+  }
+  Fit best = {0, 0};
+  int idle = 1 << 30;
+  for (int n : {4, 5, 3, 6}) {
+    const int nt = std::max(64, (V + 32 * n - 1) / (32 * n) * 32);
+    if (nt > kMaxFitThreads) continue;
+    if (nt * n - V < idle) {
+      idle = nt * n - V;
+      best = {nt, n};
+    }
+  }
+  if (best.n == 0) best = {kMaxFitThreads, std::max(2, (V + kMaxFitThreads - 1) / kMaxFitThreads)};
+  return best;
+}
+
 // Vectors per consumer thread when the 256 consumers of a pipelined CTA
 // share one row (rows of more than 256 vectors).
 inline int bulk_cta_n(int hidden, int vec_elems) {
@@ -255,13 +286,14 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
     }
   }
   if (!bwd && vec && c.kind == 1 && !ring) {
+    const Fit f = cta_fit(hidden / Vec<T>::N);
     p->bulk = false;
     p->kind = 5;
-    p->group = kBulkThreads;
-    p->n = bulk_cta_n(hidden, Vec<T>::N);
-    p->block = kBulkThreads;
+    p->group = f.threads;
+    p->n = f.n;
+    p->block = f.threads;
     p->smem = 0;
-    p->fn = Tables<T>::fwd_bulk(5, kBulkThreads, p->n);
+    p->fn = Tables<T>::fwd_bulk(5, f.threads, p->n);
     cudaError_t e = size_grid(p, 1);
     if (e != cudaSuccess) return e;
     if (rows > 0x7fffffff) return cudaErrorInvalidConfiguration;
