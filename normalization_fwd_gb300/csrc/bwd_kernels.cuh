@@ -666,9 +666,10 @@ __global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdA
 }
 
 // The same rows with the next row's dy and x_sum (and statistics) loaded
-// into registers while this row is worked on. One CTA per SM holds two row
-// groups of 256 threads; group g of CTA b takes rows 2b + g, 2b + g + 2G, ...
-// (G CTAs), so each SM keeps four rows in flight (two groups, two rows each).
+// into registers while this row is worked on. A CTA holds two row groups of
+// GT threads (256; 128 for rows of up to 512 vectors, two CTAs per SM);
+// group g of CTA b takes rows 2b + g, 2b + g + 2G, ... (G CTAs), so each
+// CTA keeps four rows in flight (two groups, two rows each).
 // Each group sums its row behind a named barrier of its own threads, so the
 // groups never wait for each other inside the row loop. w = gamma (+1 for
 // zero-centered gamma) is staged once per kernel in shared memory as fp32
@@ -687,12 +688,17 @@ __global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdA
 // registers is what lets rows of four vectors per thread keep both rows in
 // registers without spilling; the same sums in the same order as the
 // register form, one 16-byte shared load and store per two pairs and sum.
-template <typename T, int N, bool kRms, bool kBias, int kSmem = 0>
-__global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs a) {
+template <typename T, int N, bool kRms, bool kBias, int kSmem = 0, int GT = kBulkThreads>
+__global__ void __launch_bounds__(kPfGroups * GT, kPfThreads / (kPfGroups * GT))
+    bwd_row_pf_kernel(const BwdArgs a) {
   constexpr int VEC = Vec<T>::N;
   constexpr int P = VEC / 2;
   constexpr int Q = P / 2;   // float4 per vector of w
-  extern __shared__ __align__(16) float4 w_s[];   // [N][Q][kBulkThreads], then the kSmem slots
+  extern __shared__ __align__(16) float4 w_s[];   // [N][Q][gt], then the kSmem slots
+  // Threads of a row group (GT: 256, or 128 for rows of up to 512 vectors)
+  // and of the CTA.
+  constexpr int gt = GT;
+  constexpr int ct = kPfGroups * GT;
   // Shared-memory sums in order: dgamma (kSmem 2), dbeta (LayerNorm), dbias.
   constexpr bool kGS = kSmem == 2;
   constexpr bool kBS = kSmem >= 1 && !kRms;
@@ -700,9 +706,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
   constexpr int kSlotB = kGS ? 1 : 0;
   constexpr int kSlotD = kSlotB + (kBS ? 1 : 0);
   constexpr int kAccS = (kGS ? 1 : 0) + (kBS ? 1 : 0) + (kDS ? 1 : 0);
-  float4* acc_s = w_s + N * Q * kBulkThreads;
+  float4* acc_s = w_s + N * Q * gt;
   auto acc_slot = [&](int which, int k, int q) -> float4& {
-    return acc_s[((which * N + k) * Q + q) * kPfThreads + threadIdx.x];
+    return acc_s[((which * N + k) * Q + q) * ct + threadIdx.x];
   };
   auto acc_add = [&](int which, int k, const float2 (&v)[P]) {
 #pragma unroll
@@ -729,8 +735,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
 #pragma unroll
       for (int q = 0; q < Q; ++q) acc_slot(which, k, q) = make_float4(0.f, 0.f, 0.f, 0.f);
   __shared__ float2 red[kPfGroups][2][kConsumerWarps];
-  const int grp = threadIdx.x / kBulkThreads;
-  const int t = threadIdx.x % kBulkThreads;
+  const int grp = threadIdx.x / gt;
+  const int t = threadIdx.x % gt;
   const int H = a.hidden;
   const int V = H / VEC;
   const T* dy = static_cast<const T*>(a.dy);
@@ -740,7 +746,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
     const T* gamma = static_cast<const T*>(a.gamma);
 #pragma unroll
     for (int k = 0; k < N; ++k) {
-      const int v = k * kBulkThreads + t;
+      const int v = k * gt + t;
       if (v < V) {
         float2 w[P];
         unpack2<T>(ld_vec_param(gamma + v * VEC), w);
@@ -751,7 +757,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
             w0 = add2(w0, splat2(1.f));
             w1 = add2(w1, splat2(1.f));
           }
-          w_s[(k * Q + q) * kBulkThreads + t] = make_float4(w0.x, w0.y, w1.x, w1.y);
+          w_s[(k * Q + q) * gt + t] = make_float4(w0.x, w0.y, w1.x, w1.y);
         }
       }
     }
@@ -760,7 +766,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
   auto load_w = [&](int k, float2 (&w)[P]) {
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
-      const float4 f = w_s[(k * Q + q) * kBulkThreads + t];
+      const float4 f = w_s[(k * Q + q) * gt + t];
       w[2 * q] = make_float2(f.x, f.y);
       w[2 * q + 1] = make_float2(f.z, f.w);
     }
@@ -771,10 +777,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
   auto group_row_sum = [&](float2 v) {
     v = group_sum2<32>(v);
     if ((t & 31) == 0) red[grp][parity][t >> 5] = v;
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(kBulkThreads) : "memory");
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(gt) : "memory");
     float2 s = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < kConsumerWarps; ++i) {
+    for (int i = 0; i < gt / 32; ++i) {
       s.x += red[grp][parity][i].x;
       s.y += red[grp][parity][i].y;
     }
@@ -791,7 +797,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
     const int64_t off = row * (int64_t)H;
 #pragma unroll
     for (int k = 0; k < N; ++k) {
-      const int v = k * kBulkThreads + t;
+      const int v = k * gt + t;
       if (v < V) {
         nd[k] = ld_vec(dy + off + v * VEC);
         nx[k] = ld_vec(xs + off + v * VEC);
@@ -818,13 +824,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
     float2 sx = splat2(0.f), sy = splat2(0.f);
 #pragma unroll
     for (int k = 0; k < N; ++k) {
-      const int v = k * kBulkThreads + t;
+      const int v = k * gt + t;
       if (v < V) {
         float2 d[P], xv[P], w[P];
         unpack2<T>(dr[k], d);
         unpack2<T>(xr[k], xv);
         load_w(k, w);
-#pragma unroll
         float2 xh[P];
 #pragma unroll
         for (int i = 0; i < P; ++i) {
@@ -848,7 +853,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
     vec_fence<N>(xr);
 #pragma unroll
     for (int k = 0; k < N; ++k) {
-      const int v = k * kBulkThreads + t;
+      const int v = k * gt + t;
       if (v < V) {
         float2 d[P], xv[P], w[P], o[P];
         unpack2<T>(dr[k], d);
@@ -877,19 +882,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
       for (int k = 0; k < N; ++k)
 #pragma unroll
         for (int q = 0; q < Q; ++q)
-          w_s[(k * Q + q) * kBulkThreads + t] =
+          w_s[(k * Q + q) * gt + t] =
               make_float4(acc[k][2 * q].x, acc[k][2 * q].y, acc[k][2 * q + 1].x, acc[k][2 * q + 1].y);
     }
     __syncthreads();
     if (grp == 0) {
 #pragma unroll
       for (int k = 0; k < N; ++k) {
-        const int v = k * kBulkThreads + t;
+        const int v = k * gt + t;
         if (v < V) {
           float4* dst = reinterpret_cast<float4*>(ws + off + v * VEC);
 #pragma unroll
           for (int q = 0; q < Q; ++q) {
-            const float4 o = w_s[(k * Q + q) * kBulkThreads + t];
+            const float4 o = w_s[(k * Q + q) * gt + t];
             const float2 lo = add2(acc[k][2 * q], make_float2(o.x, o.y));
             const float2 hi = add2(acc[k][2 * q + 1], make_float2(o.z, o.w));
             dst[q] = make_float4(lo.x, lo.y, hi.x, hi.y);
@@ -905,13 +910,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) bwd_row_pf_kernel(const BwdArgs
     if (grp == 0) {
 #pragma unroll
       for (int k = 0; k < N; ++k) {
-        const int v = k * kBulkThreads + t;
+        const int v = k * gt + t;
         if (v < V) {
           float4* dst = reinterpret_cast<float4*>(ws + off + v * VEC);
 #pragma unroll
           for (int q = 0; q < Q; ++q) {
             const float4 m = acc_slot(which, k, q);
-            const float4 o = acc_s[((which * N + k) * Q + q) * kPfThreads + kBulkThreads + t];
+            const float4 o = acc_s[((which * N + k) * Q + q) * ct + gt + t];
             const float2 lo = add2(make_float2(m.x, m.y), make_float2(o.x, o.y));
             const float2 hi = add2(make_float2(m.z, m.w), make_float2(o.z, o.w));
             dst[q] = make_float4(lo.x, lo.y, hi.x, hi.y);

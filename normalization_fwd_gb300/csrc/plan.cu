@@ -95,6 +95,22 @@ inline Fit cta_fit(int V) {
   return best;
 }
 
+// The register forward's lane groups: four, then three, five, two or one
+// vectors per lane where the row splits exactly over 8, 16 or 32 lanes; rows
+// of more than kFwdGroupMaxV vectors take the row-fitted CTA kernel instead.
+// (268 MB per tensor, bf16 with residual: 256 wide 159 us as 8 x 4, 189 as
+// 32 x 1; 512 wide 160 as 16 x 4, 172 as 32 x 2; 1536 wide 155 as a 64 x 3
+// CTA, 168 as 32 x 6 lanes; 2048 wide 157 as a 64 x 4 CTA, 161 as 32 x 8.)
+constexpr int kFwdGroupMaxV = 160;
+inline Choice fwd_group_choice(const Choice& c, int V) {
+  for (int n : {4, 3, 5, 2, 1}) {
+    if (V % n) continue;
+    const int lanes = V / n;
+    if (lanes == 8 || lanes == 16 || lanes == 32) return {0, lanes, n};
+  }
+  return c;
+}
+
 // Vectors per consumer thread when the 256 consumers of a pipelined CTA
 // share one row (rows of more than 256 vectors).
 inline int bulk_cta_n(int hidden, int vec_elems) {
@@ -244,14 +260,33 @@ inline bool bwd_row_pf_smem_fits(int n, int vec_elems, bool rms, bool dbias) {
 inline bool bwd_row_pf_all_smem(int n, bool rms, bool dbias) {
   return n == 4 && !rms && !dbias;
 }
-// Dynamic shared memory of kinds 6-8: w staged as fp32 (n vectors of VEC
-// floats per thread of a row group), then the shared-memory sums of both
-// row groups (smem_sums: 1 for kind 7, 2 for kind 8).
-inline size_t bwd_row_pf_smem(int n, int vec_elems, bool rms, bool dbias, int smem_sums) {
+// Dynamic shared memory of kinds 6-8 with row groups of gt threads: w
+// staged as fp32 (n vectors of VEC floats per thread of a row group), then
+// the shared-memory sums of both row groups (smem_sums: 1 for kind 7, 2 for
+// kind 8).
+inline size_t bwd_row_pf_smem(int n, int vec_elems, bool rms, bool dbias, int smem_sums,
+                              int gt = kBulkThreads) {
   const size_t per = (size_t)n * vec_elems * sizeof(float);
   const int n_acc = smem_sums == 0 ? 0
                                    : (smem_sums == 2 ? 1 : 0) + (rms ? 0 : 1) + (dbias ? 1 : 0);
-  return per * kBulkThreads + per * kPfThreads * n_acc;
+  return per * gt + per * kPfGroups * gt * n_acc;
+}
+
+// Rows of 257 to 512 vectors, where 256-thread row groups of two vectors a
+// thread leave slots idle or hold too few rows per SM: two 128-thread row
+// groups per CTA and two CTAs per SM, three or four vectors a thread.
+// RMSNorm keeps its sums in registers (kind 6), LayerNorm and dbias rows of
+// three vectors keep dbeta / dbias in shared memory (kind 7). Measured at
+// 268 MB per tensor, bf16, kernel alone: RMSNorm 2560 wide 131.5 us against
+// 151.0 (256 x 2, kind 5), 3072 125.2 against 141.3, 4096 (four vectors)
+// 123.1 against 130.0; LayerNorm 2560 141.3 against 176.6 (256 x 2, kind 6),
+// 3072 129.3 against 177.0. LayerNorm at 4096 stays on 256 x 2 (142.7 us;
+// 147.6 as 128 x 4 with every sum in shared memory).
+inline int bwd_small_group_kind(int V, bool rms, bool dbias) {
+  if (V <= 256 || V > 512) return 0;
+  const int n = (V + 127) / 128;
+  if (rms && !dbias) return 6;
+  return n == 3 ? 7 : 0;
 }
 constexpr int kRowsInFlightPf = 4;   // kind 6: two row groups per SM, two rows each
 
@@ -261,6 +296,18 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
   const Choice c = choose(hidden, Vec<T>::N, vec);
   const bool ring = kernel_family(bwd ? kFamilyBackward : kFamilyForward) == kFamilyRing;
   if (bwd && vec && c.kind == 1 && !ring) {
+    const int sk = bwd_small_group_kind(hidden / Vec<T>::N, rms, dbias);
+    if (sk != 0) {
+      const int n = (hidden / Vec<T>::N + 127) / 128;
+      p->bulk = false;
+      p->kind = sk;
+      p->group = 128;
+      p->n = n;
+      p->block = kPfGroups * 128;
+      p->smem = bwd_row_pf_smem(n, Vec<T>::N, rms, dbias, sk - 6, 128);
+      p->fn = Tables<T>::bwd_bulk(p->kind, 128, n, rms, dbias, false);
+      return size_grid(p, rows);
+    }
     const int n = bulk_cta_n(hidden, Vec<T>::N);
     const bool one = bwd_row_cta_fits(n, Vec<T>::N, rms, dbias);
     bool pf = bwd_row_pf_fits(n, Vec<T>::N, rms, dbias);
@@ -285,8 +332,9 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
       return size_grid(p, rows);
     }
   }
-  if (!bwd && vec && c.kind == 1 && !ring) {
-    const Fit f = cta_fit(hidden / Vec<T>::N);
+  const int V = vec ? hidden / Vec<T>::N : 0;
+  if (!bwd && vec && !ring && (c.kind == 1 || (c.kind == 0 && V > kFwdGroupMaxV))) {
+    const Fit f = cta_fit(V);
     p->bulk = false;
     p->kind = 5;
     p->group = f.threads;
@@ -301,16 +349,17 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
     return cudaSuccess;
   }
   if (!bwd && vec && c.kind == 0 && !ring) {
+    const Choice g = fwd_group_choice(c, V);
     p->bulk = false;
     p->kind = 4;
-    p->group = c.group;
-    p->n = c.n;
+    p->group = g.group;
+    p->n = g.n;
     p->block = kBulkThreads;
     p->smem = 0;
-    p->fn = Tables<T>::fwd_bulk(4, c.group, c.n);
+    p->fn = Tables<T>::fwd_bulk(4, g.group, g.n);
     cudaError_t e = size_grid(p, 1);   // occupancy check and attributes
     if (e != cudaSuccess) return e;
-    const int64_t rpc = (int64_t)kConsumerWarps * (32 / c.group);
+    const int64_t rpc = (int64_t)kConsumerWarps * (32 / g.group);
     const int64_t ctas = (rows + rpc - 1) / rpc;
     if (ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
     p->grid = (int)ctas;

@@ -110,6 +110,12 @@ const void* bwd_bulk_table_impl(int kind, int group, int n, bool exact) {
       case 4: return (const void*)bwd_row_cta_kernel<T, 4, kRms, kBias>;
       default: return nullptr;
     }
+  } else if (kind == 6 && group == 128) {
+    // two 128-thread row groups (RMSNorm rows of up to 512 vectors)
+    if constexpr (kRms && !kBias) {
+      if (n == 3) return (const void*)bwd_row_pf_kernel<T, 3, kRms, kBias, 0, 128>;
+      if (n == 4) return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 0, 128>;
+    }
   } else if (kind == 6) {
     switch (n) {
       case 2: return (const void*)bwd_row_pf_kernel<T, 2, kRms, kBias>;
@@ -117,16 +123,19 @@ const void* bwd_bulk_table_impl(int kind, int group, int n, bool exact) {
       case 4: return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias>;
       default: return nullptr;
     }
-  } else if (kind == 7 && (!kRms || kBias)) {
-    // dbeta / dbias sums in shared memory (RMSNorm without dbias has none)
-    switch (n) {
-      case 3: return (const void*)bwd_row_pf_kernel<T, 3, kRms, kBias, 1>;
-      case 4: return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 1>;
-      default: return nullptr;
+  } else if (kind == 7 && group == 128) {
+    if constexpr (!kRms || kBias) {
+      if (n == 3) return (const void*)bwd_row_pf_kernel<T, 3, kRms, kBias, 1, 128>;
     }
-  } else if (kind == 8 && !kRms && !kBias && n == 4) {
+  } else if (kind == 7) {
+    // dbeta / dbias sums in shared memory (RMSNorm without dbias has none)
+    if constexpr (!kRms || kBias) {
+      if (n == 3) return (const void*)bwd_row_pf_kernel<T, 3, kRms, kBias, 1>;
+      if (n == 4) return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 1>;
+    }
+  } else if (kind == 8 && n == 4) {
     // every column sum in shared memory (LayerNorm rows of four vectors)
-    return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 2>;
+    if constexpr (!kRms && !kBias) return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 2>;
   }
   return nullptr;
 }
