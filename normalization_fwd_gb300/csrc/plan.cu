@@ -47,14 +47,30 @@ inline Choice choose(int hidden, int vec_elems, bool vec) {
 // of 8 per lane, LayerNorm with dbias from 4).
 constexpr int kMaxAccFloats = 80;
 
-// A backward lane group whose accumulators (n * VEC floats per reduction:
-// dgamma; dbeta for LayerNorm; dbias) would not fit moves to a row group of
-// 64 or 128 threads (kind 3), the smallest that fits.
+// Backward lane groups: four vectors a lane, else three, five, two or one,
+// where the row splits exactly over 8, 16 or 32 lanes and the accumulators
+// (n * VEC floats per reduction: dgamma; dbeta for LayerNorm; dbias) fit.
+// A lane group whose accumulators would not fit, or whose lanes would hold
+// more than 40 floats of each input row (more than five 16-byte vectors of
+// a 16-bit type), moves to a row group of 64 or 128 threads (kind 3), the
+// smallest that fits. Measured at 268 MB per tensor, bf16, kernel alone:
+// 256 wide LayerNorm 127 us as 8 x 4 against 208 as 32 x 1 (RMSNorm 138
+// against 190); 512 wide LayerNorm 131 as 16 x 4 against 160 as 32 x 2;
+// 1536 wide RMSNorm 127 as a 64 x 3 row group against 139 as 32 x 6 lanes;
+// 2048 wide RMSNorm 137 as 64 x 4 against 149 as 32 x 8.
+constexpr int kMaxLaneRowFloats = 40;
 inline Choice bwd_choice(const Choice& c, int hidden, int vec_elems, bool rms, bool dbias) {
   if (c.kind != 0) return c;
   const int n_acc = 1 + (rms ? 0 : 1) + (dbias ? 1 : 0);
-  if (c.n * vec_elems * n_acc <= kMaxAccFloats) return c;
   const int V = hidden / vec_elems;
+  for (int n : {4, 3, 5, 2, 1}) {
+    if (V % n) continue;
+    const int lanes = V / n;
+    if ((lanes == 8 || lanes == 16 || lanes == 32) && n * vec_elems * n_acc <= kMaxAccFloats &&
+        n * vec_elems <= kMaxLaneRowFloats)
+      return {0, lanes, n};
+  }
+  if (c.n * vec_elems * n_acc <= kMaxAccFloats && c.n * vec_elems <= kMaxLaneRowFloats) return c;
   for (int g : {64, 128}) {
     int n = (V + g - 1) / g;
     if (n == 7) n = 8;
