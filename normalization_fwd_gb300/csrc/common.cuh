@@ -370,6 +370,22 @@ __device__ __forceinline__ float cta_sum_db_fit(float v, float (*red)[kMaxFitWar
   return t;
 }
 
+__device__ __forceinline__ float2 cta_sum2_db_fit(float2 v, float2 (*red)[kMaxFitWarps],
+                                                  int& parity) {
+  const int W = blockDim.x >> 5;
+  v = group_sum2<32>(v);
+  if ((threadIdx.x & 31) == 0) red[parity][threadIdx.x >> 5] = v;
+  __syncthreads();
+  float2 t = make_float2(0.f, 0.f);
+#pragma unroll 4
+  for (int i = 0; i < W; ++i) {
+    t.x += red[parity][i].x;
+    t.y += red[parity][i].y;
+  }
+  parity ^= 1;
+  return t;
+}
+
 // Max over the CTA with one barrier (double buffer and parity as above).
 template <int THREADS>
 __device__ __forceinline__ float cta_max_db(float v, float (*red)[THREADS / 32], int& parity) {

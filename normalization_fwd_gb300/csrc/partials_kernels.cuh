@@ -19,7 +19,8 @@
 //
 //  * fwdp_tile_kernel: rows of up to 256 16-byte vectors, a lane group of
 //    LANES lanes per row, one CTA per tile of 8 * (32 / LANES) rows.
-//  * fwdp_cta_kernel: longer rows, one CTA of 256 threads per row.
+//  * fwdp_cta_kernel: longer rows, one CTA per row, its size fitted to the
+//    row at launch.
 //  * fwdp_scalar_kernel: any width and alignment, one CTA per row.
 #pragma once
 
@@ -203,30 +204,31 @@ __global__ void __launch_bounds__(kBulkThreads) fwdp_tile_kernel(const PartialsA
   if (a.amax) partial_amax_commit<T>(a, amax_acc, red_amax);
 }
 
+// The CTA's size is fitted to the row at launch (blockDim.x, a whole number
+// of warps up to kMaxFitThreads).
 template <typename T, int N>
-__global__ void __launch_bounds__(kBulkThreads) fwdp_cta_kernel(const PartialsArgs a) {
+__global__ void __launch_bounds__(kMaxFitThreads) __maxnreg__(N <= 4 ? 48 : 80) fwdp_cta_kernel(const PartialsArgs a) {
   constexpr int VEC = Vec<T>::N;
-  __shared__ float2 red[2][kConsumerWarps];
-  __shared__ float red1[2][kConsumerWarps];
+  __shared__ float2 red[2][kMaxFitWarps];
+  __shared__ float red1[2][kMaxFitWarps];
   int parity1 = 0;
-  __shared__ unsigned red_amax[kConsumerWarps];
+  __shared__ unsigned red_amax[kMaxFitWarps];
+  const int nt = blockDim.x;
   const int64_t row = blockIdx.x;
   const int V = a.hidden / VEC;
   const T* x = static_cast<const T*>(a.x) + row * (int64_t)a.hidden;
   uint4 xr[N];
 #pragma unroll
   for (int k = 0; k < N; ++k) {
-    const int v = k * kBulkThreads + threadIdx.x;
+    const int v = k * nt + threadIdx.x;
     if (v < V) xr[k] = ld_vec(x + v * VEC);
   }
   int parity = 0;
-  const float2 sq = cta_sum2_db<kBulkThreads>(partial_first(a, row, threadIdx.x, kBulkThreads),
-                                              red, parity);
+  const float2 sq = cta_sum2_db_fit(partial_first(a, row, threadIdx.x, nt), red, parity);
   float Q = sq.y;
   if (a.kind == 1) {
     const float mean0 = a.rms ? 0.f : sq.x * a.inv_hidden;
-    Q = cta_sum_db<kBulkThreads>(partial_second(a, row, threadIdx.x, kBulkThreads, mean0),
-                                 red1, parity1);
+    Q = cta_sum_db_fit(partial_second(a, row, threadIdx.x, nt, mean0), red1, parity1);
   }
   const float2 st = partial_stats(a, sq.x, Q);
   if (threadIdx.x == 0) {
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(kBulkThreads) fwdp_cta_kernel(const PartialsAr
   T* yrow = static_cast<T*>(a.y) + row * (int64_t)a.hidden;
 #pragma unroll
   for (int k = 0; k < N; ++k) {
-    const int v = k * kBulkThreads + threadIdx.x;
+    const int v = k * nt + threadIdx.x;
     if (v < V) partial_store<T>(a, yrow, v, xr[k], st.x, st.y, amax_acc);
   }
   if (a.amax) partial_amax_commit<T>(a, amax_acc, red_amax);

@@ -448,15 +448,17 @@ cudaError_t bwd_launch(const BwdArgs& a, const Plan& p, void* dgamma, void* dbet
 template <typename T> cudaError_t softmax_plan(int64_t rows, int hidden, bool vec, Plan* p) {
   const Choice c = choose(hidden, Vec<T>::N, vec);
   const int smx_path = kernel_family(kFamilySoftmax);
-  if (smx_path == 0 && c.kind == 1) {
-    // Rows of more than 256 vectors: a CTA per one or two rows, from registers.
+  const int V = vec ? hidden / Vec<T>::N : 0;
+  if (smx_path == 0 && (c.kind == 1 || (c.kind == 0 && V > kFwdGroupMaxV))) {
+    // Longer rows: a row-fitted CTA per one or two rows, from registers.
+    const Fit f = cta_fit(V);
     p->bulk = false;
     p->kind = 5;
-    p->group = kBulkThreads;
-    p->n = bulk_cta_n(hidden, Vec<T>::N);
-    p->block = kBulkThreads;
+    p->group = f.threads;
+    p->n = f.n;
+    p->block = f.threads;
     p->smem = 0;
-    p->fn = Tables<T>::softmax(5, kBulkThreads, p->n);
+    p->fn = Tables<T>::softmax(5, f.threads, p->n);
     cudaError_t e = size_grid(p, 1);
     if (e != cudaSuccess) return e;
     const int64_t ctas = smx_cta_grid(rows, p->n);
@@ -465,18 +467,19 @@ template <typename T> cudaError_t softmax_plan(int64_t rows, int hidden, bool ve
     return cudaSuccess;
   }
   if (smx_path == 0 && c.kind == 0) {
-    // Lane groups of up to 4 vectors: rows straight into registers, one CTA
-    // per 8 * (32 / lanes) rows, as many CTAs as the rows need.
+    // Lane groups (the forward's choice of lanes): rows straight into
+    // registers, one CTA per 8 * (32 / lanes) rows, as many CTAs as needed.
+    const Choice g = fwd_group_choice(c, V);
     p->bulk = false;
     p->kind = 4;
-    p->group = c.group;
-    p->n = c.n;
+    p->group = g.group;
+    p->n = g.n;
     p->block = kBulkThreads;
     p->smem = 0;
-    p->fn = Tables<T>::softmax(4, c.group, c.n);
+    p->fn = Tables<T>::softmax(4, g.group, g.n);
     cudaError_t e = size_grid(p, 1);   // occupancy check and attributes
     if (e != cudaSuccess) return e;
-    const int64_t rpc = (int64_t)kConsumerWarps * (32 / c.group);
+    const int64_t rpc = (int64_t)kConsumerWarps * (32 / g.group);
     const int64_t ctas = (rows + rpc - 1) / rpc;
     if (ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
     p->grid = (int)ctas;
@@ -535,9 +538,11 @@ template <typename T> cudaError_t partials_plan(int64_t rows, int hidden, bool v
     const int64_t rpc = (int64_t)kConsumerWarps * (32 / c.group);
     ctas = (rows + rpc - 1) / rpc;
   } else if (c.kind == 1) {
+    const Fit f = cta_fit(hidden / Vec<T>::N);
     p->kind = 5;
-    p->group = kBulkThreads;
-    p->n = bulk_cta_n(hidden, Vec<T>::N);
+    p->group = f.threads;
+    p->n = f.n;
+    p->block = f.threads;
   } else {
     p->kind = 2;
     p->group = kScalarCta;

@@ -161,22 +161,23 @@ __global__ void __launch_bounds__(kBulkThreads, N <= 3 ? 6 : (N <= 4 ? 4 : 2))
                             [](float v) { return group_sum<LANES>(v); });
 }
 
-// CTA rows (all 256 threads on one row), with one barrier per row: each warp
+// CTA rows (all the CTA's threads on one row), with one barrier per row: each warp
 // takes the exponentials against its own max m_w and sums them to s_w; the
 // warps' (m_w, s_w) pairs meet in shared memory, where every warp forms the
 // row max M and s = sum_w s_w * exp(m_w - M); thread scale exp(m_w - M) / s
 // (all in log2 units: L = m * log2 e).
 // This is the online normalizer of Milakov and Gimelshein ("Online normalizer
-// calculation for softmax", 2018) applied across the eight warps. A warp
+// calculation for softmax", 2018) applied across the CTA's warps. A warp
 // whose entries are all -inf shifts by 0 instead (its e are 0 either way)
 // and contributes 0; a row that is all -inf stays NaN.
 template <typename T, int N>
 __device__ __forceinline__ void smx_row_cta_regs(const SmxArgs& a, int64_t row,
                                                  const uint4 (&raw)[N],
-                                                 float2 (*red)[kConsumerWarps], int& parity) {
+                                                 float2 (*red)[kMaxFitWarps], int& parity) {
   constexpr int VEC = Vec<T>::N;
   constexpr int P = VEC / 2;
   const int V = a.hidden / VEC;
+  const int nt = blockDim.x;
   const int t = threadIdx.x;
   const int lane = t & 31;
   T* y_row = static_cast<T*>(a.y) + row * (int64_t)a.hidden;
@@ -184,7 +185,7 @@ __device__ __forceinline__ void smx_row_cta_regs(const SmxArgs& a, int64_t row,
   RowMax<T> rm;
 #pragma unroll
   for (int k = 0; k < N; ++k)
-    if (k * kBulkThreads + t < V) rm.add(raw[k]);
+    if (k * nt + t < V) rm.add(raw[k]);
   // Lw: this warp's shift in log2 units, rounded once. The warps exchange Lw
   // itself, so the factor 2^(Lw - L) that moves a warp's e onto the row max
   // carries exactly the rounding its exponentials were taken with.
@@ -193,20 +194,23 @@ __device__ __forceinline__ void smx_row_cta_regs(const SmxArgs& a, int64_t row,
   float2 acc = splat2(0.f);
 #pragma unroll
   for (int k = 0; k < N; ++k) {
-    if (k * kBulkThreads + t < V) exp_vec<T>(raw[k], Lw == -INFINITY ? 0.f : -Lw, e[k], acc);
+    if (k * nt + t < V) exp_vec<T>(raw[k], Lw == -INFINITY ? 0.f : -Lw, e[k], acc);
   }
   const float sw = group_sum<32>(acc.x + acc.y);
   if (lane == 0) red[parity][t >> 5] = make_float2(Lw, sw);
   __syncthreads();
-  const float2 q = red[parity][lane & (kConsumerWarps - 1)];
+  // Lane w of each 16-lane half takes warp w's pair; lanes past the CTA's
+  // warps hold (-inf, 0), which change neither the max nor the sum.
+  const int w = lane & (kMaxFitWarps - 1);
+  const float2 q = w < (nt >> 5) ? red[parity][w] : make_float2(-INFINITY, 0.f);
   parity ^= 1;
-  const float L = group_max<kConsumerWarps>(q.x);
-  const float S = group_sum<kConsumerWarps>(q.y * exp2f(q.x - L));
+  const float L = group_max<kMaxFitWarps>(q.x);
+  const float S = group_sum<kMaxFitWarps>(q.y * exp2f(q.x - L));
   const float2 f = splat2(exp2f(Lw - L) * __frcp_rn(S));
 
 #pragma unroll
   for (int k = 0; k < N; ++k) {
-    const int i = k * kBulkThreads + t;
+    const int i = k * nt + t;
     if (i < V) {
       float2 o[P];
 #pragma unroll
@@ -218,12 +222,12 @@ __device__ __forceinline__ void smx_row_cta_regs(const SmxArgs& a, int64_t row,
 
 template <typename T, int N>
 __device__ __forceinline__ void smx_row_cta(const SmxArgs& a, int64_t row, uint32_t xrow,
-                                            float2 (*red)[kConsumerWarps], int& parity) {
+                                            float2 (*red)[kMaxFitWarps], int& parity) {
   const int V = a.hidden / Vec<T>::N;
   uint4 raw[N];
 #pragma unroll
   for (int k = 0; k < N; ++k) {
-    const int i = k * kBulkThreads + threadIdx.x;
+    const int i = k * (int)blockDim.x + threadIdx.x;
     if (i < V) raw[k] = lds_u4(xrow + i * 16);
   }
   smx_row_cta_regs<T, N>(a, row, raw, red, parity);
@@ -238,11 +242,12 @@ constexpr int kSmxRowsPerCta = N <= 4 ? 2 : 1;
 
 // Rows of more than 256 vectors straight from global memory into registers:
 // a CTA loads all of its rows' vectors at once, then finishes each row in
-// turn (as many CTAs as the rows need).
+// turn (as many CTAs as the rows need). The CTA's size is fitted to the row
+// at launch (blockDim.x, a whole number of warps up to kMaxFitThreads).
 template <typename T, int N>
-__global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 4 : 2) smx_reg_cta_kernel(const SmxArgs a) {
+__global__ void __launch_bounds__(kMaxFitThreads, N <= 4 ? 2 : 1) smx_reg_cta_kernel(const SmxArgs a) {
   constexpr int R = kSmxRowsPerCta<N>;
-  __shared__ float2 red[2][kConsumerWarps];
+  __shared__ float2 red[2][kMaxFitWarps];
   constexpr int VEC = Vec<T>::N;
   const int V = a.hidden / VEC;
   uint4 raw[R][N];
@@ -252,7 +257,7 @@ __global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 4 : 2) smx_reg_cta_kern
     const T* x = static_cast<const T*>(a.x) + row * (int64_t)a.hidden;
 #pragma unroll
     for (int k = 0; k < N; ++k) {
-      const int i = k * kBulkThreads + threadIdx.x;
+      const int i = k * (int)blockDim.x + threadIdx.x;
       if (row < a.rows && i < V) raw[r][k] = ld_vec(x + i * VEC);
     }
   }
@@ -305,7 +310,7 @@ template <typename T, int N>
 __global__ void __launch_bounds__(kBulkThreads, N <= 4 ? 3 : 2) smx_bulk_cta_kernel(const SmxArgs a,
                                                                         const BulkCfg c) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ float2 red[2][kConsumerWarps];
+  __shared__ float2 red[2][kMaxFitWarps];
   __shared__ int s_abort;
   __shared__ long long s_taken;
   const int H = a.hidden;
