@@ -57,12 +57,13 @@ def fwd_bwd_parity(lib, w, seed=0, x_override=None, **fwd_kw):
 
 
 # Hidden sizes that reach every family: warp exact fits (LANES x N), warp
-# with masked lanes, CTA per row (exact and masked), and the scalar kernel
-# (row width not a multiple of 16 bytes).
-HIDDEN_16BIT = [8, 56, 64, 128, 136, 200, 256, 320, 384, 512, 640, 768, 1000, 1024, 1280, 2048,
-                2056, 3000, 3072, 4096, 8192, 16384,    # vector paths
+# with masked lanes, CTA per row (exact and masked, at the CTA sizes fitted
+# to 1536 to 16384 wide), the backward's 64-thread and 128-thread row
+# groups, and the scalar kernel (row width not a multiple of 16 bytes).
+HIDDEN_16BIT = [8, 56, 64, 128, 136, 200, 256, 320, 384, 512, 640, 768, 1000, 1024, 1280, 1536,
+                2048, 2056, 2560, 3000, 3072, 4096, 5120, 6144, 8192, 16384,   # vector paths
                 1, 2, 3, 7, 100, 1001, 4100]            # scalar path
-HIDDEN_F32 = [4, 28, 64, 96, 384, 500, 768, 1024, 1028, 2048, 4096, 8192,
+HIDDEN_F32 = [4, 28, 64, 96, 384, 500, 768, 1024, 1028, 1536, 2048, 2560, 4096, 8192,
               1, 3, 7, 99, 1001]
 
 

@@ -38,6 +38,8 @@ CASES = [
     (_case("p_f32_513x384", "f32", 513, 384, W.LAYERNORM), 64),
     (_case("p_bf16_300x8192", "bf16", 300, 8192, W.LAYERNORM), 128),       # CTA per row, T = 64
     (_case("p_bf16_300x8192_rms", "bf16", 300, 8192, W.RMSNORM), 1000),
+    (_case("p_bf16_211x2560", "bf16", 211, 2560, W.LAYERNORM), 128),       # 64-thread CTA, 5 vectors
+    (_case("p_bf16_97x3000_rms", "bf16", 97, 3000, W.RMSNORM), 256),       # fitted CTA, idle slots
     (_case("p_bf16_257x1001", "bf16", 257, 1001, W.LAYERNORM), 128),       # scalar kernel
     (_case("p_f32_64x5", "f32", 64, 5, W.LAYERNORM), 2),
 ]

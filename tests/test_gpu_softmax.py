@@ -72,14 +72,16 @@ def check(got, x64, fmt, what):
 
 
 # (dtype, rows, hidden): lane groups of 8/16/32 with every N, the CTA-per-row
-# kernel, ragged last tiles, widths the vector path cannot take (scalar
-# kernel) and the largest widths of each path.
+# kernel at several CTA sizes, ragged last tiles, widths the vector path
+# cannot take (scalar kernel) and the largest widths of each path.
 SHAPES = [
     ("f32", 4096, 384), ("f32", 257, 4), ("f32", 1000, 40), ("f32", 333, 1000),
     ("f32", 37, 8192), ("f32", 50, 1025), ("f32", 9, 1),
     ("bf16", 1000, 384), ("bf16", 515, 8), ("bf16", 300, 24), ("bf16", 129, 2048),
     ("bf16", 77, 4096), ("bf16", 33, 16384), ("bf16", 100, 1000), ("bf16", 40, 8191),
     ("bf16", 41, 8192), ("bf16", 23, 6144),    # two rows per CTA with an odd row count
+    ("bf16", 515, 256), ("bf16", 129, 1536),   # 8 lanes x 4; a 64-thread CTA
+    ("bf16", 37, 2560), ("bf16", 31, 3072),    # row-fitted CTAs: 64 x 5, 96 x 4
     ("bf16", 17, 3),
     ("f16", 8192, 320), ("f16", 999, 640), ("f16", 601, 1280), ("f16", 65, 12288),
     ("f16", 31, 7),
