@@ -17,6 +17,8 @@
  * Returns LN_ERR_INVALID for any other value, leaving the choice unchanged.
  * The choice is process-wide and applies to calls planned after it returns;
  * change it only while no other thread calls into the library.
+ *
+ * ln_testing_plan (below) reports the launch a shape would get.
  */
 #ifndef NORMFUSE_TESTING_H
 #define NORMFUSE_TESTING_H
@@ -31,6 +33,34 @@ extern "C" {
 #define LN_TESTING_RING_KERNELS 1
 
 ln_status ln_testing_select_kernels(int forward, int backward, int softmax);
+
+/*
+ * The launch the library would plan for a call of this shape on the current
+ * device (16-byte aligned pointers assumed), so that a test can check which
+ * kernel layout a width gets. Nothing is launched or allocated.
+ *
+ * direction: LN_TESTING_PLAN_FORWARD (ln_fwd; option != 0: with a residual),
+ *   LN_TESTING_PLAN_BACKWARD (ln_bwd / ln_bwd_ex; option != 0: with dbias),
+ *   LN_TESTING_PLAN_SOFTMAX (ln_softmax_fwd; mode ignored),
+ *   LN_TESTING_PLAN_PARTIALS (ln_fwd_from_partials; option ignored).
+ * out: six ints, caller-owned: kernel kind (0 pipelined lane group, 1
+ *   pipelined CTA per row, 2 scalar, 3 pipelined row group, 4 lane group
+ *   from registers, 5 CTA per row from registers, 6 prefetching CTA-per-row
+ *   backward, 7 and 8 the same with column sums in shared memory), threads
+ *   per row (lanes or row group), 16-byte vectors per thread, threads per
+ *   CTA, CTAs, dynamic shared-memory bytes.
+ * Returns LN_ERR_NULL (out null), LN_ERR_UNSUPPORTED (dtype, mode or
+ * direction unknown), LN_ERR_SHAPE (rows < 1, or hidden outside what the
+ * entry point accepts), LN_ERR_CUDA (no usable device); out is written only
+ * on LN_OK.
+ */
+#define LN_TESTING_PLAN_FORWARD 0
+#define LN_TESTING_PLAN_BACKWARD 1
+#define LN_TESTING_PLAN_SOFTMAX 2
+#define LN_TESTING_PLAN_PARTIALS 3
+
+ln_status ln_testing_plan(int direction, int64_t rows, int64_t hidden, ln_dtype dtype,
+                          ln_mode mode, int option, int* out);
 
 #ifdef __cplusplus
 }

@@ -28,7 +28,7 @@ __all__ = [
     "load_library", "build_library", "ln_fwd", "ln_fwd_ex", "ln_bwd", "ln_bwd_ex",
     "ln_bwd_workspace_bytes",
     "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc",
-    "ln_testing_select_kernels", "exported_symbols", "ln_fwd_from_partials",
+    "ln_testing_select_kernels", "ln_testing_plan", "exported_symbols", "ln_fwd_from_partials",
     "LN_PARTIALS_SUM_SQ", "LN_PARTIALS_SUM_M2", "fused_norm_fwd_from_partials",
     "fused_norm_fwd", "fused_norm_bwd", "Workspace",
 ]
@@ -104,6 +104,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.ln_fwd_from_partials.restype = ci
         lib.ln_testing_select_kernels.argtypes = [ci, ci, ci]
         lib.ln_testing_select_kernels.restype = ci
+        lib.ln_testing_plan.argtypes = [ci, i64, i64, ci, ci, ci, ctypes.POINTER(ci)]
+        lib.ln_testing_plan.restype = ci
         _lib = lib
         return lib
 
@@ -112,7 +114,8 @@ def exported_symbols() -> list[str]:
     """Names of the C entry points this binding wraps."""
     return ["ln_fwd", "ln_fwd_ex", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes",
             "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc",
-            "ln_softmax_fwd", "ln_testing_select_kernels", "ln_fwd_from_partials"]
+            "ln_softmax_fwd", "ln_testing_select_kernels", "ln_fwd_from_partials",
+            "ln_testing_plan"]
 
 
 _FAMILY_CODES = {"default": 0, "ring": 1}
@@ -130,6 +133,29 @@ def ln_testing_select_kernels(forward="default", backward="default", softmax="de
     st = lib.ln_testing_select_kernels(*codes)
     if st:
         raise NormError(st, "ln_testing_select_kernels")
+
+
+_PLAN_DIRECTIONS = {"forward": 0, "backward": 1, "softmax": 2, "partials": 3}
+_PLAN_FIELDS = ("kind", "group", "n", "block", "grid", "smem")
+
+
+def ln_testing_plan(direction, rows, hidden, dtype, mode="layernorm", option=False) -> dict:
+    """Testing hook (include/normfuse_testing.h): the launch the library
+    would plan for this shape on the current device, as a dict of kind,
+    group, n, block, grid and smem. ``direction`` is "forward", "backward",
+    "softmax" or "partials"; ``option`` a residual (forward) or dbias
+    (backward)."""
+    lib = load_library()
+    try:
+        d = _PLAN_DIRECTIONS[direction]
+    except KeyError:
+        raise ValueError(f"unknown direction {direction!r}") from None
+    code = _DTYPE_CODES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    out = (ctypes.c_int * 6)()
+    st = lib.ln_testing_plan(d, int(rows), int(hidden), code, _mode(mode), int(bool(option)), out)
+    if st:
+        raise NormError(st, "ln_testing_plan")
+    return dict(zip(_PLAN_FIELDS, list(out)))
 
 
 def ln_status_string(status: int) -> str:

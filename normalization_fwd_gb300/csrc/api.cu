@@ -192,6 +192,42 @@ ln_status ln_testing_select_kernels(int forward, int backward, int softmax) {
   return LN_OK;
 }
 
+ln_status ln_testing_plan(int direction, int64_t rows, int64_t hidden, ln_dtype dtype,
+                          ln_mode mode, int option, int* out) {
+  if (out == nullptr) return LN_ERR_NULL;
+  if (dtype != LN_F32 && dtype != LN_BF16 && dtype != LN_F16) return LN_ERR_UNSUPPORTED;
+  if (direction < LN_TESTING_PLAN_FORWARD || direction > LN_TESTING_PLAN_PARTIALS)
+    return LN_ERR_UNSUPPORTED;
+  if (direction != LN_TESTING_PLAN_SOFTMAX && mode != LN_LAYERNORM && mode != LN_RMSNORM)
+    return LN_ERR_UNSUPPORTED;
+  if (rows < 1 || hidden < 1) return LN_ERR_SHAPE;
+  const size_t es = elem_size(dtype);
+  bool vec = (hidden * (int64_t)es) % 16 == 0;
+  if (hidden > max_hidden(dtype, vec)) {
+    if (!vec || hidden > max_hidden(dtype, false)) return LN_ERR_SHAPE;
+    vec = false;
+  }
+  const bool rms = mode == LN_RMSNORM;
+  Plan p;
+  cudaError_t e = by_dtype(dtype, [&](auto t) {
+    using T = decltype(t);
+    switch (direction) {
+      case LN_TESTING_PLAN_FORWARD:
+        return fwd_plan<T>(rows, (int)hidden, vec, option != 0, rms ? 1 : 2, &p);
+      case LN_TESTING_PLAN_BACKWARD:
+        return bwd_plan<T>(rows, (int)hidden, rms, option != 0, vec, &p);
+      case LN_TESTING_PLAN_SOFTMAX:
+        return softmax_plan<T>(rows, (int)hidden, vec, &p);
+      default:
+        return partials_plan<T>(rows, (int)hidden, vec, &p);
+    }
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int v[6] = {p.kind, p.group, p.n, p.block, p.grid, (int)p.smem};
+  for (int i = 0; i < 6; ++i) out[i] = v[i];
+  return LN_OK;
+}
+
 ln_status ln_device_error(cudaStream_t stream, unsigned* flags) {
   if (flags == nullptr) return LN_ERR_NULL;
   *flags = 0;

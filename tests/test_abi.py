@@ -44,7 +44,8 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["ln_fwd", "ln_fwd_ex", "ln_bwd", "ln_bwd_ex", "ln_bwd_workspace_bytes",
          "ln_status_string", "ln_last_cuda_error", "ln_device_error", "ln_bwd_noalloc",
-         "ln_softmax_fwd", "ln_testing_select_kernels", "ln_fwd_from_partials"])
+         "ln_softmax_fwd", "ln_testing_select_kernels", "ln_fwd_from_partials",
+         "ln_testing_plan"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -258,6 +259,18 @@ def test_kernel_family_hook_validates_on_host(lib):
         nf.ln_testing_select_kernels(forward="registers")
 
 
+def test_plan_hook_validates_on_host(lib):
+    out = (ctypes.c_int * 6)()
+    assert lib.ln_testing_plan(0, 16, 384, 1, 0, 1, None) == NULL
+    assert lib.ln_testing_plan(4, 16, 384, 1, 0, 1, out) == UNSUPPORTED
+    assert lib.ln_testing_plan(0, 16, 384, 7, 0, 1, out) == UNSUPPORTED
+    assert lib.ln_testing_plan(1, 16, 384, 1, 5, 0, out) == UNSUPPORTED
+    assert lib.ln_testing_plan(0, 0, 384, 1, 0, 1, out) == SHAPE
+    assert lib.ln_testing_plan(0, 16, 0, 1, 0, 1, out) == SHAPE
+    with pytest.raises(ValueError):
+        nf.ln_testing_plan("sideways", 16, 384, 1)
+
+
 def test_library_reads_no_environment():
     """Kernel choice depends on the arguments and the device only: no source
     of the library reads an environment variable."""
@@ -296,4 +309,6 @@ def test_cuda_errors_propagate_as_status_without_a_device(lib):
     assert lib.ln_last_cuda_error() != 0
     flags = ctypes.c_uint(7)
     assert lib.ln_device_error(None, ctypes.byref(flags)) == CUDA
+    out = (ctypes.c_int * 6)()
+    assert lib.ln_testing_plan(0, 16, 384, 1, 0, 1, out) == CUDA
     assert nf.ln_status_string(CUDA).startswith("LN_ERR_CUDA")
