@@ -37,8 +37,10 @@ def test_entries_are_near_the_algorithmic_bytes():
             w = bench.BENCH_WORKLOADS[workload]
             algo = {"ln_fwd": bench.fwd_bytes(w), "ln_bwd": bench.bwd_bytes(w)}
         for kernel, traffic in kernels.items():
+            # At most 1.05 of the minimum bytes (no wasted re-reads); the
+            # lower bound only catches a capture of the wrong launch.
             ratio = traffic / algo[kernel]
-            assert 0.6 <= ratio <= 1.3, (workload, kernel, ratio)
+            assert 0.6 <= ratio <= 1.05, (workload, kernel, ratio)
 
 
 def test_changed_sources_read_as_unmeasured(monkeypatch):
