@@ -232,8 +232,9 @@ inline cudaError_t size_grid(Plan* p, int64_t steps) {
 // memory as fp32.
 //
 // Forward: rows straight into registers with one CTA per row tile (kind 4,
-// lane groups) or per row (kind 5, rows of more than 256 vectors); the ring
-// family selects the bulk-copy ring kernels instead.
+// lane groups, up to kFwdGroupMaxV vectors) or per row (kind 5, the CTA
+// sized by cta_fit); the ring family selects the bulk-copy ring kernels
+// instead.
 //
 // Backward rows of more than 256 vectors run from registers with a CTA per
 // row when the accumulators (n * VEC floats per reduction: dgamma; dbeta for
