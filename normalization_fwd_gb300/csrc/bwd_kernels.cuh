@@ -688,17 +688,18 @@ __global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdA
 // registers is what lets rows of four vectors per thread keep both rows in
 // registers without spilling; the same sums in the same order as the
 // register form, one 16-byte shared load and store per two pairs and sum.
-template <typename T, int N, bool kRms, bool kBias, int kSmem = 0, int GT = kBulkThreads>
-__global__ void __launch_bounds__(kPfGroups * GT, kPfThreads / (kPfGroups * GT))
+template <typename T, int N, bool kRms, bool kBias, int kSmem = 0, int GT = kBulkThreads,
+          int G = kPfGroups>
+__global__ void __launch_bounds__(G * GT, G * GT <= 256 ? 2 : 1)
     bwd_row_pf_kernel(const BwdArgs a) {
   constexpr int VEC = Vec<T>::N;
   constexpr int P = VEC / 2;
   constexpr int Q = P / 2;   // float4 per vector of w
   extern __shared__ __align__(16) float4 w_s[];   // [N][Q][gt], then the kSmem slots
-  // Threads of a row group (GT: 256, or 128 for rows of up to 512 vectors)
-  // and of the CTA.
+  // Threads of a row group (GT: 256; 128 for rows of up to 512 vectors; 320
+  // to 512, one group per CTA, for rows of more than 1024) and of the CTA.
   constexpr int gt = GT;
-  constexpr int ct = kPfGroups * GT;
+  constexpr int ct = G * GT;
   // Shared-memory sums in order: dgamma (kSmem 2), dbeta (LayerNorm), dbias.
   constexpr bool kGS = kSmem == 2;
   constexpr bool kBS = kSmem >= 1 && !kRms;
@@ -734,7 +735,7 @@ __global__ void __launch_bounds__(kPfGroups * GT, kPfThreads / (kPfGroups * GT))
     for (int k = 0; k < N; ++k)
 #pragma unroll
       for (int q = 0; q < Q; ++q) acc_slot(which, k, q) = make_float4(0.f, 0.f, 0.f, 0.f);
-  __shared__ float2 red[kPfGroups][2][kConsumerWarps];
+  __shared__ float2 red[G][2][GT / 32];
   const int grp = threadIdx.x / gt;
   const int t = threadIdx.x % gt;
   const int H = a.hidden;
@@ -806,8 +807,8 @@ __global__ void __launch_bounds__(kPfGroups * GT, kPfThreads / (kPfGroups * GT))
     nr = a.rstd[row];
     if (!kRms) nm = a.mean[row];
   };
-  const int64_t first = (int64_t)blockIdx.x * kPfGroups + grp;
-  const int64_t stride = (int64_t)gridDim.x * kPfGroups;
+  const int64_t first = (int64_t)blockIdx.x * G + grp;
+  const int64_t stride = (int64_t)gridDim.x * G;
   if (first < a.rows) load_row(first);
   for (int64_t row = first; row < a.rows; row += stride) {
     uint4 dr[N], xr[N];
@@ -872,12 +873,13 @@ __global__ void __launch_bounds__(kPfGroups * GT, kPfThreads / (kPfGroups * GT))
     }
   }
   allow_dependent_launch();
-  // One partial row per CTA: group 1's sums go through shared memory (the
-  // staged w is no longer needed) and group 0 adds them to its own.
+  // One partial row per CTA: with two groups, group 1's sums go through
+  // shared memory (the staged w is no longer needed) and group 0 adds them
+  // to its own.
   float* ws = a.ws + (int64_t)blockIdx.x * a.ws_cols;
   auto put = [&](float2 (&acc)[N][P], int off) {
     __syncthreads();
-    if (grp == 1) {
+    if (G == 2 && grp == 1) {
 #pragma unroll
       for (int k = 0; k < N; ++k)
 #pragma unroll
@@ -894,16 +896,21 @@ __global__ void __launch_bounds__(kPfGroups * GT, kPfThreads / (kPfGroups * GT))
           float4* dst = reinterpret_cast<float4*>(ws + off + v * VEC);
 #pragma unroll
           for (int q = 0; q < Q; ++q) {
-            const float4 o = w_s[(k * Q + q) * gt + t];
-            const float2 lo = add2(acc[k][2 * q], make_float2(o.x, o.y));
-            const float2 hi = add2(acc[k][2 * q + 1], make_float2(o.z, o.w));
-            dst[q] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            if (G == 2) {
+              const float4 o = w_s[(k * Q + q) * gt + t];
+              const float2 lo = add2(acc[k][2 * q], make_float2(o.x, o.y));
+              const float2 hi = add2(acc[k][2 * q + 1], make_float2(o.z, o.w));
+              dst[q] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            } else {
+              dst[q] = make_float4(acc[k][2 * q].x, acc[k][2 * q].y, acc[k][2 * q + 1].x,
+                                   acc[k][2 * q + 1].y);
+            }
           }
         }
       }
     }
   };
-  // Shared-memory sums: group 0 adds group 1's slots (thread t + 256) to its
+  // Shared-memory sums: group 0 adds group 1's slots (thread t + gt) to its
   // own, after a barrier that orders the row loop's last shared stores.
   auto put_s = [&](int which, int off) {
     __syncthreads();
@@ -916,10 +923,14 @@ __global__ void __launch_bounds__(kPfGroups * GT, kPfThreads / (kPfGroups * GT))
 #pragma unroll
           for (int q = 0; q < Q; ++q) {
             const float4 m = acc_slot(which, k, q);
-            const float4 o = acc_s[((which * N + k) * Q + q) * ct + gt + t];
-            const float2 lo = add2(make_float2(m.x, m.y), make_float2(o.x, o.y));
-            const float2 hi = add2(make_float2(m.z, m.w), make_float2(o.z, o.w));
-            dst[q] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            if (G == 2) {
+              const float4 o = acc_s[((which * N + k) * Q + q) * ct + gt + t];
+              const float2 lo = add2(make_float2(m.x, m.y), make_float2(o.x, o.y));
+              const float2 hi = add2(make_float2(m.z, m.w), make_float2(o.z, o.w));
+              dst[q] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            } else {
+              dst[q] = m;
+            }
           }
         }
       }

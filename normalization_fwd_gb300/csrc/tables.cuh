@@ -110,6 +110,26 @@ const void* bwd_bulk_table_impl(int kind, int group, int n, bool exact) {
       case 4: return (const void*)bwd_row_cta_kernel<T, 4, kRms, kBias>;
       default: return nullptr;
     }
+  } else if (kind >= 6 && kind <= 8 && group > kBulkThreads) {
+    // rows of more than 1024 vectors: one row group of `group` threads per
+    // CTA, four vectors a thread
+    if (n != 4) return nullptr;
+#define NF_PF_WIDE(GTV)                                                                    \
+  if (group == GTV) {                                                                      \
+    if constexpr (kRms && !kBias) {                                                        \
+      if (kind == 6) return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 0, GTV, 1>;  \
+    } else if constexpr (!kRms && !kBias) {                                                \
+      if (kind == 8) return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 2, GTV, 1>;  \
+    } else {                                                                               \
+      if (kind == 7) return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 1, GTV, 1>;  \
+    }                                                                                      \
+    return nullptr;                                                                        \
+  }
+    NF_PF_WIDE(320)
+    NF_PF_WIDE(384)
+    NF_PF_WIDE(448)
+    NF_PF_WIDE(512)
+#undef NF_PF_WIDE
   } else if (kind == 6 && group == 128) {
     // two 128-thread row groups (RMSNorm rows of up to 512 vectors)
     if constexpr (kRms && !kBias) {

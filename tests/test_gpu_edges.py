@@ -147,11 +147,15 @@ def test_unaligned_pointers_use_scalar_path(cuda_lib, dtype):
 # registers allow) and the last steps are ragged: each n of the prefetching
 # kernel for both modes, with dbias, in each dtype, and the form that keeps
 # the dbeta / dbias sums in shared memory (8192-wide LayerNorm in 16-bit
-# types, 6144-wide LayerNorm and 8192-wide RMSNorm with dbias).
+# types, 6144-wide LayerNorm and 8192-wide RMSNorm with dbias), and the
+# one-group form for wider rows (9000 wide: idle slots in the last vector).
 WIDE = [("bf16", 2056, W.LAYERNORM), ("bf16", 4096, W.RMSNORM), ("bf16", 6144, W.LAYERNORM),
         ("bf16", 6144, W.RMSNORM), ("bf16", 8192, W.RMSNORM), ("bf16", 8192, W.LAYERNORM),
         ("f16", 3000, W.RMSNORM), ("f16", 8192, W.LAYERNORM), ("f32", 2048, W.LAYERNORM),
-        ("f32", 3072, W.RMSNORM)]
+        ("f32", 3072, W.RMSNORM),
+        # one row group per CTA for rows of more than 1024 vectors
+        ("bf16", 10240, W.RMSNORM), ("bf16", 12288, W.LAYERNORM), ("f16", 16384, W.RMSNORM),
+        ("bf16", 16384, W.LAYERNORM), ("f32", 8192, W.LAYERNORM), ("bf16", 9000, W.RMSNORM)]
 
 
 @pytest.mark.parametrize("dtype,hidden,mode", WIDE, ids=lambda v: str(v))

@@ -39,6 +39,9 @@ EXPECTED = [
     (("backward", 8192, "layernorm", False), (8, 256, 4, 512)),
     (("backward", 8192, "layernorm", True), (7, 256, 4, 512)),
     (("backward", 8192, "rmsnorm", True), (7, 256, 4, 512)),
+    (("backward", 12288, "layernorm", False), (8, 384, 4, 384)),  # one row group per CTA
+    (("backward", 16384, "rmsnorm", False), (6, 512, 4, 512)),
+    (("backward", 10240, "layernorm", True), (7, 320, 4, 320)),
     (("softmax", 384, "layernorm", False), (4, 16, 3, 256)),
     (("softmax", 256, "layernorm", False), (4, 8, 4, 256)),
     (("softmax", 2560, "layernorm", False), (5, 64, 5, 64)),
@@ -78,8 +81,8 @@ def test_every_width_is_covered_by_whole_warps(direction, dtype):
                 assert g * n >= V, (hidden, p)
             elif k == 5:          # row-fitted CTA
                 assert g == b and 64 <= b and b * n >= V and b * (n - 1) < V, (hidden, p)
-            elif k in (6, 7, 8):  # two row groups of g threads
-                assert b == 2 * g and g * n >= V, (hidden, p)
+            elif k in (6, 7, 8):  # one or two row groups of g threads
+                assert b in (g, 2 * g) and g * n >= V, (hidden, p)
             else:
                 assert k == 2, (hidden, p)
             if direction == "softmax":
