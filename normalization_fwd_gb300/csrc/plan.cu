@@ -291,20 +291,24 @@ inline size_t bwd_row_pf_smem(int n, int vec_elems, bool rms, bool dbias, int sm
 
 // Rows of more than 1024 vectors (wider than 8192 in 16-bit types, than 4096
 // in fp32): one row group per CTA of 320 to 512 threads (a multiple of 64,
-// the row at four vectors a thread) with the next row prefetched, the
-// sums placed as at 8192 wide: RMSNorm in registers (kind 6), LayerNorm in
-// shared memory (kind 8), with dbias dbeta / dbias in shared memory (kind
-// 7). Two rows of 40 to 64 KB each are in flight per SM. The ring kernel
-// these replace ran 12288-wide bf16 LayerNorm at 0.53 of the measured copy
-// rate and 16384-wide at 0.35 (RMSNorm 0.75 and 0.68).
+// the row at four vectors a thread) with the next row prefetched: RMSNorm
+// keeps its sums in registers (kind 6); with dbias, dbeta / dbias go to
+// shared memory (kind 7); LayerNorm without dbias keeps every sum in shared
+// memory (kind 8) up to 384-thread groups and dgamma in registers (kind 7)
+// from 448 (16384-wide bf16: 164.5 us as kind 7, 187.1 as kind 8;
+// 12288-wide: 178.3 as kind 7, 157.7 as kind 8). Two rows of 40 to 64 KB
+// each are in flight per SM. The ring kernel these replace ran 12288-wide
+// bf16 LayerNorm at 0.53 of the measured copy rate and 16384-wide at 0.35
+// (RMSNorm 0.75 and 0.68).
 constexpr int kWideMaxThreads = 512;
 inline int bwd_wide_threads(int V) {
   if (V <= 4 * kBulkThreads || V > 4 * kWideMaxThreads) return 0;
   return (V + 255) / 256 * 64;
 }
-inline int bwd_wide_kind(bool rms, bool dbias) {
+inline int bwd_wide_kind(bool rms, bool dbias, int threads) {
   if (rms && !dbias) return 6;
-  return (!rms && !dbias) ? 8 : 7;
+  if (!rms && !dbias) return threads >= 448 ? 7 : 8;
+  return 7;
 }
 
 // Rows of 257 to 512 vectors, where 256-thread row groups of two vectors a
@@ -333,7 +337,7 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
   if (bwd && vec && c.kind == 1 && !ring) {
     const int wt = bwd_wide_threads(hidden / Vec<T>::N);
     if (wt != 0) {
-      const int kind = bwd_wide_kind(rms, dbias);
+      const int kind = bwd_wide_kind(rms, dbias, wt);
       p->bulk = false;
       p->kind = kind;
       p->group = wt;

@@ -120,6 +120,9 @@ const void* bwd_bulk_table_impl(int kind, int group, int n, bool exact) {
       if (kind == 6) return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 0, GTV, 1>;  \
     } else if constexpr (!kRms && !kBias) {                                                \
       if (kind == 8) return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 2, GTV, 1>;  \
+      if constexpr (GTV >= 448) {                                                          \
+        if (kind == 7) return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 1, GTV, 1>; \
+      }                                                                                    \
     } else {                                                                               \
       if (kind == 7) return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 1, GTV, 1>;  \
     }                                                                                      \

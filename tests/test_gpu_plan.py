@@ -41,6 +41,7 @@ EXPECTED = [
     (("backward", 8192, "rmsnorm", True), (7, 256, 4, 512)),
     (("backward", 12288, "layernorm", False), (8, 384, 4, 384)),  # one row group per CTA
     (("backward", 16384, "rmsnorm", False), (6, 512, 4, 512)),
+    (("backward", 16384, "layernorm", False), (7, 512, 4, 512)),
     (("backward", 10240, "layernorm", True), (7, 320, 4, 320)),
     (("softmax", 384, "layernorm", False), (4, 16, 3, 256)),
     (("softmax", 256, "layernorm", False), (4, 8, 4, 256)),
