@@ -294,10 +294,11 @@ ln_status ln_bwd_workspace_bytes(int64_t rows, int64_t hidden, ln_dtype dtype,
  * - Limit: shapes whose partials need more than LN_NOALLOC_SCRATCH_BYTES
  *   return LN_ERR_SCRATCH_LIMIT before anything is enqueued
  *   (ln_bwd_workspace_bytes() gives a bound of the need: it also covers
- *   ln_bwd_ex's dbias columns, which this entry point does not compute). At 2 CTAs per SM on 152 SMs that is about
- *   hidden <= 6800 for LayerNorm and hidden <= 13700 for RMSNorm (rows of
- *   2049 to 8192 bf16 elements whose backward runs from registers at 3 CTAs
- *   per SM, up to 4096 for LayerNorm, also fit).
+ *   ln_bwd_ex's dbias columns, which this entry point does not compute).
+ *   The backward keeps one to three partial rows per SM for 16-byte
+ *   aligned rows (one for rows wider than 4096 16-bit elements), so on a
+ *   152-SM GB300 aligned LayerNorm rows fit up to about 13,700 elements
+ *   and RMSNorm rows up to the 16,384 maximum.
  * - Every call on a device shares the one array and nothing in it needs to
  *   start at zero (each call overwrites the partials it reads). Calls whose
  *   execution overlaps on the GPU (different streams, or different host
