@@ -106,34 +106,49 @@ int device_sm_count(int* sms) {
 struct SmemEntry {
   const void* fn;
   int device;
-  size_t allowed;     // dynamic bytes the kernel is opted in to
   size_t static_bytes;
+  size_t optin;       // the device's opt-in shared memory per block
 };
 std::vector<SmemEntry>& smem_cache() {
   static std::vector<SmemEntry> v;
   return v;
 }
 
+// Opt a kernel in to more than 48 KiB of dynamic shared memory. The opt-in
+// is a property of the kernel in the current context, which a
+// cudaDeviceReset or a caller's own context does not carry over, so it is
+// set on every call that needs it, always to the same value (everything
+// the device allows beyond the kernel's static shared memory): the call is
+// idempotent, and two threads planning different sizes never lower it
+// under each other's launch. Only the static size and the device limit,
+// which no context changes, are cached.
 int allow_dyn_smem(const void* fn, size_t smem) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return (int)e;
-  std::lock_guard<std::mutex> lk(g_mu);
-  SmemEntry* ent = nullptr;
-  for (SmemEntry& s : smem_cache())
-    if (s.fn == fn && s.device == dev) ent = &s;
-  if (ent == nullptr) {
-    cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, fn);
-    if (e != cudaSuccess) return (int)e;
-    smem_cache().push_back({fn, dev, 0, attr.sharedSizeBytes});
-    ent = &smem_cache().back();
+  size_t static_bytes = 0, optin = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const SmemEntry* ent = nullptr;
+    for (const SmemEntry& s : smem_cache())
+      if (s.fn == fn && s.device == dev) ent = &s;
+    if (ent == nullptr) {
+      cudaFuncAttributes attr;
+      e = cudaFuncGetAttributes(&attr, fn);
+      if (e != cudaSuccess) return (int)e;
+      int opt = 0;
+      e = cudaDeviceGetAttribute(&opt, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+      if (e != cudaSuccess) return (int)e;
+      smem_cache().push_back({fn, dev, attr.sharedSizeBytes, (size_t)opt});
+      ent = &smem_cache().back();
+    }
+    static_bytes = ent->static_bytes;
+    optin = ent->optin;
   }
-  if (smem <= ent->allowed || smem + ent->static_bytes <= 48 * 1024) return (int)cudaSuccess;
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return (int)e;
-  ent->allowed = smem;
-  return (int)cudaSuccess;
+  if (smem + static_bytes <= 48 * 1024) return (int)cudaSuccess;
+  if (smem + static_bytes > optin) return (int)cudaErrorInvalidValue;
+  return (int)cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)(optin - static_bytes));
 }
 
 int resident_blocks(const void* fn, int block, size_t smem, int* out) {
