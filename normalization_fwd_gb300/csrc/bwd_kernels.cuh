@@ -690,7 +690,7 @@ __global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdA
 // register form, one 16-byte shared load and store per two pairs and sum.
 template <typename T, int N, bool kRms, bool kBias, int kSmem = 0, int GT = kBulkThreads,
           int G = kPfGroups>
-__global__ void __launch_bounds__(G * GT, G * GT <= 256 ? 2 : 1)
+__global__ void __launch_bounds__(G * GT, G * GT < kPfThreads ? kPfThreads / (G * GT) : 1)
     bwd_row_pf_kernel(const BwdArgs a) {
   constexpr int VEC = Vec<T>::N;
   constexpr int P = VEC / 2;

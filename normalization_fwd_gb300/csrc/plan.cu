@@ -321,11 +321,26 @@ inline int bwd_wide_kind(bool rms, bool dbias, int threads) {
 // 123.1 against 130.0; LayerNorm 2560 141.3 against 176.6 (256 x 2, kind 6),
 // 3072 129.3 against 177.0. LayerNorm at 4096 stays on 256 x 2 (142.7 us;
 // 147.6 as 128 x 4 with every sum in shared memory).
-inline int bwd_small_group_kind(int V, bool rms, bool dbias) {
-  if (V <= 256 || V > 512) return 0;
-  const int n = (V + 127) / 128;
-  if (rms && !dbias) return 6;
-  return n == 3 ? 7 : 0;
+//
+// The same one size down for rows of 129 to 256 vectors (1032 to 2048 wide
+// in 16-bit types): two 64-thread row groups per CTA, four CTAs per SM.
+// Kernel alone, bf16: RMSNorm 1280 wide 128.2 us against 134.1 (32 x 5
+// lanes), 1536 123.0 against 127.5 (64 x 3 row-group ring), 2048 127.7
+// against 139.3 (64 x 4 ring); LayerNorm 1280 130.4 against 144.2, 1536
+// 124.9 against 138.9. LayerNorm at 2048 stays on the ring (129.0 against
+// 135.3 with every sum in shared memory).
+inline Choice bwd_small_group(int V, bool rms, bool dbias) {
+  int gt = 0;
+  if (V > 128 && V <= 256) {
+    gt = 64;
+  } else if (V > 256 && V <= 512) {
+    gt = 128;
+  } else {
+    return {0, 0, 0};
+  }
+  const int n = (V + gt - 1) / gt;
+  if (rms && !dbias) return {6, gt, n};
+  return n == 3 ? Choice{7, gt, n} : Choice{0, 0, 0};
 }
 constexpr int kRowsInFlightPf = 4;   // kind 6: two row groups per SM, two rows each
 
@@ -334,6 +349,19 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
                       int n_in, int n_params, Plan* p) {
   const Choice c = choose(hidden, Vec<T>::N, vec);
   const bool ring = kernel_family(bwd ? kFamilyBackward : kFamilyForward) == kFamilyRing;
+  if (bwd && vec && (c.kind == 0 || c.kind == 1) && !ring) {
+    const Choice sg = bwd_small_group(hidden / Vec<T>::N, rms, dbias);
+    if (sg.kind != 0) {
+      p->bulk = false;
+      p->kind = sg.kind;
+      p->group = sg.group;
+      p->n = sg.n;
+      p->block = kPfGroups * sg.group;
+      p->smem = bwd_row_pf_smem(sg.n, Vec<T>::N, rms, dbias, sg.kind - 6, sg.group);
+      p->fn = Tables<T>::bwd_bulk(p->kind, sg.group, sg.n, rms, dbias, false);
+      return size_grid(p, rows);
+    }
+  }
   if (bwd && vec && c.kind == 1 && !ring) {
     const int wt = bwd_wide_threads(hidden / Vec<T>::N);
     if (wt != 0) {
@@ -345,18 +373,6 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
       p->block = wt;
       p->smem = bwd_row_pf_smem(4, Vec<T>::N, rms, dbias, kind - 6, wt, 1);
       p->fn = Tables<T>::bwd_bulk(kind, wt, 4, rms, dbias, false);
-      return size_grid(p, rows);
-    }
-    const int sk = bwd_small_group_kind(hidden / Vec<T>::N, rms, dbias);
-    if (sk != 0) {
-      const int n = (hidden / Vec<T>::N + 127) / 128;
-      p->bulk = false;
-      p->kind = sk;
-      p->group = 128;
-      p->n = n;
-      p->block = kPfGroups * 128;
-      p->smem = bwd_row_pf_smem(n, Vec<T>::N, rms, dbias, sk - 6, 128);
-      p->fn = Tables<T>::bwd_bulk(p->kind, 128, n, rms, dbias, false);
       return size_grid(p, rows);
     }
     const int n = bulk_cta_n(hidden, Vec<T>::N);

@@ -133,11 +133,13 @@ const void* bwd_bulk_table_impl(int kind, int group, int n, bool exact) {
     NF_PF_WIDE(448)
     NF_PF_WIDE(512)
 #undef NF_PF_WIDE
-  } else if (kind == 6 && group == 128) {
-    // two 128-thread row groups (RMSNorm rows of up to 512 vectors)
+  } else if (kind == 6 && (group == 64 || group == 128)) {
+    // two 64- or 128-thread row groups (RMSNorm rows of up to 256 or 512 vectors)
     if constexpr (kRms && !kBias) {
-      if (n == 3) return (const void*)bwd_row_pf_kernel<T, 3, kRms, kBias, 0, 128>;
-      if (n == 4) return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 0, 128>;
+      if (group == 64 && n == 3) return (const void*)bwd_row_pf_kernel<T, 3, kRms, kBias, 0, 64>;
+      if (group == 64 && n == 4) return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 0, 64>;
+      if (group == 128 && n == 3) return (const void*)bwd_row_pf_kernel<T, 3, kRms, kBias, 0, 128>;
+      if (group == 128 && n == 4) return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias, 0, 128>;
     }
   } else if (kind == 6) {
     switch (n) {
@@ -146,9 +148,10 @@ const void* bwd_bulk_table_impl(int kind, int group, int n, bool exact) {
       case 4: return (const void*)bwd_row_pf_kernel<T, 4, kRms, kBias>;
       default: return nullptr;
     }
-  } else if (kind == 7 && group == 128) {
+  } else if (kind == 7 && (group == 64 || group == 128)) {
     if constexpr (!kRms || kBias) {
-      if (n == 3) return (const void*)bwd_row_pf_kernel<T, 3, kRms, kBias, 1, 128>;
+      if (group == 64 && n == 3) return (const void*)bwd_row_pf_kernel<T, 3, kRms, kBias, 1, 64>;
+      if (group == 128 && n == 3) return (const void*)bwd_row_pf_kernel<T, 3, kRms, kBias, 1, 128>;
     }
   } else if (kind == 7) {
     // dbeta / dbias sums in shared memory (RMSNorm without dbias has none)

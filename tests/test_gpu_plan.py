@@ -30,7 +30,10 @@ EXPECTED = [
     (("backward", 384, "layernorm", False), (0, 16, 3, 256)),   # the bench step's backward
     (("backward", 256, "layernorm", False), (0, 8, 4, 256)),
     (("backward", 512, "layernorm", False), (0, 16, 4, 256)),
-    (("backward", 1536, "rmsnorm", False), (3, 64, 3, 256)),
+    (("backward", 1536, "rmsnorm", False), (6, 64, 3, 128)),     # two 64-thread groups
+    (("backward", 1280, "layernorm", False), (7, 64, 3, 128)),
+    (("backward", 2048, "layernorm", False), (3, 64, 4, 256)),     # row-group ring
+    (("backward", 1024, "layernorm", False), (0, 32, 4, 256)),
     (("backward", 2560, "layernorm", False), (7, 128, 3, 256)),
     (("backward", 3072, "rmsnorm", False), (6, 128, 3, 256)),
     (("backward", 4096, "rmsnorm", False), (6, 128, 4, 256)),
