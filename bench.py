@@ -8,8 +8,12 @@ so no flush is needed between steps.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--no-e2e] [--no-cpu-baseline] [--no-clocks]
 
-``--workload softmax_bf16_576000x384`` (or ``softmax_bf16_16384x8192``) times
-the row softmax (ln_softmax_fwd) instead, with its own metric line.
+``--workload rms_fwd_bwd_bf16_16384x8192`` or
+``ln_fwd_bwd_fp8_dbias_bf16_576000x384`` time other forward + backward steps
+(the default line also carries the first under ``workloads``);
+``softmax_bf16_576000x384`` / ``softmax_bf16_16384x8192`` time the row softmax
+(ln_softmax_fwd) and ``partials_bf16_576000x384`` the normalize-from-partials
+step (ln_fwd_from_partials), each with its own metric line.
 
 Rank 0 prints one JSON line. Under torchrun (N > 1) every rank runs its own
 replica of the workload on its own GPU (the block has no cross-row exchange),
