@@ -36,8 +36,15 @@ def _with_partials(inp):
     return inp
 
 
-@pytest.mark.parametrize("base", [W.BENCH_LN_BF16_576000x384, W.BENCH_RMS_BF16_16384x8192],
-                         ids=lambda w: w.name)
+# The two bench shapes, and widths that take the other backward layouts: two
+# 64- or 128-thread row groups per CTA (1536, 2560), one 384-thread group
+# per CTA with every column sum in more than 48 KiB of shared memory (12288).
+@pytest.mark.parametrize("base", [
+    W.BENCH_LN_BF16_576000x384, W.BENCH_RMS_BF16_16384x8192,
+    W.BENCH_RMS_BF16_16384x8192.with_(name="rms_bf16_x1536", hidden=1536),
+    W.BENCH_LN_BF16_576000x384.with_(name="ln_bf16_x2560", hidden=2560),
+    W.BENCH_LN_BF16_576000x384.with_(name="ln_bf16_x12288", hidden=12288),
+], ids=lambda w: w.name)
 def test_fwd_bwd_softmax_replay_in_a_cuda_graph(cuda_lib, base):
     nf = cuda_lib
     w = base.with_(rows=4099 if base.hidden <= 1024 else 257)
