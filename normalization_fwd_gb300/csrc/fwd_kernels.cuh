@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kBulkThreads, N <= 3 ? 4 : 2) fwd_tile_kernel(
 // per SM than a fixed 256 threads that leave vector slots idle (2560 bf16,
 // 52428 rows: 157 us as 64 x 5 against 228 as 256 x 2).
 template <typename T, int N>
-__global__ void __launch_bounds__(kMaxFitThreads, N <= 4 ? 2 : 1) fwd_tile_cta_kernel(const FwdArgs a) {
+__global__ void __launch_bounds__(kMaxFitThreads) __maxnreg__(N <= 4 ? 56 : 128) fwd_tile_cta_kernel(const FwdArgs a) {
   constexpr int VEC = Vec<T>::N;
   __shared__ float red[2][kMaxFitWarps];
   __shared__ unsigned red_amax[kMaxFitWarps];
