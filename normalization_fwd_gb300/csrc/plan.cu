@@ -362,6 +362,23 @@ cudaError_t make_plan(int64_t rows, int hidden, bool vec, bool bwd, bool rms, bo
       return size_grid(p, rows);
     }
   }
+  if (bwd && vec && c.kind == 1 && !ring && !rms && !dbias && Vec<T>::N == 8 &&
+      hidden / Vec<T>::N == 1024) {
+    // 16-bit LayerNorm rows of 1024 vectors (8192 wide): one 512-thread row
+    // group per CTA, two vectors a thread, dgamma in registers and dbeta in
+    // shared memory (16384 x 8192, with the finalize, back to back: fp16
+    // 154.5 us against 160.7 for two 256-thread groups of four vectors with
+    // every sum in shared memory, bf16 within 2 us either way; at 6152 to
+    // 8184 wide, where 512 x 2 leaves slots idle, the two groups stay).
+    p->bulk = false;
+    p->kind = 7;
+    p->group = 512;
+    p->n = 2;
+    p->block = 512;
+    p->smem = bwd_row_pf_smem(2, Vec<T>::N, rms, dbias, 1, 512, 1);
+    p->fn = Tables<T>::bwd_bulk(7, 512, 2, rms, dbias, false);
+    return size_grid(p, rows);
+  }
   if (bwd && vec && c.kind == 1 && !ring) {
     const int wt = bwd_wide_threads(hidden / Vec<T>::N);
     if (wt != 0) {

@@ -111,8 +111,13 @@ const void* bwd_bulk_table_impl(int kind, int group, int n, bool exact) {
       default: return nullptr;
     }
   } else if (kind >= 6 && kind <= 8 && group > kBulkThreads) {
-    // rows of more than 1024 vectors: one row group of `group` threads per
-    // CTA, four vectors a thread
+    // one row group of `group` threads per CTA: 16-bit LayerNorm rows of
+    // exactly 1024 vectors at two vectors a thread, rows of more than 1024
+    // vectors at four
+    if constexpr (!kRms && !kBias && sizeof(T) == 2) {
+      if (kind == 7 && group == 512 && n == 2)
+        return (const void*)bwd_row_pf_kernel<T, 2, kRms, kBias, 1, 512, 1>;
+    }
     if (n != 4) return nullptr;
 #define NF_PF_WIDE(GTV)                                                                    \
   if (group == GTV) {                                                                      \

@@ -39,7 +39,8 @@ EXPECTED = [
     (("backward", 4096, "rmsnorm", False), (6, 128, 4, 256)),
     (("backward", 6144, "layernorm", False), (6, 256, 3, 512)),
     (("backward", 8192, "rmsnorm", False), (6, 256, 4, 512)),  # the second gate shape
-    (("backward", 8192, "layernorm", False), (8, 256, 4, 512)),
+    (("backward", 8192, "layernorm", False), (7, 512, 2, 512)),   # one 512-thread group
+    (("backward", 7168, "layernorm", False), (8, 256, 4, 512)),
     (("backward", 8192, "layernorm", True), (7, 256, 4, 512)),
     (("backward", 8192, "rmsnorm", True), (7, 256, 4, 512)),
     (("backward", 12288, "layernorm", False), (8, 384, 4, 384)),  # one row group per CTA
