@@ -666,18 +666,20 @@ __global__ void __launch_bounds__(kBulkThreads, 3) bwd_row_cta_kernel(const BwdA
 }
 
 // The same rows with the next row's dy and x_sum (and statistics) loaded
-// into registers while this row is worked on. A CTA holds two row groups of
-// GT threads (256; 128 for rows of up to 512 vectors, two CTAs per SM);
-// group g of CTA b takes rows 2b + g, 2b + g + 2G, ... (G CTAs), so each
-// CTA keeps four rows in flight (two groups, two rows each).
+// into registers while this row is worked on. A CTA holds G row groups of
+// GT threads: two groups of 256, or of 128 or 64 for rows of up to 512 or
+// 256 vectors (two or four CTAs per SM); one group of 320 to 512 for wider
+// rows (and for 16-bit LayerNorm rows of 1024 vectors, at two vectors a
+// thread). Group g of CTA b takes rows G b + g, G b + g + G C, ... (C
+// CTAs), so each group keeps two rows in flight.
 // Each group sums its row behind a named barrier of its own threads, so the
 // groups never wait for each other inside the row loop. w = gamma (+1 for
 // zero-centered gamma) is staged once per kernel in shared memory as fp32
 // ([k][pair of float2][thread] float4: no bank conflicts), which saves the
-// per-row unpacking of gamma. At the end the two groups' column sums are
-// added (group 0's plus group 1's) through shared memory, so the CTA writes
-// one partial row: half as many partials for the finalize to read as two
-// CTAs per SM would leave. Per-row results are those of bwd_row_cta_kernel
+// per-row unpacking of gamma. At the end two groups' column sums are added
+// (group 0's plus group 1's) through shared memory, so the CTA writes one
+// partial row: half as many partials for the finalize to read as two
+// single-group CTAs would leave. Per-row results are those of bwd_row_cta_kernel
 // (the same operations in the same order). Taken when the accumulators and
 // both rows fit in registers (the planner's bwd_row_pf_fits).
 //
