@@ -1,6 +1,7 @@
 """GPU parity on edge cases: every kernel family and lane layout, ragged row
 counts, empty inputs, optional operands switched off, unaligned pointers
-(scalar path), determinism, non-default streams and NaN propagation in amax.
+(scalar path), determinism, non-default streams, NaN propagation in amax,
+zero-variance rows and rows whose mean is large against their spread.
 """
 
 import numpy as np
@@ -252,3 +253,80 @@ def test_overlapping_output_is_rejected(cuda_lib):
     g = torch.ones(384, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(nf.NormError, match="INVALID"):
         nf.ln_fwd(x, None, None, g, None, 1e-5, "layernorm", False, None, x, None, None, None)
+
+
+# Widths that take the lane-group, CTA-per-row and scalar forward kernels.
+DEGENERATE_WIDTHS = [384, 8192, 1001]
+ZERO_VAR_CONSTS = [0.0, 1.5, -3.25, 1000.0, 0.30078125, -0.0078125]
+
+
+@pytest.mark.parametrize("mode", [W.LAYERNORM, W.RMSNORM])
+@pytest.mark.parametrize("hidden", DEGENERATE_WIDTHS)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_zero_variance_rows(cuda_lib, dtype, hidden, mode):
+    """Rows of one repeated value (LayerNorm: variance exactly 0) and all-zero
+    rows (RMSNorm: mean square exactly 0), so rstd = 1/sqrt(eps). The values
+    carry few significant bits, so the fp32 row sum and the division that
+    gives the mean are exact: LayerNorm's mean is the value itself and y is
+    beta bit for bit; RMSNorm's y of a zero row is 0. Everything else,
+    including the backward of these rows (xhat = 0, dx = rstd (g - mean g)),
+    is held to the oracle.
+
+    fp32 dx: the 2e-5 bound is an absolute one for rows whose dx terms are
+    O(1); a zero-variance row's terms are rstd * |dy w| with rstd ~ 316, and
+    fp32 carries ~1e-7 of them, so on those rows the bound is taken relative
+    to that scale (2e-5 * rstd * max |dy w|); the other rows keep the plain
+    bound."""
+    w = wl(dtype, 24, hidden, mode, bias_std=None, residual_std=None)
+    inp = make_inputs(w, seed=9)
+    x = inp["x"].clone()
+    rows = [2 * i for i in range(len(ZERO_VAR_CONSTS))]
+    other = [r for r in range(w.rows) if r not in rows]
+    for r, c in zip(rows, ZERO_VAR_CONSTS):
+        x[r] = c if mode == W.LAYERNORM else 0.0
+    fwd_bwd_parity(cuda_lib, w.with_(backward=False), seed=9, x_override=x)
+    got = gpu_fwd(cuda_lib, w, inp, x_override=x)
+    y = got["y"][rows]
+    if mode == W.LAYERNORM:
+        assert torch.equal(y, inp["beta"].expand_as(y)), "y of a constant row must be beta"
+        assert got["mean"][rows].tolist() == [float(x[r, 0]) for r in rows]
+    else:
+        assert (y == 0).all(), "y of a zero row must be 0"
+    eps32 = np.float32(w.eps)
+    want = np.float32(1.0) / np.sqrt(eps32, dtype=np.float32)
+    check_rel(as_f64(got["rstd"][rows]), np.full(len(rows), float(want)), 1e-6, "rstd")
+
+    # Backward on the oracle's forward outputs.
+    ref = oracle_fwd(w, inp, x_override=x)
+    dt = W.TORCH_DTYPES[w.dtype]
+    x_sum = torch.from_numpy(ref["sum"]).to(dt)
+    mean = None if ref["mean"] is None else torch.from_numpy(ref["mean"]).float()
+    rstd = torch.from_numpy(ref["rstd"]).float()
+    bref = oracle_bwd_rows(w, inp["dy"], x_sum, inp["gamma"], mean, rstd, slice(None))
+    bgot = gpu_bwd(cuda_lib, w, inp["dy"], x_sum, inp["gamma"], mean, rstd)
+    assert bgot["guards_ok"]
+    dx = as_f64(bgot["dx"])
+    scale = dx_row_scale(as_f64(inp["dy"]), as_f64(inp["gamma"]), as_f64(rstd),
+                         w.zero_centered_gamma)
+    if dtype == "f32":
+        check_elementwise(dx[other], bref["dx_exact"][other], "f32", "dx")
+        err = np.abs(dx[rows] - bref["dx_exact"][rows]).max(axis=1)
+        assert (err <= 2e-5 * np.maximum(1.0, scale[rows])).all(), (err, scale[rows])
+    else:
+        check_elementwise(dx, bref["dx_exact"], dtype, "dx", scale_rows=scale)
+    check_rel_l2(as_f64(bgot["dgamma"]), bref["dgamma"], 1e-4, "dgamma")
+    if bref["dbeta"] is not None:
+        check_rel_l2(as_f64(bgot["dbeta"]), bref["dbeta"], 1e-4, "dbeta")
+
+
+@pytest.mark.parametrize("hidden", DEGENERATE_WIDTHS)
+@pytest.mark.parametrize("dtype,offset", [("f32", 16.0), ("bf16", 64.0), ("f16", 100.0)])
+def test_rows_with_a_large_mean(cuda_lib, dtype, offset, hidden):
+    """s = offset + N(0, 1): the variance is 1e-2 to 1e-4 of the mean square,
+    where a one-pass E[s^2] - E[s]^2 in fp32 loses enough digits to miss the
+    1e-5 rstd bound. The centred second pass keeps every output within the
+    parity tolerances."""
+    w = wl(dtype, 37, hidden, W.LAYERNORM, bias_std=None, residual_std=None, x_std=1.0)
+    inp = make_inputs(w, seed=10)
+    x = (inp["x"].double() + offset).to(inp["x"].dtype)
+    fwd_bwd_parity(cuda_lib, w, seed=10, x_override=x)
