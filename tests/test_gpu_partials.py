@@ -123,3 +123,21 @@ def test_from_partials_zero_rows_and_one_tile(cuda_lib):
     for tile in (384, 5000):    # one tile either way
         got, ref = run_partials(cuda_lib, w, tile, "sum_m2", inp)
         check_elementwise(as_f64(got["y"]), ref["y_exact"], w.dtype, "y")
+
+
+@pytest.mark.parametrize("hidden,tile", [(384, 128), (8192, 128), (1001, 100)])
+def test_from_partials_m2_with_a_large_mean(cuda_lib, hidden, tile):
+    """(Σ, M2) partials of rows s = 64 + N(0, 1), the variance ~1e-4 of the
+    mean square: the parallel-variance combination takes no difference of
+    large sums, so every output stays within the parity tolerances (the
+    (Σ, Σ²) form's Q/H - mean² in fp32 would lose most of the variance's
+    digits on such rows)."""
+    w = _case(f"p_bf16_200x{hidden}_offset", "bf16", 200, hidden, W.LAYERNORM)
+    inp = make_inputs(w, seed=41)
+    inp = dict(inp, x=(inp["x"].double() + 64.0).to(torch.bfloat16))
+    got, ref = run_partials(cuda_lib, w, tile, "sum_m2", inp)
+    assert got["guards_ok"]
+    check_elementwise(as_f64(got["y"]), ref["y_exact"], w.dtype, "y", max_floored=1e-3)
+    check_rel(as_f64(got["rstd"]), ref["rstd_exact"], 1e-5, "rstd")
+    check_mean(as_f64(got["mean"]), ref["mean_exact"], as_f64(inp["x"]))
+    assert amax_bits_got(got["amax"]) == amax_bits_of(got["y"])
