@@ -13,7 +13,13 @@ so no flush is needed between steps.
 (the default line also carries the first under ``workloads``);
 ``softmax_bf16_576000x384`` / ``softmax_bf16_16384x8192`` time the row softmax
 (ln_softmax_fwd) and ``partials_bf16_576000x384`` the normalize-from-partials
-step (ln_fwd_from_partials), each with its own metric line.
+step (ln_fwd_from_partials), each with its own metric line. The other
+configurations the block is checked on have lines of their own too:
+``ln_f32_4096x384`` (fwd + bwd), ``bwd_ln_bf16_576000x384`` and
+``bwd_rms_bf16_576000x384`` (the backward alone), ``fwd_amax_bf16_32768x768``
+(the forward alone) and ``unet_ln_f16_8192x{320,640,1280}`` (fwd + bwd);
+those whose buffers fit in L2 cycle through enough copies of them that no
+step reads its inputs from L2.
 
 Rank 0 prints one JSON line. Under torchrun (N > 1) every rank runs its own
 replica of the workload on its own GPU (the block has no cross-row exchange),
@@ -55,6 +61,18 @@ PARTIALS_WORKLOADS = {W.PARTIALS_BF16_576000x384.name: W.PARTIALS_BF16_576000x38
 # The row softmax is measured on its own workloads (its own metric line).
 SOFTMAX_METRIC = "softmax rows/s and achieved HBM GB/s (one read of x, one write of y)"
 SOFTMAX_WORKLOADS = {w.name: w for w in (W.SMX_BF16_576000x384, W.SMX_BF16_16384x8192)}
+# The other configurations the block is checked on, each timed on its own
+# line: the fp32 4096 x 384 LayerNorm step, the 576000 x 384 backward alone
+# (LayerNorm and RMSNorm, no residual; its statistics come from one untimed
+# forward), the 32768 x 768 fused add + LayerNorm + amax forward alone, and
+# the three fp16 UNet widths. Buffers that fit in L2 are rotated
+# (rotation_copies), so every timed step reads its inputs from HBM.
+CONFIG_METRIC = ("rows/s and achieved HBM GB/s of one configuration's calls (forward, backward "
+                 "or both)")
+CONFIG_WORKLOADS = {w.name: w for w in (W.LN_F32_4096x384, W.BWD_BF16_576000x384_LN,
+                                        W.BWD_BF16_576000x384_RMS, W.FWD_AMAX_BF16_32768x768,
+                                        *W.UNET_F16.values())}
+L2_BYTES_FALLBACK = 129_000_000
 
 
 def is_softmax(w) -> bool:
@@ -103,6 +121,26 @@ def partials_bytes(w, tile_cols) -> int:
 def softmax_bytes(w) -> int:
     """Minimal HBM bytes of one ln_softmax_fwd: x read once, y written once."""
     return 2 * w.rows * w.hidden * elem_bytes(w)
+
+
+def step_bytes(w) -> int:
+    """Minimal HBM bytes of one timed step: the calls the workload makes."""
+    return (fwd_bytes(w) if w.forward else 0) + (bwd_bytes(w) if w.backward else 0)
+
+
+def rotation_copies(w, l2_bytes: int) -> int:
+    """Buffer sets a timed loop cycles through: one when every [rows, hidden]
+    tensor is larger than L2; otherwise enough sets that a pass over them
+    moves at least three times the L2's bytes, so the inputs a step reads
+    were last touched three L2s of traffic earlier (evicted, not L2 hits)."""
+    if w.rows * w.hidden * elem_bytes(w) > l2_bytes:
+        return 1
+    return max(2, -(-3 * l2_bytes // step_bytes(w)))
+
+
+def l2_bytes(device) -> int:
+    props = torch.cuda.get_device_properties(device)
+    return int(getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK)
 
 
 # ---------------------------------------------------------------- clocks
@@ -281,7 +319,10 @@ def ncu_traffic(workload: str, kernel: str):
 
 
 class Step:
-    """Device buffers and the two C-ABI calls of one fused fwd + bwd step."""
+    """Device buffers and the C-ABI calls of one step: ln_fwd then ln_bwd,
+    or only the one the workload has (w.forward / w.backward). A backward-only
+    workload (no bias, no residual: the backward's x_sum is x itself) gets
+    its statistics from one untimed ln_fwd here, as inputs."""
 
     def __init__(self, nf, w, inp, device):
         self.nf, self.w = nf, w
@@ -291,24 +332,37 @@ class Step:
         dt = W.TORCH_DTYPES[w.dtype]
         self.rms = w.mode == W.RMSNORM
         f32 = dict(dtype=torch.float32, device=device)
-        self.sum = torch.empty(R, H, dtype=dt, device=device)
-        self.y = torch.empty(R, H, dtype=dt, device=device)
+        if not w.forward and (w.bias_std is not None or w.residual_std is not None):
+            raise ValueError(f"{w.name}: a backward-only step takes x as its sum (no add)")
+        self.sum = torch.empty(R, H, dtype=dt, device=device) if w.forward else g["x"]
+        self.y = torch.empty(R, H, dtype=dt, device=device) if w.forward else None
         self.mean = None if self.rms else torch.empty(R, **f32)
         self.rstd = torch.empty(R, **f32)
-        self.amax = torch.empty(1, **f32) if w.amax else None
-        self.dx = torch.empty(R, H, dtype=dt, device=device)
-        self.dgamma = torch.empty(H, **f32)
-        self.dbeta = None if self.rms else torch.empty(H, **f32)
-        self.dbias = torch.empty(H, **f32) if w.dbias else None
+        self.amax = torch.empty(1, **f32) if (w.amax and w.forward) else None
+        bwd = w.backward
+        self.dx = torch.empty(R, H, dtype=dt, device=device) if bwd else None
+        self.dgamma = torch.empty(H, **f32) if bwd else None
+        self.dbeta = None if (self.rms or not bwd) else torch.empty(H, **f32)
+        self.dbias = torch.empty(H, **f32) if (w.dbias and bwd) else None
         # FP8 copy of y with a per-tensor scale (delayed scaling: 448 over an
         # amax of an earlier step; a fixed value here)
         self.y_fp8 = torch.empty(R, H, dtype=torch.uint8, device=device) if w.fp8_out else None
         self.fp8_scale = torch.full((1,), 64.0, **f32) if w.fp8_out else None
-        need = nf.ln_bwd_workspace_bytes(R, H, dt, w.mode)
-        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+        self.ws = None
+        if bwd:
+            need = nf.ln_bwd_workspace_bytes(R, H, dt, w.mode)
+            self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+        if not w.forward:
+            y = torch.empty(R, H, dtype=dt, device=device)
+            nf.ln_fwd(g["x"], None, None, g["gamma"], g["beta"], w.eps, w.mode,
+                      w.zero_centered_gamma, None, y, self.mean, self.rstd, None)
+            torch.cuda.synchronize(device)
+            del y
 
     def fwd(self, stream):
         g, w = self.inp, self.w
+        if not w.forward:
+            return
         if w.fp8_out:
             self.nf.ln_fwd_ex(g["x"], g["bias"], g["residual"], g["gamma"], g["beta"], w.eps,
                               w.mode, w.zero_centered_gamma, self.sum, self.y, self.mean,
@@ -320,6 +374,8 @@ class Step:
 
     def bwd(self, stream):
         g, w = self.inp, self.w
+        if not w.backward:
+            return
         if w.dbias:
             self.nf.ln_bwd_ex(g["dy"], self.sum, g["gamma"], self.mean, self.rstd, self.dx,
                               self.dgamma, self.dbeta, self.dbias, stream, mode=w.mode,
@@ -334,14 +390,44 @@ class Step:
         self.bwd(stream)
 
     def h2d_tensors(self):
-        return [(k, self.inp[k]) for k in ("x", "residual", "bias", "gamma", "beta", "dy")
-                if self.inp[k] is not None]
+        ins = [(k, self.inp[k]) for k in ("x", "residual", "bias", "gamma", "beta", "dy")
+               if self.inp[k] is not None]
+        if not self.w.forward:   # the statistics are inputs of a backward-only step
+            ins += [(k, t) for k, t in (("mean", self.mean), ("rstd", self.rstd))
+                    if t is not None]
+        return ins
 
     def d2h_tensors(self):
-        out = [("sum", self.sum), ("y", self.y), ("mean", self.mean), ("rstd", self.rstd),
-               ("amax", self.amax), ("dx", self.dx), ("dgamma", self.dgamma),
-               ("dbeta", self.dbeta), ("dbias", self.dbias), ("y_fp8", self.y_fp8)]
+        out = [("dx", self.dx), ("dgamma", self.dgamma), ("dbeta", self.dbeta),
+               ("dbias", self.dbias)]
+        if self.w.forward:
+            out = [("sum", self.sum), ("y", self.y), ("mean", self.mean), ("rstd", self.rstd),
+                   ("amax", self.amax), ("y_fp8", self.y_fp8)] + out
         return [(k, t) for k, t in out if t is not None]
+
+    def launches(self) -> int:
+        """Kernels of this library one step launches (the backward's main
+        kernel and its finalize)."""
+        return (1 if self.w.forward else 0) + (2 if self.w.backward else 0)
+
+
+class RotatingStep:
+    """`copies` Steps over their own buffers, used in turn (step i on set
+    i mod copies), so buffers that would fit in L2 are not re-read from it."""
+
+    def __init__(self, nf, w, inp, device, copies):
+        self.steps = [Step(nf, w, inp, device) for _ in range(copies)]
+        self.i = 0
+
+    def fwd(self, stream):
+        self.steps[self.i].fwd(stream)
+
+    def bwd(self, stream):
+        self.steps[self.i].bwd(stream)
+        self.i = (self.i + 1) % len(self.steps)
+
+    def launches(self) -> int:
+        return self.steps[0].launches()
 
 
 def producer_partials(x, tile_cols):
@@ -439,7 +525,9 @@ def nbytes(t) -> int:
 
 # ---------------------------------------------------------------- oracle timing
 def oracle_step(w, inp, rows):
-    """One fwd + bwd of the fp64 oracle over the first `rows` rows."""
+    """One step of the fp64 oracle over the first `rows` rows: forward, then
+    backward (a backward-only workload takes its statistics from the
+    oracle's forward, inside the step; a forward-only one stops there)."""
     from oracle import norm_bwd, norm_fwd
     sl = slice(0, rows)
     f = W.as_f64
@@ -447,8 +535,17 @@ def oracle_step(w, inp, rows):
     ref = norm_fwd(f(inp["x"][sl]), f(inp["bias"]), None if res is None else f(res[sl]),
                    f(inp["gamma"]), f(inp["beta"]), w.eps, w.mode, w.zero_centered_gamma,
                    w.dtype)
-    norm_bwd(f(inp["dy"][sl]), ref["sum"], f(inp["gamma"]), ref["mean"], ref["rstd"], w.mode,
-             w.zero_centered_gamma, w.dtype)
+    if w.backward:
+        norm_bwd(f(inp["dy"][sl]), ref["sum"], f(inp["gamma"]), ref["mean"], ref["rstd"],
+                 w.mode, w.zero_centered_gamma, w.dtype)
+
+
+def oracle_what(w) -> str:
+    if w.forward and w.backward:
+        return "fwd+bwd"
+    if w.forward:
+        return "fwd"
+    return "bwd (with the forward for its statistics)"
 
 
 def oracle_softmax_step(w, x, rows):
@@ -585,7 +682,7 @@ def run_reference(args, w, rank):
         oracle_any_step(w, inp, rows)
     el = time.perf_counter() - t0
     value = rows * args.steps / el
-    what = "softmax" if smx else ("normalize from partials" if is_partials(w) else "fwd+bwd")
+    what = "softmax" if smx else ("normalize from partials" if is_partials(w) else oracle_what(w))
     sample = f"first {rows} of {w.rows} rows per step, fp64 numpy oracle {what}, 1 thread"
     ms_step = 1000.0 * el / args.steps
     line = {
@@ -607,15 +704,21 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+def is_config(w) -> bool:
+    return w.name.split("@")[0] in CONFIG_WORKLOADS
+
+
 def metric_of(w):
     if is_softmax(w):
         return SOFTMAX_METRIC
     if is_partials(w):
         return PARTIALS_METRIC
+    if is_config(w):
+        return CONFIG_METRIC
     return METRIC
 
 
-def config_of(w, n):
+def config_of(w, n, copies=1):
     if is_softmax(w):
         return {"workload": w.name, "rows": w.rows, "hidden": w.hidden, "io_dtype": w.dtype,
                 "x_std": w.x_std, "mask_frac": w.mask_frac,
@@ -633,6 +736,18 @@ def config_of(w, n):
     if is_partials(w):
         c["partials"] = {"kind": "sum_sq", "tile_cols": W.PARTIALS_TILE_COLS,
                          "producer": "fp32 tile sums of the stored row, precomputed (stand-in)"}
+    if is_config(w):
+        c["calls"] = [k for k, on in (("ln_fwd", w.forward), ("ln_bwd", w.backward)) if on]
+        if not w.forward:
+            c["stats"] = "mean/rstd from one untimed ln_fwd of x (inputs of the backward)"
+        if w.zero_centered_gamma:
+            c["zero_centered_gamma"] = True
+    if copies > 1:
+        c["l2"] = (f"no flush: the steps cycle through {copies} copies of every buffer "
+                   f"({copies} x {step_bytes(w)} algorithmic bytes, at least 3x the L2), so "
+                   "each step reads inputs last touched 3 L2s of traffic earlier")
+        c["timing"] = ("the K steps captured in one CUDA graph and replayed (per-call means "
+                       "from graphs of K forwards and K backwards)")
     return c
 
 
@@ -650,11 +765,14 @@ def clock_record(sampler, t_warm0, t_host0, t_host1):
     return rec
 
 
-def time_fwd_bwd(nf, w, inp_host, device, args, world, sampler):
-    """Warm up, then time exactly K fused steps (ln_fwd + ln_bwd) between
-    barriers with CUDA events on the launching stream; per-kernel means from
-    events around each call."""
-    step = Step(nf, w, inp_host, device)
+def time_fwd_bwd(nf, w, inp_host, device, args, world, sampler, copies=1):
+    """Warm up, then time exactly K fused steps (ln_fwd + ln_bwd, or the one
+    call the workload has) between barriers with CUDA events on the launching
+    stream; per-kernel means from events around each call. copies > 1: the
+    steps cycle through that many buffer sets (RotatingStep)."""
+    step = (RotatingStep(nf, w, inp_host, device, copies) if copies > 1
+            else Step(nf, w, inp_host, device))
+    launches = step.launches()
     stream = torch.cuda.current_stream(device)
 
     def barrier():
@@ -692,6 +810,82 @@ def time_fwd_bwd(nf, w, inp_host, device, args, world, sampler):
     del step
     torch.cuda.empty_cache()
     return {"ms_step": elapsed / K, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "launches_per_step": launches,
+            "clocks": clock_record(sampler, t_warm0, t_host0, t_host1)}
+
+
+def time_fwd_bwd_graph(nf, w, inp_host, device, args, world, sampler, copies):
+    """The small configurations: their kernels take 10-20 us, less than the
+    host needs to issue a call through Python and ctypes, so an eager loop
+    would time the host. The K timed steps (cycling through `copies` buffer
+    sets) are captured into one CUDA graph and replayed once between
+    barriers, with CUDA events around the replay; for a forward + backward
+    step, K forwards alone and K backwards alone are captured and replayed
+    the same way for the per-call means."""
+    step = RotatingStep(nf, w, inp_host, device, copies)
+    launches = step.launches()
+    n = len(step.steps)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    torch.cuda.synchronize(device)
+    t_warm0 = time.time()
+    with torch.cuda.stream(side):   # eager warm-up: plans and kernel attributes
+        for _ in range(args.warmup):
+            step.fwd(side)
+            step.bwd(side)
+    torch.cuda.synchronize(device)
+
+    K = args.steps
+
+    def capture(do_fwd, do_bwd):
+        g = torch.cuda.CUDAGraph()
+        step.i = 0
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream(device)
+            for _ in range(K):
+                if do_fwd:
+                    step.steps[step.i].fwd(cs)
+                if do_bwd:
+                    step.steps[step.i].bwd(cs)
+                step.i = (step.i + 1) % n
+        return g
+
+    graphs = {"step": capture(True, True)}
+    if w.forward and w.backward:
+        graphs["fwd"] = capture(True, False)
+        graphs["bwd"] = capture(False, True)
+    stream = torch.cuda.current_stream(device)
+    times = {"fwd": 0.0, "bwd": 0.0}
+    t_host0 = t_host1 = None
+    for name in [k for k in ("fwd", "bwd") if k in graphs] + ["step"]:
+        g = graphs[name]
+        g.replay()                      # warm replay
+        torch.cuda.synchronize(device)
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize(device)
+        h0 = time.time()
+        a.record(stream)
+        g.replay()
+        z.record(stream)
+        torch.cuda.synchronize(device)
+        h1 = time.time()
+        barrier()
+        times[name] = max_over_ranks(a.elapsed_time(z), world, device)
+        if name == "step":
+            t_host0, t_host1 = h0, h1
+    if not (w.forward and w.backward):   # one call per step: the step is that call
+        times["fwd" if w.forward else "bwd"] = times["step"]
+    del graphs, step
+    torch.cuda.empty_cache()
+    return {"ms_step": times["step"] / K, "fwd_ms": times["fwd"] / K,
+            "bwd_ms": times["bwd"] / K, "launches_per_step": launches,
             "clocks": clock_record(sampler, t_warm0, t_host0, t_host1)}
 
 
@@ -699,9 +893,12 @@ def kernel_report(w, t):
     """Per-kernel algorithmic GB/s against the measured copy peak and the
     nominal 8 TB/s, and the roofline of the dominant kernel."""
     peak, peak_kind = measured_peak()
-    fb, bb = fwd_bytes(w), bwd_bytes(w)
+    fb = fwd_bytes(w) if w.forward else 0
+    bb = bwd_bytes(w) if w.backward else 0
+    calls = [c for c, on in ((("ln_fwd", t["fwd_ms"], fb), w.forward),
+                             (("ln_bwd", t["bwd_ms"], bb), w.backward)) if on]
     kernels = {}
-    for name, ms, by in (("ln_fwd", t["fwd_ms"], fb), ("ln_bwd", t["bwd_ms"], bb)):
+    for name, ms, by in calls:
         gbs = by / (ms * 1e-3) / 1e9
         kernels[name] = {"us": ms * 1e3, "algorithmic_bytes": by, "GBps": gbs,
                          f"frac_of_{peak_kind}": gbs / peak, "frac_of_8TBps": gbs / NOMINAL_HBM_GBS,
@@ -725,10 +922,14 @@ def run_ours(args, w, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     inp_host = W.make_inputs(w, seed=0)
+    copies = rotation_copies(w, l2_bytes(device))
     sampler = ClockSampler(local_rank) if (rank == 0 and not args.no_clocks) else None
     if sampler is not None:
         time.sleep(0.3)
-    t = time_fwd_bwd(nf, w, inp_host, device, args, world, sampler)
+    if copies > 1:
+        t = time_fwd_bwd_graph(nf, w, inp_host, device, args, world, sampler, copies)
+    else:
+        t = time_fwd_bwd(nf, w, inp_host, device, args, world, sampler)
 
     # the second gate shape, same steps and warm-up (default workload only)
     extra = {}
@@ -741,7 +942,7 @@ def run_ours(args, w, rank, world, local_rank):
         extra[w2.name] = {
             "value": replica_throughput(w2.rows, world, t2["ms_step"]), "unit": "rows/s",
             "ms_per_step": t2["ms_step"], "config": config_of(w2, world), "roofline": r2,
-            "kernels": k2, "step_GBps": g2, "gpu_launches": 3 * args.steps,
+            "kernels": k2, "step_GBps": g2, "gpu_launches": t2["launches_per_step"] * args.steps,
             "clocks": t2["clocks"]}
     if sampler is not None:
         time.sleep(0.05)
@@ -758,16 +959,17 @@ def run_ours(args, w, rank, world, local_rank):
     kernels, roofline, step_gbs = kernel_report(w, t)
     cpu = cpu_all = None
     if not args.no_cpu_baseline and world == 1:
-        cpu, cpu_all = cpu_baselines(w, inp_host, "fwd+bwd")
+        cpu, cpu_all = cpu_baselines(w, inp_host, oracle_what(w))
     K = args.steps
     line = {
-        "metric": METRIC, "value": replica_throughput(w.rows, world, t["ms_step"]),
+        "metric": metric_of(w), "value": replica_throughput(w.rows, world, t["ms_step"]),
         "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": t["ms_step"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config_of(w, world),
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(w, world, copies),
         "roofline": roofline, "kernels": kernels, "step_GBps": step_gbs,
         "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all, "e2e": e2e,
-        "gpu_launches": 3 * K, "clocks": t["clocks"], "impl": "ours",
+        "gpu_launches": t["launches_per_step"] * K, "clocks": t["clocks"], "impl": "ours",
     }
     if extra:
         line["workloads"] = extra
@@ -936,7 +1138,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(BENCH_WORKLOADS) + sorted(SOFTMAX_WORKLOADS)
-                    + sorted(PARTIALS_WORKLOADS),
+                    + sorted(PARTIALS_WORKLOADS) + sorted(CONFIG_WORKLOADS),
                     default=W.BENCH_LN_BF16_576000x384.name)
     ap.add_argument("--rows", type=int, default=None,
                     help="override the workload's row count (smaller profiling captures)")
@@ -951,7 +1153,7 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = (BENCH_WORKLOADS.get(args.workload) or SOFTMAX_WORKLOADS.get(args.workload)
-         or PARTIALS_WORKLOADS[args.workload])
+         or PARTIALS_WORKLOADS.get(args.workload) or CONFIG_WORKLOADS[args.workload])
     if args.rows is not None:
         w = w.with_(rows=args.rows, name=f"{w.name}@rows={args.rows}")
 

@@ -168,18 +168,24 @@ __device__ __forceinline__ int partial_offset(const BwdArgs& a, int which) {
 
 // Partials of a lane-group kernel: W warps, each with 32 / LANES groups that
 // hold the same columns. Groups of a warp are added by a fixed butterfly,
-// then the warps through shared memory in warp order, one vector slot at a
-// time. Slot k covers columns [k * LANES * VEC, (k + 1) * LANES * VEC). All
-// threads of the CTA call this (threads of warps >= W only pass barriers).
-// Accumulators: 0 = dgamma, 1 = dbeta (LayerNorm), 2 = dbias (kBias).
+// then the warps through shared memory in warp order. Slot k of a warp covers
+// columns [k * LANES * VEC, (k + 1) * LANES * VEC). When `buf` (the ring's
+// slots, idle once the pipeline has drained) holds every warp's N slots, a
+// sum goes through it in one step, two barriers per sum; otherwise one slot
+// at a time through `red` (two barriers per slot and sum). Both add the same
+// values in the same order. All threads of the CTA call this (threads of
+// warps >= W only pass barriers). Accumulators: 0 = dgamma, 1 = dbeta
+// (LayerNorm), 2 = dbias (kBias).
 template <typename T, int LANES, int N, int W, bool kRms, bool kBias>
 __device__ __forceinline__ void store_group_partials(const BwdArgs& a,
                                                      float (&acc_g)[N][Vec<T>::N],
                                                      float (&acc_b)[N][Vec<T>::N],
                                                      float (&acc_d)[N][Vec<T>::N],
-                                                     float (*red)[LANES * Vec<T>::N]) {
+                                                     float (*red)[LANES * Vec<T>::N],
+                                                     float* buf, size_t buf_bytes) {
   constexpr int VEC = Vec<T>::N;
   constexpr int SLOT = LANES * VEC;
+  constexpr int NS = N * SLOT;   // columns a warp holds
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int sub = lane / LANES;
@@ -199,10 +205,30 @@ __device__ __forceinline__ void store_group_partials(const BwdArgs& a,
   }
   const int H = a.hidden;
   float* ws = a.ws + (int64_t)blockIdx.x * a.ws_cols;
+  const bool whole = (size_t)W * NS * sizeof(float) <= buf_bytes;
   for (int which = 0; which < 3; ++which) {
     if (which == 1 && (kRms || rms)) continue;
     if (which == 2 && !kBias) continue;
     const int off = partial_offset(a, which);
+    if (whole) {
+      if (warp < W && sub == 0) {
+#pragma unroll
+        for (int k = 0; k < N; ++k)
+#pragma unroll
+          for (int e = 0; e < VEC; ++e)
+            buf[warp * NS + k * SLOT + l * VEC + e] =
+                which == 0 ? acc_g[k][e] : (which == 1 ? acc_b[k][e] : acc_d[k][e]);
+      }
+      __syncthreads();
+      for (int col = threadIdx.x; col < H; col += blockDim.x) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) t += buf[w * NS + col];
+        ws[off + col] = t;
+      }
+      __syncthreads();
+      continue;
+    }
 #pragma unroll
     for (int k = 0; k < N; ++k) {
       if (warp < W && sub == 0) {
@@ -253,26 +279,49 @@ __device__ __forceinline__ void store_thread_partials(const BwdArgs& a, int t,
 
 // Partials of a row-group kernel: 256 / G groups of G threads (G = 64 or
 // 128), thread t of every group holding the same columns (vectors k * G + t).
-// The groups are added through shared memory in group order, one vector slot
-// (G * VEC columns) at a time. All threads of the CTA call this.
+// The groups are added through shared memory in group order: through `buf`
+// (the drained ring's slots) in one step per sum when it holds every group's
+// N slots, else one vector slot (G * VEC columns) at a time through `red`;
+// the same values in the same order either way. All threads of the CTA call
+// this.
 template <typename T, int G, int N, bool kRms, bool kBias>
 __device__ __forceinline__ void store_rowgroup_partials(const BwdArgs& a,
                                                         float (&acc_g)[N][Vec<T>::N],
                                                         float (&acc_b)[N][Vec<T>::N],
                                                         float (&acc_d)[N][Vec<T>::N],
-                                                        float (*red)[G * Vec<T>::N]) {
+                                                        float (*red)[G * Vec<T>::N],
+                                                        float* buf, size_t buf_bytes) {
   constexpr int VEC = Vec<T>::N;
   constexpr int SLOT = G * VEC;
+  constexpr int NS = N * SLOT;   // columns a group holds
   constexpr int NG = kBulkThreads / G;
   const int grp = threadIdx.x / G;
   const int t = threadIdx.x % G;
   const bool rms = kRms || a.rms;
   const int H = a.hidden;
   float* ws = a.ws + (int64_t)blockIdx.x * a.ws_cols;
+  const bool whole = (size_t)NG * NS * sizeof(float) <= buf_bytes;
   for (int which = 0; which < 3; ++which) {
     if (which == 1 && rms) continue;
     if (which == 2 && !kBias) continue;
     const int off = partial_offset(a, which);
+    if (whole) {
+#pragma unroll
+      for (int k = 0; k < N; ++k)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+          buf[grp * NS + k * SLOT + t * VEC + e] =
+              which == 0 ? acc_g[k][e] : (which == 1 ? acc_b[k][e] : acc_d[k][e]);
+      __syncthreads();
+      for (int col = threadIdx.x; col < H; col += kBulkThreads) {
+        float s = 0.f;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) s += buf[g * NS + col];
+        ws[off + col] = s;
+      }
+      __syncthreads();
+      continue;
+    }
 #pragma unroll
     for (int k = 0; k < N; ++k) {
 #pragma unroll
@@ -364,7 +413,11 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_warp_kernel(const Bw
   unpair_acc<T, N>(acc_g, fg);
   unpair_acc<T, N>(acc_b, fb);
   unpair_acc<T, N>(acc_d, fd);
-  store_group_partials<T, LANES, N, kConsumerWarps, kRms, kBias>(a, fg, fb, fd, red);
+  // The ring's slots are idle now: every issued copy has landed and been
+  // consumed (an aborted pipeline returned above).
+  store_group_partials<T, LANES, N, kConsumerWarps, kRms, kBias>(
+      a, fg, fb, fd, red, reinterpret_cast<float*>(ring.base),
+      (size_t)ring.stages * ring.slot_bytes);
 }
 
 // Whether the CTA-per-row backward keeps w in registers: its accumulators
@@ -457,7 +510,9 @@ __global__ void __launch_bounds__(kBulkThreads, 2) bwd_bulk_group_kernel(const B
   unpair_acc<T, N>(acc_g, fg);
   unpair_acc<T, N>(acc_b, fb);
   unpair_acc<T, N>(acc_d, fd);
-  store_rowgroup_partials<T, G, N, kRms, kBias>(a, fg, fb, fd, red);
+  store_rowgroup_partials<T, G, N, kRms, kBias>(a, fg, fb, fd, red,
+                                                reinterpret_cast<float*>(ring.base),
+                                                (size_t)ring.stages * ring.slot_bytes);
 }
 
 template <typename T, int N, bool kRms, bool kBias>

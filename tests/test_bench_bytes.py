@@ -61,3 +61,35 @@ def test_softmax_bytes():
 def test_replica_throughput_counts_every_rank():
     # whole-job rows/s: every replica's rows over the slowest rank's step time
     assert bench.replica_throughput(1000, 4, 2.0) == 4 * 1000 / 2e-3
+
+
+def test_step_bytes_and_rotation():
+    l2 = 129_000_000
+    # every [rows, hidden] tensor larger than L2: no rotation
+    assert bench.rotation_copies(W.BENCH_LN_BF16_576000x384, l2) == 1
+    assert bench.rotation_copies(W.BWD_BF16_576000x384_LN, l2) == 1
+    assert bench.rotation_copies(W.BENCH_RMS_BF16_16384x8192, l2) == 1
+    # smaller ones cycle through enough buffer sets to move 3 L2s per pass
+    for w in (W.LN_F32_4096x384, W.FWD_AMAX_BF16_32768x768, *W.UNET_F16.values()):
+        n = bench.rotation_copies(w, l2)
+        assert n >= 2 and n * bench.step_bytes(w) >= 3 * l2, (w.name, n)
+        assert n == 2 or (n - 1) * bench.step_bytes(w) < 3 * l2, (w.name, n)
+    # one-direction workloads count only the call they make
+    w = W.FWD_AMAX_BF16_32768x768
+    assert bench.step_bytes(w) == bench.fwd_bytes(w)
+    w = W.BWD_BF16_576000x384_RMS
+    assert bench.step_bytes(w) == bench.bwd_bytes(w)
+    w = W.LN_F32_4096x384
+    assert bench.step_bytes(w) == bench.fwd_bytes(w) + bench.bwd_bytes(w)
+
+
+def test_every_configuration_has_a_bench_line_and_an_oracle_step():
+    names = set(bench.BENCH_WORKLOADS) | set(bench.CONFIG_WORKLOADS)
+    for w in (W.LN_F32_4096x384, W.BWD_BF16_576000x384_LN, W.BWD_BF16_576000x384_RMS,
+              W.FWD_AMAX_BF16_32768x768, *W.UNET_F16.values(), W.BENCH_RMS_BF16_16384x8192,
+              W.BENCH_LN_BF16_576000x384):
+        assert w.name in names, w.name
+    for w in bench.CONFIG_WORKLOADS.values():
+        small = w.with_(rows=4)
+        bench.oracle_step(small, W.make_inputs(small, seed=0), 4)
+        assert bench.metric_of(w) == bench.CONFIG_METRIC
