@@ -815,9 +815,9 @@ def time_fwd_bwd(nf, w, inp_host, device, args, world, sampler, copies=1):
 
 
 def time_fwd_bwd_graph(nf, w, inp_host, device, args, world, sampler, copies):
-    """The small configurations: their kernels take 10-20 us, less than the
-    host needs to issue a call through Python and ctypes, so an eager loop
-    would time the host. The K timed steps (cycling through `copies` buffer
+    """The configurations whose buffers fit in L2: their calls take 6-40 us,
+    about what the host needs to issue a call through Python and ctypes, so
+    an eager loop would time the host. The K timed steps (cycling through `copies` buffer
     sets) are captured into one CUDA graph and replayed once between
     barriers, with CUDA events around the replay; for a forward + backward
     step, K forwards alone and K backwards alone are captured and replayed
