@@ -156,7 +156,8 @@ WIDE = [("bf16", 2056, W.LAYERNORM), ("bf16", 4096, W.RMSNORM), ("bf16", 6144, W
         ("f32", 3072, W.RMSNORM),
         # one row group per CTA for rows of more than 1024 vectors
         ("bf16", 10240, W.RMSNORM), ("bf16", 12288, W.LAYERNORM), ("f16", 16384, W.RMSNORM),
-        ("bf16", 16384, W.LAYERNORM), ("f32", 8192, W.LAYERNORM), ("bf16", 9000, W.RMSNORM)]
+        ("bf16", 16384, W.LAYERNORM), ("f32", 8192, W.LAYERNORM), ("bf16", 9000, W.RMSNORM),
+        ("bf16", 14336, W.LAYERNORM), ("f16", 16384, W.LAYERNORM)]
 
 
 @pytest.mark.parametrize("dtype,hidden,mode", WIDE, ids=lambda v: str(v))
@@ -187,7 +188,8 @@ def test_wide_rows_many_rows_per_cta(cuda_lib, dtype, hidden, mode, dbias):
     (3001, 8192, W.RMSNORM, False),       # register CTA-per-row backward
     (2001, 3072, W.LAYERNORM, True),      # the same with zero-centered gamma
     (3001, 8192, W.LAYERNORM, False),     # dbeta summed in shared memory
-], ids=["ln384", "rms8192", "ln3072zc", "ln8192"])
+    (1001, 16384, W.LAYERNORM, False),    # one 512-thread row group per CTA
+], ids=["ln384", "rms8192", "ln3072zc", "ln8192", "ln16384"])
 def test_backward_is_deterministic(cuda_lib, rows, hidden, mode, zc):
     w = wl("bf16", rows, hidden, mode, zero_centered_gamma=zc)
     inp = make_inputs(w, seed=3)

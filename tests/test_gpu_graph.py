@@ -44,6 +44,7 @@ def _with_partials(inp):
     W.BENCH_RMS_BF16_16384x8192.with_(name="rms_bf16_x1536", hidden=1536),
     W.BENCH_LN_BF16_576000x384.with_(name="ln_bf16_x2560", hidden=2560),
     W.BENCH_LN_BF16_576000x384.with_(name="ln_bf16_x12288", hidden=12288),
+    W.BENCH_LN_BF16_576000x384.with_(name="ln_bf16_x16384", hidden=16384),
 ], ids=lambda w: w.name)
 def test_fwd_bwd_softmax_replay_in_a_cuda_graph(cuda_lib, base):
     nf = cuda_lib
