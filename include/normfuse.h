@@ -29,7 +29,8 @@
  *    thread. No entry point aborts, throws or prints.
  *  - Limits: rows >= 0; 1 <= hidden <= LN_MAX_HIDDEN_VEC16 (bf16/fp16) or
  *    LN_MAX_HIDDEN_VEC32 (fp32) on the vectorised path, and
- *    1 <= hidden <= LN_MAX_HIDDEN_SCALAR on the scalar path.
+ *    1 <= hidden <= LN_MAX_HIDDEN_SCALAR on the scalar path. Element
+ *    offsets are 64-bit: rows * hidden may exceed 2^31 (tensors past 4 GiB).
  *
  * Citations are to the four pages the method comes from: NVIDIA/cutlass
  * discussion 874 (GEMM -> residual add -> LayerNorm), iree-org/iree issue
