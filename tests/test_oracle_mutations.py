@@ -6,7 +6,9 @@ below run against the mutated copy. Every mutation must fail at least one
 pin; the unmutated oracle must pass all of them. The pins do not reuse the
 oracle's arithmetic: torch's fp64 layer_norm and autograd, the RMSNorm
 formula written out, the stored sum formed here, a constant row's closed
-form, and amax of the rounded output; for the softmax, torch's fp64 softmax
+form, and amax of the rounded output; for the rounding helpers, numpy's
+fp16/fp32 casts, torch's bf16 and E4M3 casts and a constructed FP8 tie; for
+the softmax, torch's fp64 softmax
 on rows whose logits sit far above and below zero, and fully masked rows.
 (The partials oracle has its own planted-slip test in test_oracle_partials.)
 """
@@ -229,3 +231,102 @@ def test_the_softmax_oracle_passes_every_pin():
 @pytest.mark.parametrize("name,old,new", SMX_MUTATIONS, ids=[m[0] for m in SMX_MUTATIONS])
 def test_each_planted_softmax_slip_fails_a_pin(name, old, new):
     assert _smx_failures(smx_mutated(old, new)), f"no pin caught: {name}"
+
+
+# ---- the rounding helpers of the norm oracle ----------------------------------
+
+ROUND_MUTATIONS = [
+    ("ties away from zero", "r = np.ldexp(np.rint(q), quantum_exp)",
+     "r = np.ldexp(np.sign(q) * np.floor(np.abs(q) + 0.5), quantum_exp)"),
+    ("no subnormal grid", "e = np.maximum(E - 1, emin)", "e = E - 1"),
+    ("one bit short", "quantum_exp = e - (p - 1)", "quantum_exp = e - p"),
+    ("overflow kept finite",
+     "r = np.where(np.abs(r) > max_finite, np.copysign(np.inf, vf), r)", "r = r"),
+    ("E4M3 without saturation", "r = np.clip(r, -E4M3_MAX, E4M3_MAX)", "r = r"),
+    ("E4M3 without subnormals", "e = np.maximum(E - 1, -6)", "e = E - 1"),
+    ("FP8 product kept in fp64",
+     'prod = round_to_format(np.asarray(y_stored, dtype=np.float64) *\n'
+     '                           float(np.float32(scale)), "f32")',
+     'prod = np.asarray(y_stored, dtype=np.float64) * float(np.float32(scale))'),
+]
+
+
+def _round_values():
+    rng = np.random.default_rng(4)
+    v = np.concatenate([
+        rng.standard_normal(2000) * np.exp2(rng.integers(-30, 30, 2000)),
+        [1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, 1 + 2.0 ** -24, -(1 + 2.0 ** -24),   # ties
+         2.0 ** -20, 3.1e-5, 2.0 ** -140, 7e-46,                               # subnormal ranges
+         70000.0, 3.5e38, -1e39]])                                            # past the maxima
+    return v
+
+
+def rnd_pin_numpy_casts(M):
+    v = _round_values()
+    with np.errstate(over="ignore"):
+        assert np.array_equal(M.round_to_format(v, "f16"), v.astype(np.float16).astype(np.float64))
+        assert np.array_equal(M.round_to_format(v, "f32"), v.astype(np.float32).astype(np.float64))
+
+
+def rnd_pin_bf16_torch(M):
+    v32 = _round_values().astype(np.float32)
+    v32 = v32[np.isfinite(v32)]
+    ref = torch.tensor(v32).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(M.round_to_format(v32.astype(np.float64), "bf16"), ref)
+
+
+def rnd_pin_e4m3(M):
+    rng = np.random.default_rng(5)
+    v = np.concatenate([rng.uniform(-448, 448, 3000), rng.uniform(-1, 1, 1000) * 2.0 ** -7,
+                        [2.0 ** -9, 3 * 2.0 ** -10, 0.0]])
+    ref = torch.tensor(v, dtype=torch.float32).to(torch.float8_e4m3fn).double().numpy()
+    got = M.round_to_e4m3_satfinite(v.astype(np.float32).astype(np.float64))
+    assert np.array_equal(got, ref)
+    big = np.array([449.0, 480.0, 1e6, -1e6, np.inf, -np.inf])
+    assert np.array_equal(M.round_to_e4m3_satfinite(big), np.sign(big) * 448.0)
+
+
+def _fp32_tie_case():
+    """A bf16 y and an fp32 scale whose exact product lies just above the
+    E4M3 tie 1.0625 (between 1 and 1.125) while its fp32 rounding is the tie
+    itself, which rounds to even (1.0): the fp32 product decides."""
+    for k in range(1, 128):
+        y0 = 1.0 + k / 128.0                      # bf16 values in (1, 2)
+        sc = float(np.float32(1.0625 / y0))
+        exact = y0 * sc
+        if exact > 1.0625 and float(np.float32(exact)) == 1.0625:
+            return y0, sc
+    raise AssertionError("no tie case found")
+
+
+def rnd_pin_fp8_product(M):
+    rng = np.random.default_rng(6)
+    y = M.round_to_format(rng.standard_normal(4000), "bf16")
+    scale = 37.3
+    prod = torch.tensor(y, dtype=torch.float32) * torch.tensor(scale, dtype=torch.float32)
+    ref = prod.clamp(-448, 448).to(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(M.quantize_fp8_e4m3(y, scale), ref)
+    y0, sc = _fp32_tie_case()
+    assert M.quantize_fp8_e4m3(np.array([y0]), sc)[0] == 1.0
+
+
+ROUND_PINS = [rnd_pin_numpy_casts, rnd_pin_bf16_torch, rnd_pin_e4m3, rnd_pin_fp8_product]
+
+
+def _round_failures(M):
+    failed = []
+    for pin in ROUND_PINS:
+        try:
+            pin(M)
+        except Exception:
+            failed.append(pin.__name__)
+    return failed
+
+
+def test_the_rounding_helpers_pass_every_pin():
+    assert _round_failures(R) == []
+
+
+@pytest.mark.parametrize("name,old,new", ROUND_MUTATIONS, ids=[m[0] for m in ROUND_MUTATIONS])
+def test_each_planted_rounding_slip_fails_a_pin(name, old, new):
+    assert _round_failures(mutated(old, new)), f"no pin caught: {name}"
